@@ -1,0 +1,475 @@
+/*
+ * sv_oracle.c -- float64 CPU oracle for batched speculative-decoding verification.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, obviously-correct implementation
+ * that the CUDA library is checked against.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load it; the library never does.  It shares no code, header,
+ * table or helper with the CUDA path.
+ *
+ * Sources (page title, section):
+ *  [R1] "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust",
+ *       section "The Memory Bandwidth Wall and Speculative Math": accept x_i with probability
+ *       min(1, p(x_i)/q(x_i)); at the first rejection discard the rest and draw from
+ *       max(0, p - q) / sum max(0, p - q).
+ *  [R2] same page, section "The Verification Algorithm": target probabilities are
+ *       softmax(logits / temperature) over all K+1 rows; the loop stops at the first
+ *       rejection; if every draft is accepted the extra token is drawn from row K.
+ *  [R3] same page, section "Orchestrating the Inference Loop": the target appended K+1
+ *       rows and keeps 1 + accepted of them (target_len = current - (K+1) + 1 + accepted);
+ *       section "KV Cache Rollback Mechanics": rolling back forward is an error.
+ *  [A1] "Adding Speculative Decoding", table "The existing base": greedy verification
+ *       accepts while draft == argmax and the extra token is the argmax at the first
+ *       mismatch; section "Verification and sampling" item 2: greedy is the degenerate
+ *       (one-hot draft) case of the uniform-vs-ratio test.
+ *  [F1] FreeToken PR #836, section "Design": every verify row samples with its own
+ *       request's temperature, top-k, top-p and greedy flag; presence and frequency
+ *       penalties count the drafts before a row as already generated.
+ *  [S2] "Speculative Decoding: Draft Model Sampling, Rejection Sampling & On-Device
+ *       Acceleration", Key Topic 2 and Section 2: the same accept/residual formulas.
+ *
+ * Readings where the pages leave a step open (each one is also listed in the design notes):
+ *  - accept iff u < min(1, p/q) with no epsilon in the denominator; q == 0 < p accepts,
+ *    p == 0 always rejects.
+ *  - penalties are additive: z_v = logit_v - presence*[c_v > 0] - frequency*c_v, where c_v
+ *    counts v among d_0..d_{i-1}; they apply before temperature and filtering, greedy rows too.
+ *  - top-k keeps every token whose scaled logit is >= the k-th largest (ties kept); k <= 0 or
+ *    k >= V disables it.  top-p then keeps v iff the renormalised mass of tokens strictly
+ *    more likely than v is < top_p; top_p >= 1 disables it.  The kept set is renormalised.
+ *  - inverse CDF in token-index order: the smallest v whose running sum exceeds u * W;
+ *    if rounding leaves none, the largest v with positive weight.
+ *  - a residual with W == 0 falls back to drawing from p.
+ *  - uniforms: slot 0 of row i is the accept test of draft i; slot 1 of the final row is
+ *    the residual or extra-token draw.
+ *  - greedy argmax breaks ties toward the lowest token id; greedy rows read neither q nor u.
+ *
+ * Near-tie bookkeeping (decisions whose float64 value lies within 1e-5 of a boundary, where
+ * an fp32 implementation may legitimately decide the other way) is reported per request.
+ *
+ * Parity pins: tests/test_oracle_*.py check this file against closed forms, the pages'
+ * worked examples, brute force on tiny vocabularies and a Monte Carlo distribution test.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define NEAR_TOL 1e-5
+#define NEAR_W 1e-6
+
+typedef struct sv_oracle_batch {
+    int32_t B, k_max, V, total_rows;
+    int32_t logits_bf16;          /* 1: target_logits holds bf16 bit patterns (uint16) */
+    const void *target_logits;    /* [total_rows, V] */
+    const float *draft_probs;     /* [total_rows - B, V] */
+    const int32_t *draft_tokens;  /* [total_rows - B] */
+    const int32_t *num_drafts;    /* [B] */
+    const int32_t *row_offsets;   /* [B+1], or NULL: request b owns rows b*(k_max+1) .. */
+    const float *temperature;     /* [B] */
+    const int32_t *top_k;         /* [B] */
+    const float *top_p;           /* [B] */
+    const float *presence;        /* [B] or NULL */
+    const float *frequency;       /* [B] or NULL */
+    const uint8_t *greedy;        /* [B] */
+    const float *uniforms;        /* [total_rows, 2] */
+} sv_oracle_batch;
+
+typedef struct sv_oracle_diag {
+    int32_t decisions;  /* accept tests + draws + greedy argmaxes + filter thresholds on the path */
+    int32_t near_ties;  /* decisions within the near-tie band */
+    int32_t error;      /* 0, or the device-data error code of the request */
+    int32_t reserved;
+} sv_oracle_diag;
+
+enum { E_OK = 0, E_LAYOUT = 1, E_TOKEN = 2, E_TEMP = 3, E_TOPP = 4, E_UNIFORM = 5, E_PENALTY = 6 };
+
+/* ---------------------------------------------------------------------------------- */
+
+static double logit_at(const sv_oracle_batch *in, int64_t row, int32_t v) {
+    int64_t off = row * (int64_t)in->V + v;
+    if (in->logits_bf16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)in->target_logits)[off] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)in->target_logits)[off];
+}
+
+static int64_t row_start(const sv_oracle_batch *in, int32_t b) {
+    return in->row_offsets ? (int64_t)in->row_offsets[b] : (int64_t)b * (in->k_max + 1);
+}
+
+/* Checks the request's layout and the inputs its path reads; returns an error code. */
+static int check_request(const sv_oracle_batch *in, int32_t b) {
+    int32_t k = in->num_drafts[b];
+    int64_t r0 = row_start(in, b);
+    int64_t cap;
+    if (in->row_offsets) {
+        int64_t r1 = in->row_offsets[b + 1];
+        if (r0 < 0 || r1 > in->total_rows || r1 <= r0) return E_LAYOUT;
+        cap = r1 - r0 - 1;
+    } else {
+        cap = in->k_max;
+        if ((int64_t)(b + 1) * (in->k_max + 1) > in->total_rows) return E_LAYOUT;
+    }
+    if (k < 0 || k > in->k_max || k > cap) return E_LAYOUT;
+    int64_t d0 = r0 - b;
+    for (int32_t i = 0; i < k; i++) {
+        int32_t d = in->draft_tokens[d0 + i];
+        if (d < 0 || d >= in->V) return E_TOKEN;
+    }
+    if (in->presence && !isfinite(in->presence[b])) return E_PENALTY;
+    if (in->frequency && !isfinite(in->frequency[b])) return E_PENALTY;
+    if (!in->greedy[b]) {
+        float T = in->temperature[b];
+        if (!(T > 0.0f) || !isfinite(T)) return E_TEMP;
+        float P = in->top_p[b];
+        if (!(P > 0.0f && P <= 1.0f)) return E_TOPP;
+        for (int32_t i = 0; i <= k; i++)
+            for (int s = 0; s < 2; s++) {
+                float u = in->uniforms[(r0 + i) * 2 + s];
+                if (!(u >= 0.0f && u < 1.0f)) return E_UNIFORM;
+            }
+    }
+    return E_OK;
+}
+
+/* z_v for row i of request b: the logit minus the presence/frequency penalty of the drafts
+ * d_0..d_{i-1} [F1].  Returns 1 when some token of the row carries a nonzero penalty. */
+static int row_logits(const sv_oracle_batch *in, int32_t b, int32_t i, double *z) {
+    int64_t row = row_start(in, b) + i;
+    for (int32_t v = 0; v < in->V; v++) z[v] = logit_at(in, row, v);
+    double pres = in->presence ? in->presence[b] : 0.0;
+    double freq = in->frequency ? in->frequency[b] : 0.0;
+    if (i == 0 || (pres == 0.0 && freq == 0.0)) return 0;
+    const int32_t *d = in->draft_tokens + (row_start(in, b) - b);
+    int penalised = 0;
+    for (int32_t j = 0; j < i; j++) {
+        int32_t v = d[j];
+        int seen = 0;
+        for (int32_t t = 0; t < j; t++) seen |= (d[t] == v);
+        if (seen) continue;             /* apply once per distinct token */
+        int32_t c = 0;
+        for (int32_t t = 0; t < i; t++) c += (d[t] == v);
+        double pen = pres * (c > 0 ? 1.0 : 0.0) + freq * (double)c;
+        z[v] -= pen;
+        if (pen != 0.0) penalised = 1;
+    }
+    return penalised;
+}
+
+static int cmp_desc(const void *a, const void *b) {
+    double x = *(const double *)a, y = *(const double *)b;
+    return (x < y) - (x > y);
+}
+
+static int close_rel(double a, double b) {
+    double s = fabs(a) > 1.0 ? fabs(a) : 1.0;
+    return fabs(a - b) <= NEAR_TOL * s;
+}
+
+/* Greedy row [A1]: the argmax of z with ties to the lowest id.  *near is set when the row
+ * carries penalties and the runner-up is within the near-tie band of the maximum. */
+static int32_t row_argmax(const double *z, int32_t V, int penalised, int *near) {
+    int32_t best = 0;
+    for (int32_t v = 1; v < V; v++)
+        if (z[v] > z[best]) best = v;
+    *near = 0;
+    if (penalised) {
+        for (int32_t v = 0; v < V; v++)
+            if (v != best && close_rel(z[best], z[v]) && z[v] != z[best]) *near = 1;
+    }
+    return best;
+}
+
+/* Sampled row [R2][F1]: p = softmax(z / T) restricted to top-k, then to top-p, renormalised.
+ * Writes p[0..V).  *decisions/*near count the filter thresholds of the row.  Returns the
+ * number of tokens kept. */
+static int32_t row_probs(const sv_oracle_batch *in, int32_t b, const double *z, int penalised,
+                         double *p, double *scratch, int *decisions, int *near) {
+    const int32_t V = in->V;
+    const double T = in->temperature[b];
+    const int32_t K = in->top_k[b];
+    const double P = in->top_p[b];
+    double *zs = scratch; /* V doubles */
+
+    for (int32_t v = 0; v < V; v++) p[v] = z[v] / T;          /* p[] holds z' for now */
+    double m = p[0];
+    for (int32_t v = 1; v < V; v++) if (p[v] > m) m = p[v];
+
+    /* top-k threshold: the K-th largest scaled logit, ties kept */
+    double tau = -INFINITY;
+    if (K > 0 && K < V) {
+        memcpy(zs, p, sizeof(double) * V);
+        qsort(zs, V, sizeof(double), cmp_desc);
+        tau = zs[K - 1];
+        (*decisions)++;
+        if (penalised) {
+            for (int32_t j = K; j < V; j++)
+                if (zs[j] < tau) { if (close_rel(tau, zs[j])) (*near)++; break; }
+        }
+    }
+    /* unnormalised weights of the top-k set */
+    double ZK = 0.0;
+    for (int32_t v = 0; v < V; v++) ZK += (p[v] >= tau) ? exp(p[v] - m) : 0.0;
+
+    /* top-p: walk distinct values from the largest; a value is kept while the mass strictly
+     * above it is < top_p (in units of the top-k mass) */
+    if (P < 1.0) {
+        int32_t n = 0;
+        for (int32_t v = 0; v < V; v++) if (p[v] >= tau) zs[n++] = p[v];
+        qsort(zs, n, sizeof(double), cmp_desc);
+        double above = 0.0, last_kept = zs[0], above_last_kept = 0.0;
+        int32_t j = 0;
+        int have_excl = 0;
+        double above_excl = 0.0, first_excl = 0.0;
+        while (j < n) {
+            double level = zs[j];
+            int32_t c = 0;
+            while (j + c < n && zs[j + c] == level) c++;
+            if (above / ZK < P) {
+                last_kept = level;
+                above_last_kept = above;
+                above += (double)c * exp(level - m);
+                j += c;
+            } else {
+                have_excl = 1;
+                above_excl = above;
+                first_excl = level;
+                break;
+            }
+        }
+        (*decisions)++;
+        int nt = fabs(above_last_kept / ZK - P) < NEAR_TOL;
+        if (have_excl) {
+            nt |= fabs(above_excl / ZK - P) < NEAR_TOL;
+            if (penalised) nt |= close_rel(last_kept, first_excl);
+        }
+        if (nt) (*near)++;
+        tau = last_kept;
+    }
+    double Z = 0.0;
+    int32_t kept = 0;
+    for (int32_t v = 0; v < V; v++) {
+        if (p[v] >= tau) { Z += exp(p[v] - m); kept++; }
+    }
+    for (int32_t v = 0; v < V; v++) p[v] = (p[v] >= tau) ? exp(p[v] - m) / Z : 0.0;
+    return kept;
+}
+
+/* Inverse CDF over w[0..V) in token-index order [R1]: the smallest v whose running sum is
+ * > u * W, where W is the running sum's total; the largest positive-weight v if rounding
+ * leaves none.  *near is set when the running sum at the boundary is within 1e-5 (of W)
+ * of u * W. */
+static int32_t inverse_cdf(const double *w, int32_t V, double u, int *near) {
+    double W = 0.0;
+    for (int32_t v = 0; v < V; v++) W += w[v];
+    double target = u * W, c = 0.0;
+    *near = 0;
+    for (int32_t v = 0; v < V; v++) {
+        double prev = c;
+        c += w[v];
+        if (c > target) {
+            if (fabs(prev / W - u) < NEAR_TOL || fabs(c / W - u) < NEAR_TOL) *near = 1;
+            return v;
+        }
+    }
+    for (int32_t v = V - 1; v >= 0; v--)
+        if (w[v] > 0.0) { *near = 1; return v; }
+    *near = 1;
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* one request                                                                          */
+
+static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, int32_t *acc,
+                       double *out_pq, uint8_t *pq_near, sv_oracle_diag *dg,
+                       double *z, double *p, double *r, double *scratch) {
+    const int32_t V = in->V;
+    const int32_t kmax1 = in->k_max + 1;
+    for (int32_t j = 0; j < kmax1; j++) out_tok[(int64_t)b * kmax1 + j] = -1;
+    sv_oracle_diag d = {0, 0, 0, 0};
+    int err = check_request(in, b);
+    const int64_t r0 = row_start(in, b), d0 = r0 - b;
+    const int32_t k = in->num_drafts[b];
+    if (err) {
+        acc[b] = -1;
+        if (out_pq && k >= 0 && k <= in->k_max && d0 >= 0)
+            for (int32_t i = 0; i < k && d0 + i < in->total_rows - in->B; i++) {
+                out_pq[(d0 + i) * 2] = NAN;
+                out_pq[(d0 + i) * 2 + 1] = NAN;
+            }
+        d.error = err;
+        if (dg) dg[b] = d;
+        return;
+    }
+    const int32_t *drafts = in->draft_tokens + d0;
+    int32_t a = k, token = -1;
+    int decided = 0;
+
+    if (in->greedy[b]) {
+        /* [A1] accept while d_i == argmax_i; the output at the first mismatch (or row k) is
+         * that row's argmax */
+        for (int32_t i = 0; i <= k; i++) {
+            int pen = row_logits(in, b, i, z), nt = 0;
+            int32_t g = row_argmax(z, V, pen, &nt);
+            if (i < k) {
+                if (out_pq) { out_pq[(d0 + i) * 2] = NAN; out_pq[(d0 + i) * 2 + 1] = NAN; }
+                if (pq_near) pq_near[d0 + i] = 0;
+            }
+            if (!decided) {
+                d.decisions++;
+                d.near_ties += nt;
+                if (i == k || drafts[i] != g) { a = i; token = g; decided = 1; }
+            }
+        }
+    } else {
+        for (int32_t i = 0; i <= k; i++) {
+            int pen = row_logits(in, b, i, z);
+            int dec = 0, nt = 0;
+            row_probs(in, b, z, pen, p, scratch, &dec, &nt);
+            if (i < k) {
+                int32_t x = drafts[i];
+                double px = p[x];
+                double qx = (double)in->draft_probs[(d0 + i) * (int64_t)V + x];
+                if (out_pq) { out_pq[(d0 + i) * 2] = px; out_pq[(d0 + i) * 2 + 1] = qx; }
+                if (pq_near) pq_near[d0 + i] = (uint8_t)(nt > 0);
+                if (decided) continue;
+                d.decisions += dec + 1;
+                d.near_ties += nt;
+                double u = in->uniforms[(r0 + i) * 2 + 0];
+                int accept;
+                if (px > 0.0 && qx == 0.0) {
+                    accept = 1;
+                } else if (px > 0.0) {
+                    double ratio = px / qx;
+                    double thr = ratio < 1.0 ? ratio : 1.0;
+                    accept = u < thr;
+                    if (fabs(u - thr) < NEAR_TOL) d.near_ties++;
+                } else {
+                    accept = 0;
+                }
+                if (!accept) {
+                    /* [R1] residual max(0, p - q) at the rejected row, normalised by its sum */
+                    const float *q = in->draft_probs + (d0 + i) * (int64_t)V;
+                    double W = 0.0;
+                    for (int32_t v = 0; v < V; v++) {
+                        double t = p[v] - (double)q[v];
+                        r[v] = t > 0.0 ? t : 0.0;
+                        W += r[v];
+                    }
+                    double u1 = in->uniforms[(r0 + i) * 2 + 1];
+                    int cn = 0;
+                    if (W > 0.0) {
+                        token = inverse_cdf(r, V, u1, &cn);
+                    } else {
+                        token = inverse_cdf(p, V, u1, &cn);   /* empty residual: draw from p */
+                    }
+                    if (W < NEAR_W) cn = 1;
+                    d.decisions++;
+                    d.near_ties += cn;
+                    a = i;
+                    decided = 1;
+                }
+            } else if (!decided) {
+                /* [R2] every draft accepted: the extra token comes from row k */
+                int cn = 0;
+                d.decisions += dec + 1;
+                d.near_ties += nt;
+                token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], &cn);
+                d.near_ties += cn;
+                a = k;
+                decided = 1;
+            }
+        }
+    }
+    for (int32_t j = 0; j < a; j++) out_tok[(int64_t)b * kmax1 + j] = drafts[j];
+    out_tok[(int64_t)b * kmax1 + a] = token;
+    acc[b] = a;
+    if (dg) dg[b] = d;
+}
+
+/* Verifies requests [b_lo, b_hi).  Output arrays are full-batch sized; only the rows of
+ * these requests are written.  Safe to call concurrently on disjoint request ranges. */
+int sv_oracle_verify(const sv_oracle_batch *in, int32_t b_lo, int32_t b_hi, int32_t *out_tokens,
+                     int32_t *accept_len, double *out_pq, uint8_t *pq_near, sv_oracle_diag *diag) {
+    if (!in || !out_tokens || !accept_len || in->V < 1 || b_lo < 0 || b_hi > in->B) return -1;
+    size_t V = (size_t)in->V;
+    double *buf = (double *)malloc(sizeof(double) * V * 4);
+    if (!buf) return -2;
+    for (int32_t b = b_lo; b < b_hi; b++)
+        verify_one(in, b, out_tokens, accept_len, out_pq, pq_near, diag, buf, buf + V, buf + 2 * V,
+                   buf + 3 * V);
+    free(buf);
+    return 0;
+}
+
+/* The full distribution a row is sampled from: the filtered, renormalised target p for a
+ * sampled request, or one-hot at the argmax for a greedy one.  Returns the kept count, or
+ * a negative value on bad arguments. */
+int32_t sv_oracle_row_probs(const sv_oracle_batch *in, int32_t b, int32_t i, double *p) {
+    if (!in || !p || b < 0 || b >= in->B || i < 0 || i > in->num_drafts[b]) return -1;
+    if (check_request(in, b) == E_LAYOUT) return -1;
+    size_t V = (size_t)in->V;
+    double *buf = (double *)malloc(sizeof(double) * V * 2);
+    if (!buf) return -2;
+    int pen = row_logits(in, b, i, buf);
+    int32_t kept;
+    if (in->greedy[b]) {
+        int nt;
+        int32_t g = row_argmax(buf, in->V, pen, &nt);
+        for (size_t v = 0; v < V; v++) p[v] = 0.0;
+        p[g] = 1.0;
+        kept = 1;
+    } else {
+        int dec = 0, nt = 0;
+        kept = row_probs(in, b, buf, pen, p, buf + V, &dec, &nt);
+    }
+    free(buf);
+    return kept;
+}
+
+/* The normalised residual max(0, p_i - q_i) / W at draft row i of request b (sampled
+ * requests), with W returned through *W_out. */
+int32_t sv_oracle_residual(const sv_oracle_batch *in, int32_t b, int32_t i, double *r, double *W_out) {
+    if (!in || !r || b < 0 || b >= in->B || i < 0 || i >= in->num_drafts[b] || in->greedy[b]) return -1;
+    size_t V = (size_t)in->V;
+    double *buf = (double *)malloc(sizeof(double) * V * 3);
+    if (!buf) return -2;
+    int pen = row_logits(in, b, i, buf);
+    int dec = 0, nt = 0;
+    row_probs(in, b, buf, pen, buf + V, buf + 2 * V, &dec, &nt);
+    const float *q = in->draft_probs + (row_start(in, b) - b + i) * (int64_t)in->V;
+    double W = 0.0;
+    for (size_t v = 0; v < V; v++) {
+        double t = buf[V + v] - (double)q[v];
+        r[v] = t > 0.0 ? t : 0.0;
+        W += r[v];
+    }
+    if (W > 0.0)
+        for (size_t v = 0; v < V; v++) r[v] /= W;
+    if (W_out) *W_out = W;
+    free(buf);
+    return 0;
+}
+
+/* Target KV rollback [R3]: the verify step appended k_b + 1 rows and keeps 1 + accept_len
+ * of them: L' = L - (k_b + 1) + 1 + a.  A length that would move forward (a > k_b), a
+ * negative accept length or a negative result is an error: that request's output is -1 and
+ * the return value counts the errors. */
+int32_t sv_oracle_rollback(const int32_t *kv_seq_len, const int32_t *accept_len,
+                           const int32_t *num_drafts, int32_t B, int32_t *out_len) {
+    int32_t errors = 0;
+    for (int32_t b = 0; b < B; b++) {
+        int64_t L = kv_seq_len[b], k = num_drafts[b], a = accept_len[b];
+        int64_t t = L - (k + 1) + 1 + a;
+        if (k < 0 || a < 0 || a > k || t < 0 || t > L) {
+            out_len[b] = -1;
+            errors++;
+        } else {
+            out_len[b] = (int32_t)t;
+        }
+    }
+    return errors;
+}
