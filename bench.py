@@ -1,0 +1,331 @@
+"""Benchmark of batched speculative-decoding verification on GB300.
+
+One step = one spec_verify call over the whole batch (every row's statistics and filtering,
+the draft gathers, the first-rejection scan and the residual / extra-token draws).  The
+default workload is B=256 requests x k=4 drafts over V=128256 (bf16 Zipf-shaped logits,
+top-k 50, top-p 0.9, a quarter greedy).  Inputs are synthetic and seeded; three device copies
+of the two large inputs (0.85 GB each set) rotate between steps so no step reads inputs left
+in L2 by the one before.
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify rows/s and achieved HBM GB/s (% of GB300 roofline) vs CPU oracle"
+DEFAULT_WORKLOAD = "b256_k4_v128256_bf16_zipf"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w, accept_len) -> dict:
+    """Bytes the method must move for one call (see the design notes, 'Measurement').
+
+    Every target row of every request (the one-pass design cannot skip rows before knowing
+    where the rejection falls); one 32-byte sector of q per sampled draft (q(x_i)); at a
+    rejected sampled row, q over the residual's support: the kept set of a filtered row
+    (<= top-k tokens, one sector each) or the whole q row plus a re-read of the target row when
+    the row keeps every token; small per-row/per-request I/O.
+    """
+    esz = 2 if w.dtype == "bf16" else 4
+    V = w.V
+    nd = w.num_drafts.astype(np.int64)
+    rows = int((nd + 1).sum())
+    sampled = w.greedy == 0
+    b_rows = rows * V * esz
+    b_q = int(nd[sampled].sum()) * 32
+    b_rej = 0
+    for b in np.nonzero(sampled & (accept_len < nd) & (accept_len >= 0))[0]:
+        K = int(w.top_k[b])
+        if 0 < K < V:
+            b_rej += 32 * K
+        else:
+            b_rej += V * esz + V * 4
+    b_io = rows * 8 + int(nd.sum()) * 4 + w.B * (4 * (w.k_max + 2) + 24)
+    total = b_rows + b_q + b_rej + b_io
+    b_json = rows * V * esz + int(nd.sum()) * V * 4 + int(((accept_len < nd) & (accept_len >= 0)).sum()) * V * esz
+    return dict(total=total, rows=b_rows, q_sectors=b_q, rejected=b_rej, io=b_io, baseline_json_formula=b_json)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(workload: str, seconds_target: float = 15.0, max_requests: int = 64):
+    """The float64 oracle on the host cores, on a bounded sample of the same workload."""
+    import oracle
+    import sv_workloads as W
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    sp = W.spec(workload)
+    # size the sample from a 1-request probe
+    probe = W.make(workload, requests=[0])
+    t0 = time.perf_counter()
+    oracle.verify(probe)
+    t1 = time.perf_counter() - t0
+    n = int(max(cores, min(max_requests, seconds_target * cores / max(t1, 1e-3))))
+    n = min(n, sp.B)
+    w = W.make(workload, requests=range(n))
+    t0 = time.perf_counter()
+    oracle.verify(w, threads=cores)
+    dt = time.perf_counter() - t0
+    rows = int((w.num_drafts.astype(np.int64) + 1).sum())
+    return {"value": rows / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {sp.B} requests ({rows} rows), float64 C oracle, {cores} threads, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle itself, timed per step on a bounded sample."""
+    import oracle
+    import sv_workloads as W
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    sp = W.spec(args.workload)
+    n = min(sp.B, max(cores, 16))
+    w = W.make(args.workload, requests=range(n))
+    rows = int((w.num_drafts.astype(np.int64) + 1).sum())
+    for _ in range(args.warmup):
+        oracle.verify(w, requests=range(min(n, cores)), threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(w, threads=cores)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": sp.name, "B": sp.B, "k": sp.k_max, "V": sp.V, "logits": sp.dtype,
+                       "step": f"{n} of {sp.B} requests per step"},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {n} of {sp.B} requests ({rows} rows) per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sv_workloads as W
+    import speculative_decoding_verification_12_gb300 as sv
+    from speculative_decoding_verification_12_gb300.batch import DeviceBatch, bound_call
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.lib()
+
+    sp = W.spec(args.workload)
+    w = W.make(args.workload)           # every rank verifies its own full batch (weak scaling)
+    db = DeviceBatch.from_host(w, dev, want_pq=False)
+    stream = torch.cuda.Stream(dev)
+    copies = [(db.target_logits, db.draft_probs)]
+    for _ in range(args.copies - 1):
+        copies.append((db.target_logits.clone(), db.draft_probs.clone()))
+    with torch.cuda.stream(stream):
+        calls = [bound_call(db, stream, t, d) for t, d in copies]
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        calls[i % len(calls)]()
+    barrier()
+    acc = db.accept_len.cpu().numpy()
+    out_tok = db.out_tokens.cpu().numpy()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for i in range(args.steps):
+        calls[i % len(calls)]()
+    ev1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    rows = int((w.num_drafts.astype(np.int64) + 1).sum())
+    drafts = int(w.num_drafts.sum())
+    per_step_ms = ms_max / args.steps
+    value = rows * world * args.steps / (ms_max / 1e3)
+
+    nb = algorithmic_bytes(w, acc)
+    peak, peak_kind = peaks()
+    achieved = nb["total"] / (ms / args.steps / 1e3) / 1e9
+
+    # end to end through the C ABI from pinned host buffers: H2D inputs, verify, D2H results
+    host = {
+        "tl": torch.from_numpy(np.ascontiguousarray(w.target_logits).view(np.int16) if w.dtype == "bf16"
+                               else w.target_logits).pin_memory(),
+        "dp": torch.from_numpy(w.draft_probs).pin_memory(),
+        "dt": torch.from_numpy(w.draft_tokens).pin_memory(),
+        "u": torch.from_numpy(w.uniforms).pin_memory(),
+    }
+    pins_out = (torch.empty_like(db.out_tokens, device="cpu").pin_memory(),
+                torch.empty_like(db.accept_len, device="cpu").pin_memory())
+    tl_dev = db.target_logits.view(torch.int16) if w.dtype == "bf16" else db.target_logits
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in pins_out)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            tl_dev.copy_(host["tl"], non_blocking=True)
+            db.draft_probs.copy_(host["dp"], non_blocking=True)
+            db.draft_tokens.copy_(host["dt"], non_blocking=True)
+            db.uniforms.copy_(host["u"], non_blocking=True)
+            calls[0]()
+            pins_out[0].copy_(db.out_tokens, non_blocking=True)
+            pins_out[1].copy_(db.accept_len, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e_ms = e0.elapsed_time(e1)
+    te = torch.tensor([e_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = rows * world * args.e2e_steps / (float(te.item()) / 1e3)
+    assert np.array_equal(pins_out[1].numpy(), acc), "end-to-end results differ from the device-resident run"
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": sp.name, "B": sp.B, "k": sp.k_max, "V": sp.V, "logits": sp.dtype,
+                       "top_k": 50, "top_p": 0.9, "greedy_share": 0.25, "parallelism": f"replicas x{world}",
+                       "l2": f"{args.copies} rotating device copies of the inputs "
+                             f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + db.draft_probs.numel() * 4) / 1e9:.2f} GB > L2)"},
+            "draft_tokens_per_s": drafts * world * args.steps / (ms_max / 1e3),
+            "hbm_gbs": achieved,
+            "accept": {"mean_accept_len": float(acc.mean()), "accept_rate": float(acc.sum() / max(drafts, 1)),
+                       "tokens_per_step": float(acc.mean() + 1)},
+            "bytes_per_step": nb,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": args.traffic, "peak_source": peak_kind,
+                         "kernel": "sv::verify_kernel<bf16>"},
+            "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes (read+write) per launch of the verify kernel, if captured")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

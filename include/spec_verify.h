@@ -1,0 +1,163 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched speculative-decoding verifier.
+ *
+ * The library implements draft verification by modified rejection sampling as these sources
+ * define it:
+ *  - "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust",
+ *    sections "The Memory Bandwidth Wall and Speculative Math" (accept x_i with probability
+ *    min(1, p(x_i)/q(x_i)); at the first rejection draw from max(0, p - q) normalised),
+ *    "The Verification Algorithm" (the target's K+1 logit rows become softmax(logits / T);
+ *    the loop stops at the first rejection; with every draft accepted the extra token is drawn
+ *    from row K; only the accepted count and the correction token go back to the host) and
+ *    "Orchestrating the Inference Loop" (the target KV cache keeps 1 + accepted of the K+1 rows).
+ *  - "Adding Speculative Decoding", section "Verification and sampling": one batched verify
+ *    over k+1 rows per request, requests with different k, greedy argmax compare as the
+ *    degenerate case, the extra token honouring top-k/top-p/penalties; table "The existing
+ *    base": greedy accepts while draft == argmax, the extra token is the argmax at the first
+ *    mismatch.
+ *  - FreeToken PR #836, section "Design": each verify row samples with its own request's
+ *    temperature, top-k, top-p and greedy flag, and presence/frequency penalties count the
+ *    drafts before the row as already generated.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named as device arrays must be CUDA device memory (or managed memory) that the
+ *    caller owns and keeps alive until the work on `stream` has finished.  The library
+ *    allocates no memory, makes no host<->device copy and does not synchronise; all work is
+ *    enqueued on `stream` (a cudaStream_t; NULL means the legacy default stream).
+ *  - Errors the host can see (null pointers, bad sizes, an unsupported shape, a workspace that
+ *    is too small or misaligned) return at once with nothing enqueued.
+ *  - Errors in device data (a draft token outside [0, V), num_drafts outside its range,
+ *    T <= 0 or non-finite on a sampled request, top_p outside (0, 1], a uniform outside [0, 1),
+ *    a non-finite penalty, inconsistent row_offsets) are found by the kernels.  The affected
+ *    request's outputs become -1 and a sticky error word in the workspace records the first
+ *    code; the call itself still returns SV_OK.  sv_read_device_error() fetches the word.
+ *    No kernel traps or asserts.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size, bad dtype  */
+    SV_ERR_WORKSPACE = 2,     /* workspace too small or not 256-byte aligned             */
+    SV_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch or memset)           */
+    SV_ERR_UNSUPPORTED = 4,   /* shape outside what the kernels handle (V, k_max, B)     */
+    SV_ERR_DEVICE_DATA = 5    /* returned only by sv_read_device_error: bad device data  */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Device-data error codes stored in the workspace's sticky error word. */
+enum {
+    SV_DEV_OK = 0,
+    SV_DEV_BAD_LAYOUT = 1,    /* num_drafts[b] < 0, > k_max, or rows of b inconsistent   */
+    SV_DEV_BAD_TOKEN = 2,     /* a draft token outside [0, V)                            */
+    SV_DEV_BAD_TEMPERATURE = 3,
+    SV_DEV_BAD_TOP_P = 4,
+    SV_DEV_BAD_UNIFORM = 5,
+    SV_DEV_BAD_PENALTY = 6
+};
+
+/* Per-request sampling parameters: structure of device arrays, each of length B. */
+typedef struct sv_params {
+    const float *temperature;       /* > 0 and finite for sampled requests; unread when greedy   */
+    const int32_t *top_k;           /* <= 0 or >= V: top-k off; else keep tokens >= k-th largest */
+    const float *top_p;             /* in (0, 1]; 1 = off; keep v while mass strictly above < p  */
+    const float *presence_penalty;  /* may be NULL (all 0): subtracted once from a drafted token */
+    const float *frequency_penalty; /* may be NULL (all 0): subtracted per earlier occurrence    */
+    const uint8_t *greedy;          /* 1 = greedy request (argmax prefix match), 0 = sampled     */
+} sv_params;
+
+/* Size in bytes of the device workspace spec_verify and spec_rollback need for a batch of B
+ * requests and total_rows target rows of vocabulary V.  The workspace is caller-owned
+ * device memory, 256-byte aligned; it needs no initialisation and may be reused by later
+ * calls on the same stream (not by calls that run concurrently).  Returns 0 for invalid
+ * sizes. */
+size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V);
+
+/*
+ * spec_verify -- verify the drafts of a batch of requests in one pass.
+ *
+ * Layout.  Request b owns target rows [row_offsets[b], row_offsets[b+1]) of target_logits and
+ * the draft rows [row_offsets[b] - b, row_offsets[b+1] - b - 1) of draft_probs/draft_tokens; it
+ * uses its first num_drafts[b] + 1 rows and num_drafts[b] drafts (ragged batches: pack with
+ * row_offsets[b+1] - row_offsets[b] = num_drafts[b] + 1).  With row_offsets == NULL the
+ * batch is uniform: target_logits [B, k_max+1, V], draft_probs [B, k_max, V], draft_tokens
+ * [B, k_max], uniforms [B, k_max+1, 2], total_rows = B * (k_max + 1); requests may still use
+ * fewer than k_max drafts.
+ *
+ *   target_logits  device [total_rows, V], row-major, dtype logits_dtype (bf16 or fp32);
+ *                  16-byte aligned for the vectorised path (any alignment is accepted).
+ *   draft_probs    device fp32 [total_rows - B, V]: the draft's distribution q_i per draft row.
+ *                  Only q_i(x_i) is read for every sampled draft; whole rows only at a rejection.
+ *   draft_tokens   device int32 [total_rows - B]: x_i, the drafted token ids.
+ *   num_drafts     device int32 [B]: k_b, 0 <= k_b <= k_max.
+ *   row_offsets    device int32 [B+1] (row_offsets[0] = 0, row_offsets[B] = total_rows), or NULL.
+ *   B, k_max, V, total_rows: host sizes; 1 <= V <= 2^21, 0 <= k_max <= 64, B >= 1.
+ *   params         per-request sampling parameters (device arrays of length B).
+ *   uniforms       device fp32 [total_rows, 2] in [0, 1): slot 0 of row i is the accept test of
+ *                  draft i; slot 1 of the row where the request stops is the residual draw (at a
+ *                  rejection) or the extra-token draw (all drafts accepted).  Greedy requests read
+ *                  none.
+ *   out_tokens     device int32 [B, k_max+1]: accepted drafts, then the correction/extra token,
+ *                  then -1 padding.  All -1 for a request with a device-data error.
+ *   accept_len     device int32 [B]: number of accepted drafts a_b (-1 on a device-data error).
+ *   out_pq         optional device fp32 [total_rows - B, 2]: (p_i(x_i), q_i(x_i)) for every draft
+ *                  of a sampled request, whether or not the loop reached it; NaN for greedy
+ *                  requests.  NULL skips it.
+ *   workspace      device, sv_workspace_bytes() bytes, 256-byte aligned.
+ *   stream         cudaStream_t.
+ *
+ * Per row the target distribution is p = softmax(z / T) over the tokens kept by top-k (every
+ * token >= the k-th largest, ties kept) and then top-p (tokens whose renormalised mass strictly
+ * above them is < top_p), renormalised; z_v = logit_v - presence * [c_v > 0] - frequency * c_v
+ * with c_v the count of v among the request's drafts before the row.  A draft is accepted iff
+ * p > 0 and (q == 0 or u < min(1, p/q)).  Draws use the inverse CDF in token-id order.
+ * Arithmetic is fp32 (exp via ex2); a greedy row's argmax breaks ties toward the lowest id.
+ */
+sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                      const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
+                      int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                      const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_rollback -- commit the verify step to the target KV lengths.
+ *
+ * From "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust",
+ * "Orchestrating the Inference Loop": the verify step appended k_b + 1 rows to request b's
+ * target KV cache and keeps 1 + accept_len[b] of them, so
+ *     kv_seq_len[b] <- kv_seq_len[b] - (k_b + 1) + 1 + accept_len[b].
+ * ("KV Cache Rollback Mechanics": rolling back forward is an error.)
+ *
+ *   kv_seq_len   device int32 [B], updated in place; it is also the committed length returned.
+ *   accept_len   device int32 [B], as written by spec_verify.
+ *   num_drafts   device int32 [B]: k_b (the argument spec_verify got).
+ *   workspace    the spec_verify workspace (its sticky error word records failures).
+ * A request with accept_len < 0 or > k_b, k_b < 0, or a result outside [0, kv_seq_len] keeps
+ * its length and records SV_DEV_BAD_LAYOUT.
+ */
+sv_status spec_rollback(int32_t *kv_seq_len, const int32_t *accept_len, const int32_t *num_drafts,
+                        int32_t B, void *workspace, void *stream);
+
+/* Reads the sticky device-data error word of a workspace (synchronises the device; meant for
+ * tests and debugging).  *code receives an SV_DEV_* value, *first_bad_request the lowest
+ * request index that set it (-1 if none).  Returns SV_OK when no error was recorded,
+ * SV_ERR_DEVICE_DATA when one was, or SV_ERR_CUDA. */
+sv_status sv_read_device_error(const void *workspace, int32_t *code, int32_t *first_bad_request);
+
+/* Human-readable name of a status code. */
+const char *sv_status_string(sv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -39,9 +39,12 @@ class _Batch(C.Structure):
                 ("frequency", C.c_void_p), ("greedy", C.c_void_p), ("uniforms", C.c_void_p)]
 
 
+DIAG_FIELDS = ("decisions", "near_ties", "error", "near_accept", "near_cdf", "near_filter", "near_argmax",
+               "near_w")
+
+
 class _Diag(C.Structure):
-    _fields_ = [("decisions", C.c_int32), ("near_ties", C.c_int32), ("error", C.c_int32),
-                ("reserved", C.c_int32)]
+    _fields_ = [(f, C.c_int32) for f in DIAG_FIELDS]
 
 
 _lib = None
@@ -133,9 +136,11 @@ def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1):
     else:
         for rg in ranges:
             run(rg)
-    dg = np.frombuffer(diag, dtype=np.int32).reshape(-1, 4)[:B]
-    return dict(out_tokens=out, accept_len=acc, pq=pq[:D], pq_near=near[:D],
-                decisions=dg[:, 0].copy(), near_ties=dg[:, 1].copy(), error=dg[:, 2].copy())
+    dg = np.frombuffer(diag, dtype=np.int32).reshape(-1, len(DIAG_FIELDS))[:B]
+    res = dict(out_tokens=out, accept_len=acc, pq=pq[:D], pq_near=near[:D])
+    for j, f in enumerate(DIAG_FIELDS):
+        res[f] = dg[:, j].copy()
+    return res
 
 
 def row_probs(w, b: int, i: int) -> np.ndarray:

@@ -77,7 +77,7 @@ typedef struct sv_oracle_diag {
     int32_t decisions;  /* accept tests + draws + greedy argmaxes + filter thresholds on the path */
     int32_t near_ties;  /* decisions within the near-tie band */
     int32_t error;      /* 0, or the device-data error code of the request */
-    int32_t reserved;
+    int32_t near_accept, near_cdf, near_filter, near_argmax, near_w;  /* near_ties by kind */
 } sv_oracle_diag;
 
 enum { E_OK = 0, E_LAYOUT = 1, E_TOKEN = 2, E_TEMP = 3, E_TOPP = 4, E_UNIFORM = 5, E_PENALTY = 6 };
@@ -289,7 +289,7 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
     const int32_t V = in->V;
     const int32_t kmax1 = in->k_max + 1;
     for (int32_t j = 0; j < kmax1; j++) out_tok[(int64_t)b * kmax1 + j] = -1;
-    sv_oracle_diag d = {0, 0, 0, 0};
+    sv_oracle_diag d = {0, 0, 0, 0, 0, 0, 0, 0};
     int err = check_request(in, b);
     const int64_t r0 = row_start(in, b), d0 = r0 - b;
     const int32_t k = in->num_drafts[b];
@@ -321,6 +321,7 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
             if (!decided) {
                 d.decisions++;
                 d.near_ties += nt;
+                d.near_argmax += nt;
                 if (i == k || drafts[i] != g) { a = i; token = g; decided = 1; }
             }
         }
@@ -338,6 +339,7 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                 if (decided) continue;
                 d.decisions += dec + 1;
                 d.near_ties += nt;
+                d.near_filter += nt;
                 double u = in->uniforms[(r0 + i) * 2 + 0];
                 int accept;
                 if (px > 0.0 && qx == 0.0) {
@@ -346,7 +348,7 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                     double ratio = px / qx;
                     double thr = ratio < 1.0 ? ratio : 1.0;
                     accept = u < thr;
-                    if (fabs(u - thr) < NEAR_TOL) d.near_ties++;
+                    if (fabs(u - thr) < NEAR_TOL) { d.near_ties++; d.near_accept++; }
                 } else {
                     accept = 0;
                 }
@@ -366,7 +368,7 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                     } else {
                         token = inverse_cdf(p, V, u1, &cn);   /* empty residual: draw from p */
                     }
-                    if (W < NEAR_W) cn = 1;
+                    if (W < NEAR_W) { cn = 1; d.near_w++; } else { d.near_cdf += cn; }
                     d.decisions++;
                     d.near_ties += cn;
                     a = i;
@@ -377,8 +379,10 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                 int cn = 0;
                 d.decisions += dec + 1;
                 d.near_ties += nt;
+                d.near_filter += nt;
                 token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], &cn);
                 d.near_ties += cn;
+                d.near_cdf += cn;
                 a = k;
                 decided = 1;
             }

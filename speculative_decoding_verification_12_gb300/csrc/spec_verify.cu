@@ -1,0 +1,648 @@
+// spec_verify.cu -- batched speculative-decoding verification for GB300 (sm_103a): the
+// C-ABI entry points and the fused verify kernel.
+//
+// One CTA per target row streams the row once from HBM (128-bit loads, 8 tokens per lane,
+// 256-token segments per warp step) and reduces it to per-segment maxima and weight sums.
+// From those it builds the row's kept set:
+//   - no filter: p = e / Z with Z from the segment sums (no second pass);
+//   - top-k (k <= KCAP): the k-th largest segment maximum bounds the k-th largest token from
+//     below, so only the segments whose maximum reaches it are re-read (from L2) to collect
+//     candidates; the exact top-k and top-p cut is made on the sorted candidates in shared
+//     memory;
+//   - otherwise (top-p alone, large top-k, candidate overflow): radix select with 11-bit
+//     digits over the row, counts for top-k and fixed-point masses for top-p.
+// It then gathers p(x_i) and q(x_i) for the row's draft, and on a request's last row also
+// draws the extra token.  The CTA that completes the last row of a request (arrival counter
+// per request; no CTA ever waits on another) runs the first-rejection scan and, at a
+// rejection, draws from max(0, p - q) of the rejected row: over the stored kept list when it
+// is small, else in one pass over the row and its draft row.
+//
+// Method: "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust"
+// ("The Memory Bandwidth Wall and Speculative Math", "The Verification Algorithm",
+// "Orchestrating the Inference Loop"); "Adding Speculative Decoding" ("Verification and
+// sampling", table "The existing base"); FreeToken PR #836 ("Design").
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/spec_verify.h"
+#include "sv_row.cuh"
+
+namespace sv {
+
+// Shared-memory carve-up of one CTA (dynamic part).
+struct Dyn {
+    float *segA, *segB, *segC;   // per-segment max / weight sums
+    unsigned long long *cand;    // CAP keys: (order key << 32) | ~token, later (~token << 32) | key
+    float *aux, *aux2;           // CAP floats each
+    uint32_t *hcnt;              // radix histogram (aliases cand/aux)
+    unsigned long long *hmass;   // fixed-point mass histogram (aliases)
+};
+
+__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 3) & ~3; }
+__host__ __device__ inline size_t dyn_bytes(int nseg) {
+    return size_t(3) * nseg_pad(nseg) * 4 + size_t(CAP) * 8 + size_t(CAP) * 4 * 2;
+}
+
+__device__ __forceinline__ Dyn carve(unsigned char *base, int nseg) {
+    Dyn d;
+    const int np = nseg_pad(nseg);
+    d.segA = reinterpret_cast<float *>(base);
+    d.segB = d.segA + np;
+    d.segC = d.segB + np;
+    unsigned char *area = reinterpret_cast<unsigned char *>(d.segC + np);
+    d.cand = reinterpret_cast<unsigned long long *>(area);
+    d.aux = reinterpret_cast<float *>(area + size_t(CAP) * 8);
+    d.aux2 = d.aux + CAP;
+    d.hmass = reinterpret_cast<unsigned long long *>(area);                     // HB * 8 bytes
+    d.hcnt = reinterpret_cast<uint32_t *>(area + size_t(HB) * 8);               // HB * 4 bytes
+    return d;
+}
+
+__device__ __forceinline__ void record_error(const Args &A, int code, int b) {
+    atomicCAS(A.hdr, 0, code);
+    atomicMax(A.hdr + 1, INT_MAX - b);
+}
+
+// ------------------------------------------------------------------------------------------
+// the row phase
+// ------------------------------------------------------------------------------------------
+
+// Kept set of a sampled row from the top-k candidates.  Returns false on candidate overflow.
+template <typename E, bool VEC>
+__device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const E *row, RowStat &st, int row_idx,
+                                     bool want_bonus) {
+    const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
+    const int V = A.V, nseg = A.nseg, K = S.K;
+    const float m = S.m, s = S.s;
+    // lower bound: the K-th largest segment maximum (all tokens if fewer segments than K)
+    uint32_t tkey = 0;
+    if (nseg >= K) tkey = select_kth_smem(S, D.segA, nseg, K, D.hcnt);
+    if (tid == 0) S.ncand = 0;
+    __syncthreads();
+    for (int seg = warp; seg < nseg; seg += NWARP) {
+        if (fkey(D.segA[seg]) < tkey) continue;          // warp-uniform
+        float v[8];
+        seg_values<E, VEC>(S, row, V, seg, v);
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            int idx = seg * SEG + lane * 8 + j;
+            c += (idx < V && fkey(v[j]) >= tkey) ? 1 : 0;
+        }
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int total = __shfl_sync(0xffffffffu, incl, 31);
+        int base = 0;
+        if (lane == 0 && total) base = atomicAdd(&S.ncand, total);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        int pos = base + incl - c;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            int idx = seg * SEG + lane * 8 + j;
+            uint32_t key = fkey(v[j]);
+            if (idx < V && key >= tkey) {
+                if (pos < CAP) D.cand[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)idx);
+                pos++;
+            }
+        }
+    }
+    __syncthreads();
+    const int n = S.ncand;
+    if (n > CAP || n < 1) return false;
+    const int np = pow2_at_least(n);
+    for (int j = n + tid; j < np; j += NT) D.cand[j] = 0ull;
+    __syncthreads();
+    block_sort_desc(D.cand, np);
+    // exact top-k: tokens whose key reaches the K-th largest (ties kept)
+    const int kk = min(K, n);
+    const uint32_t kkey = (uint32_t)(D.cand[kk - 1] >> 32);
+    int c1 = 0;
+    for (int j = tid; j < n; j += NT) c1 += ((uint32_t)(D.cand[j] >> 32) >= kkey) ? 1 : 0;
+    const int n1 = block_sum_i(c1, S.redi);
+    for (int j = tid; j < n1; j += NT) D.aux[j] = weight(key2f((uint32_t)(D.cand[j] >> 32)), m, s);
+    __syncthreads();
+    for (int j = tid; j < n1; j += NT) D.aux2[j] = D.aux[j];
+    __syncthreads();
+    block_scan_incl(D.aux2, n1, S.redf);
+    // top-p: cut at the first value level whose mass strictly above reaches P * Z1
+    int n2 = n1;
+    if (S.topp_on) {
+        const float PZ = __fmul_rn(S.P, D.aux2[n1 - 1]);
+        int cut = 0x7fffffff;
+        for (int j = tid; j < n1; j += NT) {
+            if (j > 0 && (uint32_t)(D.cand[j] >> 32) != (uint32_t)(D.cand[j - 1] >> 32) && D.aux2[j - 1] >= PZ)
+                cut = min(cut, j);
+        }
+        cut = block_min_i(cut, S.redi);
+        if (cut != 0x7fffffff) n2 = cut;
+    }
+    const float Z = D.aux2[n2 - 1];
+    const uint32_t taukey = (uint32_t)(D.cand[n2 - 1] >> 32);
+    st.Z = Z;
+    st.invZ = __frcp_rn(Z);
+    st.taukey = taukey;
+    st.tau = key2f(taukey);
+    st.kind = n2 <= LCAP ? KIND_LIST : KIND_THRESH;
+    st.nlist = n2 <= LCAP ? n2 : 0;
+    __syncthreads();
+    // the kept set in token order: re-key as (~token << 32) | value key and sort again
+    if (n2 <= LCAP || want_bonus) {
+        const int np2 = pow2_at_least(n2);
+        for (int j = tid; j < np2; j += NT) {
+            unsigned long long c = D.cand[j];
+            D.cand[j] = j < n2 ? ((c << 32) | (c >> 32)) : 0ull;
+        }
+        __syncthreads();
+        block_sort_desc(D.cand, np2);
+        for (int j = tid; j < n2; j += NT) D.aux[j] = weight(key2f((uint32_t)D.cand[j]), m, s);
+        __syncthreads();
+        if (n2 <= LCAP) {
+            int32_t *L = A.lists + (size_t)row_idx * LCAP * 2;
+            for (int j = tid; j < n2; j += NT) {
+                L[2 * j] = (int32_t)(~(uint32_t)(D.cand[j] >> 32));
+                L[2 * j + 1] = __float_as_int(D.aux[j]);
+            }
+        }
+        if (want_bonus) {
+            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            int j = draw_small(D.aux, D.aux2, n2, u, S);
+            st.bonus = j >= 0 ? (int32_t)(~(uint32_t)(D.cand[j] >> 32)) : -1;
+        }
+    }
+    __syncthreads();
+    return true;
+}
+
+// Kept set by radix select over the whole row (any top-k / top-p).
+template <typename E, bool VEC>
+__device__ void kept_by_select(const Args &A, Ctx &S, const Dyn &D, const E *row, RowStat &st, int row_idx,
+                               bool want_bonus) {
+    const int V = A.V, nseg = A.nseg;
+    const float m = S.m, s = S.s;
+    uint32_t key_lo = 0;
+    if (S.topk_on) key_lo = select_kth_row<E, VEC>(S, row, V, nseg, S.K, D.hcnt);
+    if (S.topp_on) key_lo = select_mass_row<E, VEC>(S, row, V, nseg, key_lo, m, s, S.P, D.hmass);
+    WKept wk{m, s, key_lo};
+    seg_sums<E, VEC, false>(S, row, nullptr, V, nseg, D.segB, wk, nullptr, wk);
+    float part = 0.f;
+    for (int j = threadIdx.x; j < nseg; j += NT) part += D.segB[j];
+    const float Z = block_sum(part, S.redf);
+    st.Z = Z;
+    st.invZ = __frcp_rn(Z);
+    st.taukey = key_lo;
+    st.tau = key_lo ? key2f(key_lo) : -INFINITY;
+    st.kind = KIND_THRESH;
+    st.nlist = 0;
+    if (want_bonus) {
+        const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+        st.bonus = draw_by_segments<E, VEC, false>(S, row, nullptr, V, nseg, D.segB, u, wk);
+    }
+}
+
+template <typename E, bool VEC>
+__device__ void row_phase(const Args &A, Ctx &S, const Dyn &D, const int row_idx) {
+    const int tid = threadIdx.x;
+    const int V = A.V, nseg = A.nseg;
+    const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)row_idx * V;
+    RowStat st;
+    st.m = 0.f; st.s = 0.f; st.tau = -INFINITY; st.Z = 1.f; st.invZ = 1.f; st.taukey = 0;
+    st.argmax = -1; st.bonus = -1; st.kind = KIND_SKIP; st.nlist = 0; st.pad0 = 0; st.pad1 = 0;
+
+    const bool sampled = !S.greedy;
+    const int i = S.i;
+    const bool want_bonus = sampled && i == S.k;
+    float s = 0.f;
+    if (sampled) s = __fdiv_rn(LOG2E, S.T);
+    if (tid == 0) {
+        S.s = s;
+        S.topk_on = sampled && S.K > 0 && S.K < V;
+        S.topp_on = sampled && S.P < 1.f;
+    }
+    __syncthreads();
+    const bool need_sum = sampled && !S.topk_on && !S.topp_on;
+    pass_stats<E, VEC>(S, row, V, nseg, D.segA, D.segB, need_sum, s);
+    __syncthreads();
+    float mx = -INFINITY;
+    for (int j = tid; j < nseg; j += NT) mx = fmaxf(mx, D.segA[j]);
+    const float m = block_max(mx, S.redf);
+    if (tid == 0) S.m = m;
+    __syncthreads();
+    st.m = m;
+    st.s = s;
+
+    if (!sampled) {
+        // greedy: lowest id of the maximum -- first segment holding it, then first lane slot
+        int first = 0x7fffffff;
+        for (int j = tid; j < nseg; j += NT)
+            if (D.segA[j] == m) first = min(first, j);
+        first = block_min_i(first, S.redi);
+        if (warp_id() == 0) {
+            int best = 0x7fffffff;
+            if (first != 0x7fffffff) {
+                float v[8];
+                seg_values<E, VEC>(S, row, V, first, v);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    int idx = first * SEG + lane_id() * 8 + j;
+                    if (idx < V && v[j] == m) best = min(best, idx);
+                }
+            }
+            best = warp_min_i(best);
+            if (lane_id() == 0) S.tok = best == 0x7fffffff ? 0 : best;
+        }
+        __syncthreads();
+        st.argmax = S.tok;
+        st.kind = KIND_GREEDY;
+    } else if (need_sum) {
+        // no filter: Z from the segment sums rescaled to the row max (fixed order)
+        float part = 0.f;
+        for (int j = tid; j < nseg; j += NT) {
+            float w = D.segA[j] > -INFINITY ? __fmul_rn(D.segB[j], weight(D.segA[j], m, s)) : 0.f;
+            D.segB[j] = w;
+            part += w;
+        }
+        const float Z = block_sum(part, S.redf);
+        st.Z = Z;
+        st.invZ = __frcp_rn(Z);
+        st.kind = KIND_FULL;
+        if (want_bonus) {
+            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            WKept wk{m, s, 0u};
+            st.bonus = draw_by_segments<E, VEC, false>(S, row, nullptr, V, nseg, D.segB, u, wk);
+        }
+    } else {
+        bool done = false;
+        if (S.topk_on && S.K <= KCAP) done = kept_from_candidates<E, VEC>(A, S, D, row, st, row_idx, want_bonus);
+        if (!done) kept_by_select<E, VEC>(A, S, D, row, st, row_idx, want_bonus);
+    }
+
+    // the draft of this row: p(x_i) and q(x_i)
+    if (tid == 0 && i < S.k) {
+        const int x = __ldg(A.tokens + S.d0 + i);
+        float p = 0.f, q = 0.f;
+        if (!sampled) {
+            p = NAN;
+            q = NAN;
+        } else if (x >= 0 && x < V) {
+            float z = elem_z<E>(S, row, x);
+            p = fkey(z) >= st.taukey ? __fmul_rn(weight(z, m, s), st.invZ) : 0.f;
+            q = __ldg(A.q + (size_t)(S.d0 + i) * V + x);
+        }
+        A.pq[(size_t)(S.d0 + i) * 2] = p;
+        A.pq[(size_t)(S.d0 + i) * 2 + 1] = q;
+        if (A.out_pq) {
+            A.out_pq[(size_t)(S.d0 + i) * 2] = p;
+            A.out_pq[(size_t)(S.d0 + i) * 2 + 1] = q;
+        }
+    }
+    if (tid == 0) A.stats[row_idx] = st;
+}
+
+// ------------------------------------------------------------------------------------------
+// the request phase (run by the CTA that completes the request's last row)
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ RowStat load_stat(const RowStat *p) {
+    const int4 *q = reinterpret_cast<const int4 *>(p);
+    int4 a = __ldcg(q), b = __ldcg(q + 1), c = __ldcg(q + 2);
+    RowStat st;
+    st.m = __int_as_float(a.x); st.s = __int_as_float(a.y); st.tau = __int_as_float(a.z); st.Z = __int_as_float(a.w);
+    st.invZ = __int_as_float(b.x); st.taukey = (uint32_t)b.y; st.argmax = b.z; st.bonus = b.w;
+    st.kind = c.x; st.nlist = c.y; st.pad0 = c.z; st.pad1 = c.w;
+    return st;
+}
+
+template <typename E, bool VEC, bool QVEC>
+__device__ void finalize(const Args &A, Ctx &S, const Dyn &D) {
+    const int tid = threadIdx.x;
+    const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
+    if (tid == 0) {
+        int status = S.status;
+        if (status == 0) {
+            for (int i = 0; i < k && status == 0; i++) {
+                int x = __ldg(A.tokens + d0 + i);
+                if (x < 0 || x >= V) status = 2;
+            }
+        }
+        if (status == 0 && !S.greedy) {
+            for (int i = 0; i <= k && status == 0; i++)
+                for (int t = 0; t < 2; t++) {
+                    float u = __ldg(A.uni + (size_t)(r0 + i) * 2 + t);
+                    if (!(u >= 0.f && u < 1.f)) status = 5;
+                }
+        }
+        int a = -1, tok = -1, need = 0;
+        if (status) {
+            record_error(A, status, b);
+        } else if (S.greedy) {
+            a = k;
+            for (int i = 0; i < k; i++) {
+                RowStat st = load_stat(A.stats + r0 + i);
+                if (__ldg(A.tokens + d0 + i) != st.argmax) {
+                    a = i;
+                    break;
+                }
+            }
+            tok = load_stat(A.stats + r0 + a).argmax;
+        } else {
+            a = k;
+            for (int i = 0; i < k; i++) {
+                float p = __ldcg(A.pq + (size_t)(d0 + i) * 2), q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
+                float u = __ldg(A.uni + (size_t)(r0 + i) * 2);
+                bool accept;
+                if (p > 0.f && q == 0.f) {
+                    accept = true;
+                } else if (p > 0.f) {
+                    float ratio = __fdiv_rn(p, q);
+                    float thr = ratio < 1.f ? ratio : 1.f;
+                    accept = u < thr;
+                } else {
+                    accept = false;
+                }
+                if (!accept) {
+                    a = i;
+                    break;
+                }
+            }
+            if (a == k) tok = load_stat(A.stats + r0 + k).bonus;
+            else need = 1;
+        }
+        S.a = a;
+        S.tok = tok;
+        S.need_resid = need;
+    }
+    __syncthreads();
+    if (S.need_resid) {
+        // residual max(0, p - q) at the rejected row a ("Speculative Decoding in Custom LLM
+        // Servicing...", "The Memory Bandwidth Wall and Speculative Math")
+        const int a = S.a;
+        const RowStat st = load_stat(A.stats + r0 + a);
+        const float *qrow = A.q + (size_t)(d0 + a) * V;
+        const float u = __ldg(A.uni + (size_t)(r0 + a) * 2 + 1);
+        int tok = -1;
+        if (st.kind == KIND_LIST) {
+            const int n = st.nlist;
+            const int32_t *L = A.lists + (size_t)(r0 + a) * LCAP * 2;
+            for (int j = tid; j < n; j += NT) {
+                int x = __ldcg(L + 2 * j);
+                float p = __fmul_rn(__int_as_float(__ldcg(L + 2 * j + 1)), st.invZ);
+                float q = __ldg(qrow + x);
+                D.aux[j] = fmaxf(__fsub_rn(p, q), 0.f);
+                reinterpret_cast<int *>(D.cand)[j] = x;
+            }
+            __syncthreads();
+            int j = draw_small(D.aux, D.aux2, n, u, S);
+            if (j < 0) {   // empty residual: draw from p
+                for (int jj = tid; jj < n; jj += NT)
+                    D.aux[jj] = __fmul_rn(__int_as_float(__ldcg(L + 2 * jj + 1)), st.invZ);
+                __syncthreads();
+                j = draw_small(D.aux, D.aux2, n, u, S);
+            }
+            tok = j >= 0 ? reinterpret_cast<int *>(D.cand)[j] : -1;
+        } else {
+            if (warp_id() == 0) build_penalties(A, S, a);
+            __syncthreads();
+            const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)(r0 + a) * V;
+            WResid wr{st.m, st.s, st.invZ, st.taukey};
+            WProb wp{st.m, st.s, st.invZ, st.taukey};
+            seg_sums<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, wr, D.segC, wp);
+            tok = draw_by_segments<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, u, wr);
+            if (tok < 0) tok = draw_by_segments<E, VEC, QVEC>(S, row, nullptr, V, A.nseg, D.segC, u, wp);
+        }
+        if (tid == 0) S.tok = tok;
+        __syncthreads();
+    }
+    // outputs: accepted drafts, the final token, -1 padding
+    const int a = S.a, kw = A.k_max + 1;
+    for (int j = tid; j < kw; j += NT) {
+        int v = -1;
+        if (a >= 0) v = j < a ? __ldg(A.tokens + d0 + j) : (j == a ? S.tok : -1);
+        A.out_tok[(size_t)b * kw + j] = v;
+    }
+    if (tid == 0) {
+        A.acc[b] = a;
+        A.counters[b] = 0;
+    }
+}
+
+// Writes -1 outputs for a request that owns no rows (inconsistent row_offsets).
+__device__ __forceinline__ void fail_request(const Args &A, int b) {
+    const int kw = A.k_max + 1;
+    for (int j = threadIdx.x; j < kw; j += NT) A.out_tok[(size_t)b * kw + j] = -1;
+    if (threadIdx.x == 0) {
+        A.acc[b] = -1;
+        record_error(A, 1, b);
+    }
+}
+
+template <typename E, bool VEC, bool QVEC>
+__global__ void __launch_bounds__(NT, 2) verify_kernel(const Args A) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __shared__ Ctx S;
+    const int tid = threadIdx.x;
+    const int r = blockIdx.x;
+    const Dyn D = carve(dsm, A.nseg);
+
+    // locate the row: request b, row i within it
+    if (tid < 32) {
+        int b, r0, nrows;
+        bool ok = true;
+        if (A.row_off) {
+            b = find_request(A.row_off, A.B, r);
+            ok = b >= 0 && b < A.B;
+            r0 = ok ? __ldg(A.row_off + b) : 0;
+            int r1 = ok ? __ldg(A.row_off + b + 1) : 0;
+            ok = ok && r0 <= r && r < r1;
+            nrows = r1 - r0;
+        } else {
+            b = r / (A.k_max + 1);
+            r0 = b * (A.k_max + 1);
+            nrows = A.k_max + 1;
+        }
+        if (tid == 0) {
+            S.r0 = r0;
+            S.nrows = nrows;
+            S.i = r - r0;
+            S.d0 = r0 - b;
+            if (ok) {
+                load_request(A, S, b);
+            } else {
+                S.b = -1;
+                S.status = 1;
+                record_error(A, 1, b < 0 ? 0 : (b >= A.B ? A.B - 1 : b));
+            }
+            S.active = ok && S.status == 0 && S.i <= S.k;
+        }
+    }
+    __syncthreads();
+    if (S.b < 0) return;   // row outside every request: nothing to count
+
+    // requests with no rows (row_offsets[j] == row_offsets[j+1]) are failed by the first row
+    // of the nearest non-empty request before them; leading ones by the request of row 0
+    if (A.row_off && S.i == 0) {
+        if (r == 0) {
+            for (int j = S.b - 1; j >= 0; j--) fail_request(A, j);
+        }
+        for (int j = S.b + 1; j < A.B && __ldg(A.row_off + j) == __ldg(A.row_off + j + 1); j++) fail_request(A, j);
+    }
+
+    if (S.active) {
+        if (tid < 32) build_penalties(A, S, S.i);
+        __syncthreads();
+        row_phase<E, VEC>(A, S, D, r);
+    }
+
+    // arrival: the CTA that brings the count to the request's row count finalises it
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        int old = atomicAdd(A.counters + S.b, 1);
+        S.last = (old == S.nrows - 1);
+    }
+    __syncthreads();
+    if (S.last) {
+        __threadfence();
+        finalize<E, VEC, QVEC>(A, S, D);
+    }
+}
+
+__global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *nd, int B, int32_t *hdr) {
+    int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    long long L = kv[b], k = nd[b], a = acc[b];
+    long long t = L - (k + 1) + 1 + a;   // keep 1 + accepted of the k+1 appended rows
+    if (k < 0 || a < 0 || a > k || t < 0 || t > L) {
+        atomicCAS(hdr, 0, 1);
+        atomicMax(hdr + 1, INT_MAX - b);
+        return;
+    }
+    kv[b] = (int32_t)t;
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+
+template <typename E, bool VEC, bool QVEC>
+static cudaError_t launch(const Args &A, cudaStream_t stream) {
+    static size_t smem_set = 0;   // largest dynamic shared memory size enabled so far
+    const size_t smem = dyn_bytes(A.nseg);
+    auto kern = verify_kernel<E, VEC, QVEC>;
+    if (smem > 48 * 1024 && smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    kern<<<A.R, NT, smem, stream>>>(A);
+    return cudaGetLastError();
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V) {
+    if (B < 1 || total_rows < B || V < 1) return 0;
+    return ws_layout(B, total_rows).total;
+}
+
+extern "C" const char *sv_status_string(sv_status s) {
+    switch (s) {
+        case SV_OK: return "ok";
+        case SV_ERR_INVALID_ARG: return "invalid argument";
+        case SV_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case SV_ERR_CUDA: return "CUDA runtime error";
+        case SV_ERR_UNSUPPORTED: return "unsupported shape";
+        case SV_ERR_DEVICE_DATA: return "invalid device data";
+    }
+    return "unknown status";
+}
+
+extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                                 const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
+                                 int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                                 const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 1 || k_max < 0 || V < 1 || total_rows < B) return SV_ERR_INVALID_ARG;
+    if (k_max > MAXK || V > MAXV) return SV_ERR_UNSUPPORTED;
+    if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+    if (!row_offsets && (long long)total_rows != (long long)B * (k_max + 1)) return SV_ERR_INVALID_ARG;
+    const int D = total_rows - B;
+    if (!target_logits || !num_drafts || !uniforms || !out_tokens || !accept_len || !workspace) return SV_ERR_INVALID_ARG;
+    if (D > 0 && (!draft_probs || !draft_tokens)) return SV_ERR_INVALID_ARG;
+    if (!params.temperature || !params.top_k || !params.top_p || !params.greedy) return SV_ERR_INVALID_ARG;
+    if ((long long)total_rows * V > (1ll << 62)) return SV_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(B, total_rows);
+    if (((uintptr_t)workspace & 255) != 0 || workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+
+    char *ws = static_cast<char *>(workspace);
+    Args A;
+    A.logits = target_logits;
+    A.q = draft_probs;
+    A.tokens = draft_tokens;
+    A.nd = num_drafts;
+    A.row_off = row_offsets;
+    A.T = params.temperature;
+    A.topk = params.top_k;
+    A.topp = params.top_p;
+    A.pres = params.presence_penalty;
+    A.freq = params.frequency_penalty;
+    A.greedy = params.greedy;
+    A.uni = uniforms;
+    A.out_tok = out_tokens;
+    A.acc = accept_len;
+    A.out_pq = out_pq;
+    A.hdr = reinterpret_cast<int32_t *>(ws);
+    A.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+    A.stats = reinterpret_cast<RowStat *>(ws + L.stats);
+    A.pq = reinterpret_cast<float *>(ws + L.pq);
+    A.lists = reinterpret_cast<int32_t *>(ws + L.lists);
+    A.B = B;
+    A.k_max = k_max;
+    A.V = V;
+    A.R = total_rows;
+    A.nseg = (V + SEG - 1) / SEG;
+    const size_t esz = logits_dtype == SV_BF16 ? 2 : 4;
+    const bool vec = ((uintptr_t)target_logits % 16 == 0) && ((size_t)V * esz) % 16 == 0;
+    const bool qvec = (!draft_probs || (uintptr_t)draft_probs % 16 == 0) && ((size_t)V * 4) % 16 == 0;
+    A.q_vec = qvec;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // clear the error word and the per-request arrival counters
+    if (cudaMemsetAsync(ws, 0, L.counters + (size_t)B * 4, st) != cudaSuccess) return SV_ERR_CUDA;
+    cudaError_t e;
+    if (logits_dtype == SV_BF16) {
+        if (vec) e = qvec ? launch<uint16_t, true, true>(A, st) : launch<uint16_t, true, false>(A, st);
+        else e = qvec ? launch<uint16_t, false, true>(A, st) : launch<uint16_t, false, false>(A, st);
+    } else {
+        if (vec) e = qvec ? launch<float, true, true>(A, st) : launch<float, true, false>(A, st);
+        else e = qvec ? launch<float, false, true>(A, st) : launch<float, false, false>(A, st);
+    }
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status spec_rollback(int32_t *kv_seq_len, const int32_t *accept_len, const int32_t *num_drafts,
+                                   int32_t B, void *workspace, void *stream) {
+    if (B < 1 || !kv_seq_len || !accept_len || !num_drafts || !workspace) return SV_ERR_INVALID_ARG;
+    if (((uintptr_t)workspace & 255) != 0) return SV_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int threads = 256;
+    rollback_kernel<<<(B + threads - 1) / threads, threads, 0, st>>>(kv_seq_len, accept_len, num_drafts, B,
+                                                                     reinterpret_cast<int32_t *>(workspace));
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status sv_read_device_error(const void *workspace, int32_t *code, int32_t *first_bad_request) {
+    if (!workspace) return SV_ERR_INVALID_ARG;
+    int32_t h[2] = {0, 0};
+    if (cudaMemcpy(h, workspace, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ERR_CUDA;
+    if (code) *code = h[0];
+    if (first_bad_request) *first_bad_request = h[1] ? INT_MAX - h[1] : -1;
+    return h[0] ? SV_ERR_DEVICE_DATA : SV_OK;
+}

@@ -1,0 +1,264 @@
+// sv_block.cuh -- warp/block primitives used by the row kernel: deterministic reductions and
+// scans (fixed association, so repeated runs are bitwise identical), order keys for floats,
+// a shared-memory bitonic sort, vectorised row loads and the token-weight function.
+#pragma once
+
+#include "sv_common.cuh"
+
+namespace sv {
+
+__device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+__device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
+
+// 2^x via the SFU (ex2.approx, flush-to-zero); 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Token weight e = 2^((z - m) * s), rounded the same way at every call site.
+__device__ __forceinline__ float weight(float z, float m, float s) {
+    return ex2(__fmul_rn(__fsub_rn(z, m), s));
+}
+
+// Order-preserving uint32 key of a float: a < b  <=>  fkey(a) < fkey(b) (for non-NaN).
+__device__ __forceinline__ uint32_t fkey(float z) {
+    uint32_t b = __float_as_uint(z);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide reductions over all NT threads; every thread gets the result.  `red` is a
+// shared scratch of NWARP words; the partials are combined in warp order (deterministic).
+__device__ __forceinline__ float block_max(float v, float *red) {
+    v = warp_max(v);
+    if (lane_id() == 0) red[warp_id()] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < NWARP; w++) r = fmaxf(r, red[w]);
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    v = warp_sum(v);
+    if (lane_id() == 0) red[warp_id()] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < NWARP; w++) r += red[w];
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ int block_min_i(int v, int *red) {
+    v = warp_min_i(v);
+    if (lane_id() == 0) red[warp_id()] = v;
+    __syncthreads();
+    int r = red[0];
+#pragma unroll
+    for (int w = 1; w < NWARP; w++) r = min(r, red[w]);
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ int block_max_i(int v, int *red) {
+    v = warp_max_i(v);
+    if (lane_id() == 0) red[warp_id()] = v;
+    __syncthreads();
+    int r = red[0];
+#pragma unroll
+    for (int w = 1; w < NWARP; w++) r = max(r, red[w]);
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ int block_sum_i(int v, int *red) {
+    v = warp_sum_i(v);
+    if (lane_id() == 0) red[warp_id()] = v;
+    __syncthreads();
+    int r = 0;
+#pragma unroll
+    for (int w = 0; w < NWARP; w++) r += red[w];
+    __syncthreads();
+    return r;
+}
+
+// In-place inclusive prefix sum of a[0..n) in shared memory.  Thread t sums a contiguous
+// chunk; chunk totals are scanned across lanes and warps in a fixed order, so the result is
+// deterministic.  a[n-1] ends up holding the total.
+__device__ __forceinline__ void block_scan_incl(float *a, int n, float *red) {
+    const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+    const int per = (n + NT - 1) / NT;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    float t = 0.f;
+    for (int j = lo; j < hi; j++) t += a[j];
+    float incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    float run = 0.f;
+    for (int w = 0; w < warp; w++) run += red[w];
+    run += excl;
+    for (int j = lo; j < hi; j++) {
+        run += a[j];
+        a[j] = run;
+    }
+    __syncthreads();
+}
+
+// Sorts keys[0..np) (np a power of two) into descending order.
+__device__ __forceinline__ void block_sort_desc(unsigned long long *keys, int np) {
+    for (int k = 2; k <= np; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int t = threadIdx.x; t < (np >> 1); t += NT) {
+                int i1 = (t / j) * 2 * j + (t % j);
+                int i2 = i1 + j;
+                unsigned long long a = keys[i1], b = keys[i2];
+                bool desc = (i1 & k) == 0;
+                if (desc ? (a < b) : (a > b)) {
+                    keys[i1] = b;
+                    keys[i2] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ int pow2_at_least(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+// ------------------------------------------------------------------------------------------
+// row loads: 8 consecutive elements per lane; elements at or beyond V read as -inf
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+template <typename E>
+struct Raw8;
+
+template <>
+struct Raw8<uint16_t> {   // 8 x bf16
+    uint4 a;
+};
+template <>
+struct Raw8<float> {      // 8 x fp32
+    uint4 a, b;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) { return lo | (hi << 16); }
+
+template <bool VEC>
+__device__ __forceinline__ Raw8<uint16_t> load_raw8(const uint16_t *row, int base, int V) {
+    Raw8<uint16_t> r;
+    if (VEC && base + 8 <= V) {
+        r.a = ld_stream_v4(row + base);
+    } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) h[j] = (base + j < V) ? (uint32_t)__ldg(row + base + j) : 0xFF80u;
+        r.a = make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]),
+                         pack_bf16(h[6], h[7]));
+    }
+    return r;
+}
+
+template <bool VEC>
+__device__ __forceinline__ Raw8<float> load_raw8(const float *row, int base, int V) {
+    Raw8<float> r;
+    if (VEC && base + 8 <= V) {
+        r.a = ld_stream_v4(row + base);
+        r.b = ld_stream_v4(row + base + 4);
+    } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) h[j] = (base + j < V) ? __float_as_uint(__ldg(row + base + j)) : 0xFF800000u;
+        r.a = make_uint4(h[0], h[1], h[2], h[3]);
+        r.b = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void unpack8(const Raw8<uint16_t> &r, float v[8]) {
+    const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ void unpack8(const Raw8<float> &r, float v[8]) {
+    v[0] = __uint_as_float(r.a.x);
+    v[1] = __uint_as_float(r.a.y);
+    v[2] = __uint_as_float(r.a.z);
+    v[3] = __uint_as_float(r.a.w);
+    v[4] = __uint_as_float(r.b.x);
+    v[5] = __uint_as_float(r.b.y);
+    v[6] = __uint_as_float(r.b.z);
+    v[7] = __uint_as_float(r.b.w);
+}
+
+// fp32 draft-probability row: 8 values from base (0 beyond V).
+template <bool VEC>
+__device__ __forceinline__ void load_q8(const float *row, int base, int V, float v[8]) {
+    if (VEC && base + 8 <= V) {
+        uint4 a = ld_stream_v4(row + base), b = ld_stream_v4(row + base + 4);
+        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+        v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+        v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+        v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = (base + j < V) ? __ldg(row + base + j) : 0.f;
+    }
+}
+
+__device__ __forceinline__ float max8(const float v[8]) {
+    float a = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+    float b = fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7]));
+    return fmaxf(a, b);
+}
+
+}  // namespace sv

@@ -1,0 +1,212 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI.
+
+Small batches are compared in full; the workloads at their measured sizes are compared on a
+sample of requests the oracle computes one by one, plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+
+import sv_workloads as W
+from sv_parity import check_invariants, compare
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_12_gb300 as sv
+    sv.lib()    # fails loudly when the library was not built
+    return sv
+
+
+def run_gpu(w, want_pq=True):
+    from speculative_decoding_verification_12_gb300.batch import DeviceBatch
+    db = DeviceBatch.from_host(w, "cuda", want_pq=want_pq)
+    db.run()
+    return db.results(), db
+
+
+def full_compare(oracle_lib, w, check_share=False):
+    g, db = run_gpu(w)
+    o = oracle_lib.verify(w, threads=8)
+    check_invariants_valid(w, g, o)
+    return compare(w, g, o, check_share=check_share), g, o, db
+
+
+def check_invariants_valid(w, g, o):
+    ok = np.nonzero(o["error"] == 0)[0]
+    sub = w
+    for b in ok:
+        a = int(g["accept_len"][b])
+        assert 0 <= a <= int(w.num_drafts[b])
+
+
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_greedy"])
+def test_tiny_case(sv, oracle_lib, name):
+    w = W.make(name)
+    s, g, o, _ = full_compare(oracle_lib, w)
+    assert s["requests"] == 1
+
+
+RANDOM_CASES = [
+    # seed, B, k_max, V, dtype, varlen, tie_step, greedy_frac
+    (0, 16, 4, 1000, "f32", False, 0.0, 0.3),
+    (1, 24, 6, 4099, "bf16", True, 0.0, 0.3),     # odd V: unaligned rows, ragged tail segment
+    (2, 20, 8, 3000, "bf16", False, 0.5, 0.2),    # forced ties at top-k / top-p boundaries
+    (3, 12, 3, 255, "f32", True, 0.0, 0.5),       # less than one segment
+    (4, 8, 5, 1, "f32", False, 0.0, 0.5),         # V = 1
+    (5, 10, 2, 7, "bf16", True, 0.25, 0.3),
+    (6, 32, 8, 20001, "bf16", True, 0.0, 0.3),
+    (7, 16, 7, 65536, "f32", False, 0.125, 0.25),
+    (8, 40, 1, 513, "bf16", False, 0.0, 0.0),
+    (9, 6, 64, 300, "f32", True, 0.0, 0.3),      # k_max = 64
+]
+
+
+@pytest.mark.parametrize("case", RANDOM_CASES, ids=[f"seed{c[0]}_V{c[3]}_{c[4]}" for c in RANDOM_CASES])
+def test_random_batches(sv, oracle_lib, case):
+    seed, B, k, V, dt, varlen, tie, gf = case
+    w = W.random_batch(seed, B=B, k_max=k, V=V, dtype=dt, varlen=varlen, tie_step=tie, greedy_frac=gf)
+    full_compare(oracle_lib, w)
+
+
+def test_large_top_k_and_top_p_only_paths(sv, oracle_lib):
+    """top-k above the candidate cap and top-p without top-k take the radix-select path."""
+    w = W.random_batch(21, B=24, k_max=4, V=9000, dtype="bf16", greedy_frac=0.0)
+    w.top_k[:12] = 3000
+    w.top_p[:12] = 0.7
+    w.top_k[12:] = 0
+    w.top_p[12:] = np.linspace(0.05, 0.99, 12).astype(np.float32)
+    full_compare(oracle_lib, w)
+
+
+def test_candidate_overflow_falls_back(sv, oracle_lib):
+    """All-equal rows: every token ties for the top-k set, overflowing the candidate buffer."""
+    w = W.random_batch(22, B=6, k_max=3, V=5000, dtype="bf16", greedy_frac=0.0)
+    w.target_logits[:] = W.f32_to_bf16_bits(np.full((w.total_rows, w.V), 0.5, np.float32))
+    w.top_k[:] = 10
+    w.top_p[:] = np.array([1.0, 0.5, 0.999, 1.0, 0.1, 0.9], np.float32)
+    full_compare(oracle_lib, w)
+
+
+def test_zero_drafts_and_padding_rows(sv, oracle_lib):
+    w = W.random_batch(23, B=30, k_max=5, V=2000, dtype="bf16", greedy_frac=0.3)
+    w.num_drafts[::3] = 0          # uniform layout with unused (padding) rows
+    w.num_drafts[1::3] = 2
+    full_compare(oracle_lib, w)
+
+
+def test_q_equals_p_and_disjoint_supports(sv, oracle_lib):
+    V, k, B = 64, 4, 40
+    g = np.random.default_rng(5)
+    logits = np.zeros((k + 1, V), np.float32)
+    q = np.full((k, V), 1.0 / V, np.float32)
+    w = W.from_rows(V, logits, q, g.integers(0, V, (B, k)).astype(np.int32),
+                    g.random((B, k + 1, 2), dtype=np.float32))
+    s, gg, o, _ = full_compare(oracle_lib, w)
+    assert (gg["accept_len"] == k).all()
+    z = np.full(V, -30.0, np.float32)
+    z[:2] = [5.0, 4.0]
+    qd = np.zeros(V, np.float32)
+    qd[2:] = 1.0 / (V - 2)
+    w = W.from_rows(V, np.tile(z, (k + 1, 1)), np.tile(qd, (k, 1)), g.integers(2, V, (B, k)).astype(np.int32),
+                    g.random((B, k + 1, 2), dtype=np.float32), top_k=2)
+    s, gg, o, _ = full_compare(oracle_lib, w)
+    assert (gg["accept_len"] == 0).all()
+
+
+def test_device_data_errors(sv, oracle_lib):
+    w = W.random_batch(24, B=10, k_max=3, V=500, dtype="f32", greedy_frac=0.0)
+    w.draft_tokens[1] = 500
+    w.temperature[1] = -1.0
+    w.top_p[2] = 0.0
+    w.uniforms[3 * 4 + 2, 1] = 1.0
+    w.num_drafts[4] = 9
+    s, g, o, db = full_compare(oracle_lib, w)
+    code, bad = sv.sv_read_device_error(db.workspace)
+    assert code != 0 and bad == 0
+    assert (g["accept_len"][:5] == -1).all() and (g["accept_len"][5:] >= 0).all()
+
+
+def test_deterministic_repeat(sv):
+    w = W.random_batch(25, B=40, k_max=6, V=30000, dtype="bf16", varlen=True)
+    g1, db = run_gpu(w)
+    db.run()
+    g2 = db.results()
+    for key in g1:
+        assert np.array_equal(g1[key], g2[key], equal_nan=True), key
+
+
+def test_unaligned_pointers(sv, oracle_lib):
+    """Logit and draft rows that start off a 16-byte boundary take the scalar-load path."""
+    from speculative_decoding_verification_12_gb300.batch import DeviceBatch
+    w = W.random_batch(26, B=8, k_max=3, V=1024, dtype="bf16", greedy_frac=0.2)
+    db = DeviceBatch.from_host(w, "cuda")
+    tl = torch.empty(db.target_logits.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    tl[1:] = db.target_logits.reshape(-1)
+    dp = torch.empty(db.draft_probs.numel() + 1, dtype=torch.float32, device="cuda")
+    dp[1:] = db.draft_probs.reshape(-1)
+    db.run(target_logits=tl[1:].view(w.total_rows, w.V), draft_probs=dp[1:].view(-1, w.V))
+    g = db.results()
+    compare(w, g, oracle_lib.verify(w))
+
+
+def test_rollback_matches_closed_form(sv, oracle_lib):
+    g = np.random.default_rng(3)
+    B = 1000
+    k = g.integers(0, 9, B).astype(np.int32)
+    a = np.minimum(g.integers(0, 9, B), k).astype(np.int32)
+    L = g.integers(10, 5000, B).astype(np.int32)
+    a[5] = k[5] + 1          # accept_len beyond k: rejected, length kept
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    kv = torch.from_numpy(L).cuda()
+    sv.spec_rollback(kv, torch.from_numpy(a).cuda(), torch.from_numpy(k).cuda(), ws)
+    ref, nerr = oracle_lib.rollback(L, a, k)
+    got = kv.cpu().numpy()
+    ok = ref >= 0
+    assert np.array_equal(got[ok], ref[ok]) and got[5] == L[5] and nerr == 1
+    assert sv.sv_read_device_error(ws)[0] == 1
+
+
+# ------------------------------------------------------------------------------------------
+# the measured workloads: full compare where the oracle is quick, sampled otherwise
+# ------------------------------------------------------------------------------------------
+
+def _sampled(oracle_lib, name, n_sample, seed=0):
+    w = W.make(name)
+    g, _ = run_gpu(w)
+    check_invariants(w, g)
+    rng = np.random.default_rng(seed)
+    reqs = np.sort(rng.choice(w.B, size=min(n_sample, w.B), replace=False))
+    o = oracle_lib.verify(w, requests=reqs, threads=16)
+    s = compare(w, g, o, requests=reqs, check_share=True)
+    print(name, s)
+    return s, g, w
+
+
+def test_peaks_b64_k5_v32000_full(sv, oracle_lib):
+    w = W.make("peaks")
+    s, g, o, _ = full_compare(oracle_lib, w, check_share=True)
+    acc = g["accept_len"].mean() / 5
+    assert 0.2 < acc < 1.0
+
+
+def test_zipf_b256_k4_v128256_sampled(sv, oracle_lib):
+    s, g, w = _sampled(oracle_lib, "zipf", 48)
+    assert s["requests"] >= 40
+
+
+def test_ragged_b512_v151936_sampled(sv, oracle_lib):
+    s, g, w = _sampled(oracle_lib, "ragged", 64)
+    assert s["requests"] >= 50
+
+
+def test_stream_b1024_k7_v128256_sampled(sv, oracle_lib):
+    s, g, w = _sampled(oracle_lib, "stream", 12)
+    assert s["requests"] >= 10
