@@ -182,16 +182,32 @@ static int32_t row_argmax(const double *z, int32_t V, int penalised, int *near) 
     return best;
 }
 
+/* Where an fp32 implementation may legitimately draw a row's kept set differently: the
+ * z/T interval [lo, hi] of the value levels whose membership sits on a near-tie (lo > hi:
+ * none), and their total mass as a share of the final kept mass. */
+typedef struct row_amb {
+    double lo, hi, mass;
+} row_amb;
+
+static void amb_add(row_amb *a, double level) {
+    if (a->lo > a->hi) { a->lo = level; a->hi = level; return; }
+    if (level < a->lo) a->lo = level;
+    if (level > a->hi) a->hi = level;
+}
+
 /* Sampled row [R2][F1]: p = softmax(z / T) restricted to top-k, then to top-p, renormalised.
- * Writes p[0..V).  *decisions/*near count the filter thresholds of the row.  Returns the
- * number of tokens kept. */
+ * Writes p[0..V).  *decisions counts the filter thresholds of the row; *amb receives the
+ * near-tie band of the cut.  Returns the number of tokens kept. */
 static int32_t row_probs(const sv_oracle_batch *in, int32_t b, const double *z, int penalised,
-                         double *p, double *scratch, int *decisions, int *near) {
+                         double *p, double *scratch, int *decisions, row_amb *amb) {
     const int32_t V = in->V;
     const double T = in->temperature[b];
     const int32_t K = in->top_k[b];
     const double P = in->top_p[b];
     double *zs = scratch; /* V doubles */
+    amb->lo = 1.0;
+    amb->hi = 0.0;
+    amb->mass = 0.0;
 
     for (int32_t v = 0; v < V; v++) p[v] = z[v] / T;          /* p[] holds z' for now */
     double m = p[0];
@@ -204,9 +220,12 @@ static int32_t row_probs(const sv_oracle_batch *in, int32_t b, const double *z, 
         qsort(zs, V, sizeof(double), cmp_desc);
         tau = zs[K - 1];
         (*decisions)++;
-        if (penalised) {
+        if (penalised) {   /* values near the cut may order differently in fp32 */
             for (int32_t j = K; j < V; j++)
-                if (zs[j] < tau) { if (close_rel(tau, zs[j])) (*near)++; break; }
+                if (zs[j] < tau) {
+                    if (close_rel(tau, zs[j])) { amb_add(amb, tau); amb_add(amb, zs[j]); }
+                    break;
+                }
         }
     }
     /* unnormalised weights of the top-k set */
@@ -219,33 +238,29 @@ static int32_t row_probs(const sv_oracle_batch *in, int32_t b, const double *z, 
         int32_t n = 0;
         for (int32_t v = 0; v < V; v++) if (p[v] >= tau) zs[n++] = p[v];
         qsort(zs, n, sizeof(double), cmp_desc);
-        double above = 0.0, last_kept = zs[0], above_last_kept = 0.0;
+        double above = 0.0, last_kept = zs[0];
         int32_t j = 0;
-        int have_excl = 0;
-        double above_excl = 0.0, first_excl = 0.0;
+        int cut = 0;
+        double first_excl = 0.0;
         while (j < n) {
             double level = zs[j];
             int32_t c = 0;
             while (j + c < n && zs[j + c] == level) c++;
-            if (above / ZK < P) {
+            double lm = (double)c * exp(level - m);
+            /* near-tie: either end of this level's cumulative mass within 1e-5 of top_p */
+            if (fabs(above / ZK - P) < NEAR_TOL || fabs((above + lm) / ZK - P) < NEAR_TOL) amb_add(amb, level);
+            if (!cut && above / ZK < P) {
                 last_kept = level;
-                above_last_kept = above;
-                above += (double)c * exp(level - m);
-                j += c;
-            } else {
-                have_excl = 1;
-                above_excl = above;
+            } else if (!cut) {
+                cut = 1;
                 first_excl = level;
-                break;
+                if (penalised && close_rel(last_kept, first_excl)) { amb_add(amb, last_kept); amb_add(amb, first_excl); }
             }
+            if (cut && above / ZK - P >= NEAR_TOL) break;   /* past the band */
+            above += lm;
+            j += c;
         }
         (*decisions)++;
-        int nt = fabs(above_last_kept / ZK - P) < NEAR_TOL;
-        if (have_excl) {
-            nt |= fabs(above_excl / ZK - P) < NEAR_TOL;
-            if (penalised) nt |= close_rel(last_kept, first_excl);
-        }
-        if (nt) (*near)++;
         tau = last_kept;
     }
     double Z = 0.0;
@@ -253,9 +268,17 @@ static int32_t row_probs(const sv_oracle_batch *in, int32_t b, const double *z, 
     for (int32_t v = 0; v < V; v++) {
         if (p[v] >= tau) { Z += exp(p[v] - m); kept++; }
     }
+    if (amb->lo <= amb->hi) {
+        double am = 0.0;
+        for (int32_t v = 0; v < V; v++)
+            if (p[v] >= amb->lo && p[v] <= amb->hi) am += exp(p[v] - m);
+        amb->mass = am / Z;
+    }
     for (int32_t v = 0; v < V; v++) p[v] = (p[v] >= tau) ? exp(p[v] - m) / Z : 0.0;
     return kept;
 }
+
+static int in_amb(const row_amb *a, double zprime) { return a->lo <= a->hi && zprime >= a->lo && zprime <= a->hi; }
 
 /* Inverse CDF over w[0..V) in token-index order [R1]: the smallest v whose running sum is
  * > u * W, where W is the running sum's total; the largest positive-weight v if rounding
@@ -328,14 +351,17 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
     } else {
         for (int32_t i = 0; i <= k; i++) {
             int pen = row_logits(in, b, i, z);
-            int dec = 0, nt = 0;
-            row_probs(in, b, z, pen, p, scratch, &dec, &nt);
+            int dec = 0;
+            row_amb amb;
+            row_probs(in, b, z, pen, p, scratch, &dec, &amb);
             if (i < k) {
                 int32_t x = drafts[i];
                 double px = p[x];
                 double qx = (double)in->draft_probs[(d0 + i) * (int64_t)V + x];
+                /* the draft's own membership in the kept set is on a near-tie */
+                int nt = in_amb(&amb, z[x] / in->temperature[b]);
                 if (out_pq) { out_pq[(d0 + i) * 2] = px; out_pq[(d0 + i) * 2 + 1] = qx; }
-                if (pq_near) pq_near[d0 + i] = (uint8_t)(nt > 0);
+                if (pq_near) pq_near[d0 + i] = (uint8_t)nt;
                 if (decided) continue;
                 d.decisions += dec + 1;
                 d.near_ties += nt;
@@ -369,6 +395,8 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                         token = inverse_cdf(p, V, u1, &cn);   /* empty residual: draw from p */
                     }
                     if (W < NEAR_W) { cn = 1; d.near_w++; } else { d.near_cdf += cn; }
+                    /* tokens of ambiguous membership could shift the running sums */
+                    if (!cn && amb.mass >= NEAR_TOL * (W > 0.0 ? W : 1.0)) { cn = 1; d.near_filter++; }
                     d.decisions++;
                     d.near_ties += cn;
                     a = i;
@@ -378,11 +406,10 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                 /* [R2] every draft accepted: the extra token comes from row k */
                 int cn = 0;
                 d.decisions += dec + 1;
-                d.near_ties += nt;
-                d.near_filter += nt;
                 token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], &cn);
-                d.near_ties += cn;
                 d.near_cdf += cn;
+                if (!cn && amb.mass >= NEAR_TOL) { cn = 1; d.near_filter++; }
+                d.near_ties += cn;
                 a = k;
                 decided = 1;
             }
@@ -427,8 +454,9 @@ int32_t sv_oracle_row_probs(const sv_oracle_batch *in, int32_t b, int32_t i, dou
         p[g] = 1.0;
         kept = 1;
     } else {
-        int dec = 0, nt = 0;
-        kept = row_probs(in, b, buf, pen, p, buf + V, &dec, &nt);
+        int dec = 0;
+        row_amb amb;
+        kept = row_probs(in, b, buf, pen, p, buf + V, &dec, &amb);
     }
     free(buf);
     return kept;
@@ -442,8 +470,9 @@ int32_t sv_oracle_residual(const sv_oracle_batch *in, int32_t b, int32_t i, doub
     double *buf = (double *)malloc(sizeof(double) * V * 3);
     if (!buf) return -2;
     int pen = row_logits(in, b, i, buf);
-    int dec = 0, nt = 0;
-    row_probs(in, b, buf, pen, buf + V, buf + 2 * V, &dec, &nt);
+    int dec = 0;
+    row_amb amb;
+    row_probs(in, b, buf, pen, buf + V, buf + 2 * V, &dec, &amb);
     const float *q = in->draft_probs + (row_start(in, b) - b + i) * (int64_t)in->V;
     double W = 0.0;
     for (size_t v = 0; v < V; v++) {

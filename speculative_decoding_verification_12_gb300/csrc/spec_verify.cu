@@ -36,6 +36,7 @@ struct Dyn {
     float *segA, *segB, *segC;   // per-segment max / weight sums
     unsigned long long *cand;    // CAP keys: (order key << 32) | ~token, later (~token << 32) | key
     float *aux, *aux2;           // CAP floats each
+    unsigned long long *sorted;  // WCAP keys (aliases aux/aux2)
     uint32_t *hcnt;              // radix histogram (aliases cand/aux)
     unsigned long long *hmass;   // fixed-point mass histogram (aliases)
 };
@@ -55,6 +56,7 @@ __device__ __forceinline__ Dyn carve(unsigned char *base, int nseg) {
     d.cand = reinterpret_cast<unsigned long long *>(area);
     d.aux = reinterpret_cast<float *>(area + size_t(CAP) * 8);
     d.aux2 = d.aux + CAP;
+    d.sorted = reinterpret_cast<unsigned long long *>(d.aux);
     d.hmass = reinterpret_cast<unsigned long long *>(area);                     // HB * 8 bytes
     d.hcnt = reinterpret_cast<uint32_t *>(area + size_t(HB) * 8);               // HB * 4 bytes
     return d;
@@ -69,6 +71,94 @@ __device__ __forceinline__ void record_error(const Args &A, int code, int b) {
 // the row phase
 // ------------------------------------------------------------------------------------------
 
+// Appends this lane's tokens of segment seg whose key reaches tkey to the candidate buffer
+// (warp-aggregated; entries beyond CAP are counted but not stored).
+__device__ __forceinline__ void append_candidates(Ctx &S, const Dyn &D, int seg, const float v[8], uint32_t tkey,
+                                                  int V) {
+    const int lane = lane_id();
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        int idx = seg * SEG + lane * 8 + j;
+        c += (idx < V && fkey(v[j]) >= tkey) ? 1 : 0;
+    }
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if (lane == 0 && total) base = atomicAdd(&S.ncand, total);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    int pos = base + incl - c;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        int idx = seg * SEG + lane * 8 + j;
+        uint32_t key = fkey(v[j]);
+        if (idx < V && key >= tkey) {
+            if (pos < CAP) D.cand[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)idx);
+            pos++;
+        }
+    }
+}
+
+// Warp 0: top-k cut, top-p cut and kept mass over n <= WCAP candidates sorted by value
+// (descending), 8 per lane.  Writes S.n2 (kept count), S.zk (kept mass), S.cutkey.
+__device__ __forceinline__ void warp_cut(Ctx &S, const unsigned long long *srt, int n, int K, float m, float s,
+                                         bool topp, float P) {
+    const int lane = lane_id(), base = lane * 8;
+    const int kk = min(K, n);
+    const uint32_t kkey = (uint32_t)(srt[kk - 1] >> 32);
+    uint32_t key[8];
+    int c1 = 0;
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const int idx = base + t;
+        key[t] = idx < n ? (uint32_t)(srt[idx] >> 32) : 0u;
+        c1 += (idx < n && key[t] >= kkey) ? 1 : 0;
+    }
+    const int n1 = warp_sum_i(c1);
+    float pre[8], loc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        loc += (base + t < n1) ? weight(key2f(key[t]), m, s) : 0.f;
+        pre[t] = loc;
+    }
+    float Z1;
+    const float ex = warp_excl_scan(loc, Z1);
+#pragma unroll
+    for (int t = 0; t < 8; t++) pre[t] += ex;
+    int n2 = n1;
+    if (topp) {
+        // a value level is cut when the mass strictly above it reaches P * Z1
+        const float PZ = __fmul_rn(P, Z1);
+        int cut = 0x7fffffff;
+        uint32_t prevkey = base > 0 ? (uint32_t)(srt[base - 1] >> 32) : 0u;
+        float prevpre = ex;
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const int idx = base + t;
+            if (idx > 0 && idx < n1 && key[t] != prevkey && prevpre >= PZ) cut = min(cut, idx);
+            prevkey = key[t];
+            prevpre = pre[t];
+        }
+        cut = warp_min_i(cut);
+        if (cut != 0x7fffffff) n2 = cut;
+    }
+    float zsel = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; t++)
+        if (base + t == n2 - 1) zsel = pre[t];
+    const float Z = __shfl_sync(0xffffffffu, zsel, (n2 - 1) >> 3);
+    if (lane == 0) {
+        S.n2 = n2;
+        S.zk = Z;
+        S.cutkey = (uint32_t)(srt[n2 - 1] >> 32);
+    }
+}
+
 // Kept set of a sampled row from the top-k candidates.  Returns false on candidate overflow.
 template <typename E, bool VEC>
 __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const E *row, RowStat &st, int row_idx,
@@ -76,50 +166,97 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
     const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
     const int V = A.V, nseg = A.nseg, K = S.K;
     const float m = S.m, s = S.s;
-    // lower bound: the K-th largest segment maximum (all tokens if fewer segments than K)
+    // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
     uint32_t tkey = 0;
-    if (nseg >= K) tkey = select_kth_smem(S, D.segA, nseg, K, D.hcnt);
-    if (tid == 0) S.ncand = 0;
+    if (nseg >= K) tkey = select_bound16(S, D.segA, nseg, K, D.hcnt);
+    // the segments holding a token at or above the bound, re-read (from L2) four at a time
+    int *segl = reinterpret_cast<int *>(D.segC);
+    if (tid == 0) {
+        S.nsel = 0;
+        S.ncand = 0;
+    }
     __syncthreads();
-    for (int seg = warp; seg < nseg; seg += NWARP) {
-        if (fkey(D.segA[seg]) < tkey) continue;          // warp-uniform
-        float v[8];
-        seg_values<E, VEC>(S, row, V, seg, v);
-        int c = 0;
+    for (int j = tid; j < nseg; j += NT)
+        if (fkey(D.segA[j]) >= tkey) segl[atomicAdd(&S.nsel, 1)] = j;
+    __syncthreads();
+    const int nsel = S.nsel;
+    constexpr int U = 4;
+    for (int j0 = warp; j0 < nsel; j0 += NWARP * U) {
+        Raw8<E> raw[U];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            int idx = seg * SEG + lane * 8 + j;
-            c += (idx < V && fkey(v[j]) >= tkey) ? 1 : 0;
+        for (int u = 0; u < U; u++) {
+            const int j = j0 + u * NWARP;
+            if (j < nsel) raw[u] = load_raw8<VEC>(row, segl[j] * SEG + lane * 8, V);
         }
-        int incl = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        int total = __shfl_sync(0xffffffffu, incl, 31);
-        int base = 0;
-        if (lane == 0 && total) base = atomicAdd(&S.ncand, total);
-        base = __shfl_sync(0xffffffffu, base, 0);
-        int pos = base + incl - c;
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            int idx = seg * SEG + lane * 8 + j;
-            uint32_t key = fkey(v[j]);
-            if (idx < V && key >= tkey) {
-                if (pos < CAP) D.cand[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)idx);
-                pos++;
+        for (int u = 0; u < U; u++) {
+            const int j = j0 + u * NWARP;
+            if (j < nsel) {
+                const int seg = segl[j];
+                float v[8];
+                unpack8(raw[u], v);
+                patch_seg(S, seg * SEG, v);
+                append_candidates(S, D, seg, v, tkey, V);
             }
         }
     }
     __syncthreads();
     const int n = S.ncand;
     if (n > CAP || n < 1) return false;
+
+    if (n <= WCAP) {
+        // rank sort by (value desc, token asc): keys are distinct, so ranks are a permutation
+        unsigned long long *srt = D.sorted;
+        for (int j = tid; j < n; j += NT) {
+            const unsigned long long c = D.cand[j];
+            int r = 0;
+            for (int i = 0; i < n; i++) r += D.cand[i] > c ? 1 : 0;
+            srt[r] = c;
+        }
+        __syncthreads();
+        if (warp == 0) warp_cut(S, srt, n, K, m, s, S.topp_on, S.P);
+        __syncthreads();
+        const int n2 = S.n2;
+        const float Z = S.zk;
+        st.Z = Z;
+        st.invZ = __frcp_rn(Z);
+        st.taukey = S.cutkey;
+        st.tau = key2f(S.cutkey);
+        st.kind = KIND_LIST;
+        st.nlist = n2;
+        // the kept set in token order (rank by token id), stored for the residual draw
+        int *ltok = reinterpret_cast<int *>(D.cand);
+        float *lw = reinterpret_cast<float *>(D.cand) + WCAP;
+        for (int j = tid; j < n2; j += NT) {
+            const uint32_t tj = ~(uint32_t)srt[j];
+            int r = 0;
+            for (int i = 0; i < n2; i++) r += (~(uint32_t)srt[i]) < tj ? 1 : 0;
+            ltok[r] = (int)tj;
+            lw[r] = weight(key2f((uint32_t)(srt[j] >> 32)), m, s);
+        }
+        __syncthreads();
+        int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
+        for (int j = tid; j < n2; j += NT) L[j] = make_int2(ltok[j], __float_as_int(lw[j]));
+        if (want_bonus) {
+            if (warp == 0) {
+                const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+                float w8[8];
+#pragma unroll
+                for (int t = 0; t < 8; t++) w8[t] = (lane * 8 + t < n2) ? lw[lane * 8 + t] : 0.f;
+                const int j = warp_draw8(w8, n2, u);
+                if (lane == 0) S.tok = j >= 0 ? ltok[j] : -1;
+            }
+            __syncthreads();
+            st.bonus = S.tok;
+        }
+        return true;
+    }
+
+    // larger candidate sets: block-wide bitonic sort and scans
     const int np = pow2_at_least(n);
     for (int j = n + tid; j < np; j += NT) D.cand[j] = 0ull;
     __syncthreads();
     block_sort_desc(D.cand, np);
-    // exact top-k: tokens whose key reaches the K-th largest (ties kept)
     const int kk = min(K, n);
     const uint32_t kkey = (uint32_t)(D.cand[kk - 1] >> 32);
     int c1 = 0;
@@ -130,7 +267,6 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
     for (int j = tid; j < n1; j += NT) D.aux2[j] = D.aux[j];
     __syncthreads();
     block_scan_incl(D.aux2, n1, S.redf);
-    // top-p: cut at the first value level whose mass strictly above reaches P * Z1
     int n2 = n1;
     if (S.topp_on) {
         const float PZ = __fmul_rn(S.P, D.aux2[n1 - 1]);
@@ -151,7 +287,6 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
     st.kind = n2 <= LCAP ? KIND_LIST : KIND_THRESH;
     st.nlist = n2 <= LCAP ? n2 : 0;
     __syncthreads();
-    // the kept set in token order: re-key as (~token << 32) | value key and sort again
     if (n2 <= LCAP || want_bonus) {
         const int np2 = pow2_at_least(n2);
         for (int j = tid; j < np2; j += NT) {
@@ -163,11 +298,9 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
         for (int j = tid; j < n2; j += NT) D.aux[j] = weight(key2f((uint32_t)D.cand[j]), m, s);
         __syncthreads();
         if (n2 <= LCAP) {
-            int32_t *L = A.lists + (size_t)row_idx * LCAP * 2;
-            for (int j = tid; j < n2; j += NT) {
-                L[2 * j] = (int32_t)(~(uint32_t)(D.cand[j] >> 32));
-                L[2 * j + 1] = __float_as_int(D.aux[j]);
-            }
+            int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
+            for (int j = tid; j < n2; j += NT)
+                L[j] = make_int2((int32_t)(~(uint32_t)(D.cand[j] >> 32)), __float_as_int(D.aux[j]));
         }
         if (want_bonus) {
             const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
@@ -224,9 +357,26 @@ __device__ void row_phase(const Args &A, Ctx &S, const Dyn &D, const int row_idx
         S.topk_on = sampled && S.K > 0 && S.K < V;
         S.topp_on = sampled && S.P < 1.f;
     }
+    // The last thread prefetches this row's draft token x and the values z_x, q(x) that the
+    // accept test needs; they land while the row streams and are used after it.
+    int xtok = -1;
+    E zraw = E(0);
+    float qx = 0.f;
+    if (tid == NT - 1 && i < S.k) {
+        xtok = __ldg(A.tokens + S.d0 + i);
+        if (xtok >= 0 && xtok < V) {
+            zraw = __ldg(row + xtok);
+            if (sampled) qx = __ldg(A.q + (size_t)(S.d0 + i) * V + xtok);
+        }
+    }
     __syncthreads();
     const bool need_sum = sampled && !S.topk_on && !S.topp_on;
     pass_stats<E, VEC>(S, row, V, nseg, D.segA, D.segB, need_sum, s);
+    if (tid == NT - 1) {
+        S.xtok = xtok;
+        S.zx = elem_z_raw(S, zraw, xtok);
+        S.qx = qx;
+    }
     __syncthreads();
     float mx = -INFINITY;
     for (int j = tid; j < nseg; j += NT) mx = fmaxf(mx, D.segA[j]);
@@ -284,15 +434,15 @@ __device__ void row_phase(const Args &A, Ctx &S, const Dyn &D, const int row_idx
 
     // the draft of this row: p(x_i) and q(x_i)
     if (tid == 0 && i < S.k) {
-        const int x = __ldg(A.tokens + S.d0 + i);
+        const int x = S.xtok;
         float p = 0.f, q = 0.f;
         if (!sampled) {
             p = NAN;
             q = NAN;
         } else if (x >= 0 && x < V) {
-            float z = elem_z<E>(S, row, x);
+            const float z = S.zx;
             p = fkey(z) >= st.taukey ? __fmul_rn(weight(z, m, s), st.invZ) : 0.f;
-            q = __ldg(A.q + (size_t)(S.d0 + i) * V + x);
+            q = S.qx;
         }
         A.pq[(size_t)(S.d0 + i) * 2] = p;
         A.pq[(size_t)(S.d0 + i) * 2 + 1] = q;
@@ -318,64 +468,67 @@ __device__ __forceinline__ RowStat load_stat(const RowStat *p) {
     return st;
 }
 
+// Accept test of one draft ("Speculative Decoding in Custom LLM Servicing...", "The Memory
+// Bandwidth Wall and Speculative Math"): accept with probability min(1, p/q), i.e. iff
+// u < min(1, p/q); q == 0 < p accepts and p == 0 rejects.
+__device__ __forceinline__ bool accept_test(float p, float q, float u) {
+    if (!(p > 0.f)) return false;
+    if (q == 0.f) return true;
+    const float ratio = __fdiv_rn(p, q);
+    return u < (ratio < 1.f ? ratio : 1.f);
+}
+
 template <typename E, bool VEC, bool QVEC>
 __device__ void finalize(const Args &A, Ctx &S, const Dyn &D) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
     const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
-    if (tid == 0) {
+    if (warp == 0) {
+        // one lane per draft: validate, test, and find the first rejection by ballot
         int status = S.status;
-        if (status == 0) {
-            for (int i = 0; i < k && status == 0; i++) {
-                int x = __ldg(A.tokens + d0 + i);
-                if (x < 0 || x >= V) status = 2;
-            }
-        }
-        if (status == 0 && !S.greedy) {
-            for (int i = 0; i <= k && status == 0; i++)
-                for (int t = 0; t < 2; t++) {
-                    float u = __ldg(A.uni + (size_t)(r0 + i) * 2 + t);
-                    if (!(u >= 0.f && u < 1.f)) status = 5;
-                }
-        }
         int a = -1, tok = -1, need = 0;
-        if (status) {
-            record_error(A, status, b);
-        } else if (S.greedy) {
+        if (status == 0) {
+            const bool greedy = S.greedy;
+            bool badtok = false, baduni = false;
             a = k;
-            for (int i = 0; i < k; i++) {
-                RowStat st = load_stat(A.stats + r0 + i);
-                if (__ldg(A.tokens + d0 + i) != st.argmax) {
-                    a = i;
-                    break;
+            for (int i0 = 0; i0 <= k; i0 += 32) {
+                const int i = i0 + lane;
+                bool rej = false;
+                if (i < k) {
+                    const int x = __ldg(A.tokens + d0 + i);
+                    if (x < 0 || x >= V) badtok = true;
+                    if (greedy) {
+                        rej = x != __ldcg(&A.stats[r0 + i].argmax);
+                    } else {
+                        const float p = __ldcg(A.pq + (size_t)(d0 + i) * 2);
+                        const float q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
+                        rej = !accept_test(p, q, __ldg(A.uni + (size_t)(r0 + i) * 2));
+                    }
                 }
+                if (!greedy && i <= k) {
+                    const float u0 = __ldg(A.uni + (size_t)(r0 + i) * 2), u1 = __ldg(A.uni + (size_t)(r0 + i) * 2 + 1);
+                    if (!(u0 >= 0.f && u0 < 1.f) || !(u1 >= 0.f && u1 < 1.f)) baduni = true;
+                }
+                const unsigned msk = __ballot_sync(0xffffffffu, rej);
+                if (msk && a == k) a = i0 + __ffs(msk) - 1;
             }
-            tok = load_stat(A.stats + r0 + a).argmax;
-        } else {
-            a = k;
-            for (int i = 0; i < k; i++) {
-                float p = __ldcg(A.pq + (size_t)(d0 + i) * 2), q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
-                float u = __ldg(A.uni + (size_t)(r0 + i) * 2);
-                bool accept;
-                if (p > 0.f && q == 0.f) {
-                    accept = true;
-                } else if (p > 0.f) {
-                    float ratio = __fdiv_rn(p, q);
-                    float thr = ratio < 1.f ? ratio : 1.f;
-                    accept = u < thr;
-                } else {
-                    accept = false;
-                }
-                if (!accept) {
-                    a = i;
-                    break;
-                }
+            badtok = __any_sync(0xffffffffu, badtok);
+            baduni = __any_sync(0xffffffffu, baduni);
+            if (badtok) status = 2;
+            else if (baduni) status = 5;
+            if (status == 0) {
+                if (greedy) tok = __ldcg(&A.stats[r0 + a].argmax);
+                else if (a == k) tok = __ldcg(&A.stats[r0 + k].bonus);
+                else need = 1;
+            } else {
+                a = -1;
             }
-            if (a == k) tok = load_stat(A.stats + r0 + k).bonus;
-            else need = 1;
         }
-        S.a = a;
-        S.tok = tok;
-        S.need_resid = need;
+        if (lane == 0) {
+            if (status) record_error(A, status, b);
+            S.a = a;
+            S.tok = tok;
+            S.need_resid = need;
+        }
     }
     __syncthreads();
     if (S.need_resid) {
@@ -385,38 +538,47 @@ __device__ void finalize(const Args &A, Ctx &S, const Dyn &D) {
         const RowStat st = load_stat(A.stats + r0 + a);
         const float *qrow = A.q + (size_t)(d0 + a) * V;
         const float u = __ldg(A.uni + (size_t)(r0 + a) * 2 + 1);
-        int tok = -1;
         if (st.kind == KIND_LIST) {
-            const int n = st.nlist;
-            const int32_t *L = A.lists + (size_t)(r0 + a) * LCAP * 2;
-            for (int j = tid; j < n; j += NT) {
-                int x = __ldcg(L + 2 * j);
-                float p = __fmul_rn(__int_as_float(__ldcg(L + 2 * j + 1)), st.invZ);
-                float q = __ldg(qrow + x);
-                D.aux[j] = fmaxf(__fsub_rn(p, q), 0.f);
-                reinterpret_cast<int *>(D.cand)[j] = x;
+            // p is zero outside the stored kept list, so r is too: gather q on the list only
+            if (warp == 0) {
+                const int n = st.nlist;
+                const int2 *L = reinterpret_cast<const int2 *>(A.lists + (size_t)(r0 + a) * LCAP * 2);
+                int tk[8];
+                float pw[8], rw[8];
+#pragma unroll
+                for (int t = 0; t < 8; t++) {
+                    const int idx = lane * 8 + t;
+                    int2 e = idx < n ? __ldcg(L + idx) : make_int2(-1, 0);
+                    tk[t] = e.x;
+                    pw[t] = idx < n ? __fmul_rn(__int_as_float(e.y), st.invZ) : 0.f;
+                }
+#pragma unroll
+                for (int t = 0; t < 8; t++) {
+                    const float q = tk[t] >= 0 ? __ldg(qrow + tk[t]) : 0.f;
+                    rw[t] = tk[t] >= 0 ? fmaxf(__fsub_rn(pw[t], q), 0.f) : 0.f;
+                }
+                int j = warp_draw8(rw, n, u);
+                if (j < 0) j = warp_draw8(pw, n, u);      // empty residual: draw from p
+                int sel = -1;
+#pragma unroll
+                for (int t = 0; t < 8; t++)
+                    if (lane * 8 + t == j) sel = tk[t];
+                sel = __shfl_sync(0xffffffffu, sel, j >= 0 ? (j >> 3) : 0);
+                if (lane == 0) S.tok = j >= 0 ? sel : -1;
             }
             __syncthreads();
-            int j = draw_small(D.aux, D.aux2, n, u, S);
-            if (j < 0) {   // empty residual: draw from p
-                for (int jj = tid; jj < n; jj += NT)
-                    D.aux[jj] = __fmul_rn(__int_as_float(__ldcg(L + 2 * jj + 1)), st.invZ);
-                __syncthreads();
-                j = draw_small(D.aux, D.aux2, n, u, S);
-            }
-            tok = j >= 0 ? reinterpret_cast<int *>(D.cand)[j] : -1;
         } else {
-            if (warp_id() == 0) build_penalties(A, S, a);
+            if (warp == 0) build_penalties(A, S, a);
             __syncthreads();
             const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)(r0 + a) * V;
             WResid wr{st.m, st.s, st.invZ, st.taukey};
             WProb wp{st.m, st.s, st.invZ, st.taukey};
             seg_sums<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, wr, D.segC, wp);
-            tok = draw_by_segments<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, u, wr);
+            int tok = draw_by_segments<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, u, wr);
             if (tok < 0) tok = draw_by_segments<E, VEC, QVEC>(S, row, nullptr, V, A.nseg, D.segC, u, wp);
+            if (tid == 0) S.tok = tok;
+            __syncthreads();
         }
-        if (tid == 0) S.tok = tok;
-        __syncthreads();
     }
     // outputs: accepted drafts, the final token, -1 padding
     const int a = S.a, kw = A.k_max + 1;
@@ -442,7 +604,7 @@ __device__ __forceinline__ void fail_request(const Args &A, int b) {
 }
 
 template <typename E, bool VEC, bool QVEC>
-__global__ void __launch_bounds__(NT, 2) verify_kernel(const Args A) {
+__global__ void __launch_bounds__(NT, 4) verify_kernel(const Args A) {
     extern __shared__ __align__(16) unsigned char dsm[];
     __shared__ Ctx S;
     const int tid = threadIdx.x;

@@ -158,6 +158,49 @@ __device__ __forceinline__ void block_sort_desc(unsigned long long *keys, int np
     }
 }
 
+// Exclusive prefix of v across the 32 lanes (lane 0 gets 0) and the warp total.
+__device__ __forceinline__ float warp_excl_scan(float v, float &total) {
+    const int lane = lane_id();
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    total = __shfl_sync(0xffffffffu, incl, 31);
+    float ex = __shfl_up_sync(0xffffffffu, incl, 1);
+    return lane == 0 ? 0.f : ex;
+}
+
+// Inverse-CDF draw by one warp over w[0..n) held 8 per lane (element lane*8 + j in w8[j]):
+// the first element whose running sum exceeds u * W, else the last positive one; -1 when
+// no weight is positive.  Running sums associate lane-locally then across lanes (fixed).
+__device__ __forceinline__ int warp_draw8(const float w8[8], int n, float u) {
+    const int lane = lane_id();
+    float pre[8], loc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        loc += w8[j];
+        pre[j] = loc;
+    }
+    float W;
+    float ex = warp_excl_scan(loc, W);
+    if (!(W > 0.f)) return -1;
+    const float target = __fmul_rn(u, W);
+    int pick = 0x7fffffff, last = -1;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        int idx = lane * 8 + j;
+        if (idx < n) {
+            if (ex + pre[j] > target && pick == 0x7fffffff) pick = idx;
+            if (w8[j] > 0.f) last = idx;
+        }
+    }
+    pick = warp_min_i(pick);
+    last = warp_max_i(last);
+    return pick != 0x7fffffff ? pick : last;
+}
+
 __device__ __forceinline__ int pow2_at_least(int n) {
     int p = 1;
     while (p < n) p <<= 1;

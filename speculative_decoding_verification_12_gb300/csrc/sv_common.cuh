@@ -7,11 +7,12 @@
 
 namespace sv {
 
-constexpr int NT = 512;               // threads per row CTA
+constexpr int NT = 256;               // threads per row CTA
 constexpr int NWARP = NT / 32;
 constexpr int SEG = 256;              // elements per segment: one warp step of 32 lanes x 8
 constexpr int CAP = 2048;             // candidate buffer (top-k candidates, kept lists) per CTA
 constexpr int KCAP = 512;             // top-k up to this goes through the candidate buffer
+constexpr int WCAP = 256;             // candidate sets up to this are cut and drawn by one warp
 constexpr int LCAP = 256;             // kept-list entries stored per row for the residual draw
 constexpr int HB = 2048;              // radix histogram bins (11-bit digits)
 constexpr int MAXK = 64;              // largest k_max

@@ -26,7 +26,10 @@ struct Ctx {
     int draft_raw[MAXK];
     float redf[NWARP];
     int redi[NWARP];
-    int ncand;
+    int ncand, nsel, n2;
+    float zx, qx, zk;
+    int xtok;
+    uint32_t cutkey;
     int sel_digit;
     long long sel_below;
     unsigned long long sel_mass;
@@ -69,17 +72,19 @@ __device__ __forceinline__ void load_request(const Args &A, Ctx &S, int b) {
     S.pres = A.pres ? __ldg(A.pres + b) : 0.f;
     S.freq = A.freq ? __ldg(A.freq + b) : 0.f;
     if (!isfinite(S.pres) || !isfinite(S.freq)) status = status ? status : 6;
+    // every field is loaded up front (one round trip); greedy requests ignore T, P and K
+    const float T = __ldg(A.T + b);
+    const float P = __ldg(A.topp + b);
+    const int K = __ldg(A.topk + b);
     S.T = 1.f;
     S.P = 1.f;
     S.K = 0;
     if (!S.greedy) {
-        float T = __ldg(A.T + b);
-        float P = __ldg(A.topp + b);
         if (!(T > 0.f) || !isfinite(T)) status = status ? status : 3;
         if (!(P > 0.f && P <= 1.f)) status = status ? status : 4;
         S.T = T;
         S.P = P;
-        S.K = __ldg(A.topk + b);
+        S.K = K;
     }
     S.status = status;
 }
@@ -166,6 +171,20 @@ __device__ __forceinline__ float elem_z<uint16_t>(const Ctx &S, const uint16_t *
 template <>
 __device__ __forceinline__ float elem_z<float>(const Ctx &S, const float *row, int x) {
     float z = __ldg(row + x);
+    for (int h = 0; h < S.npen; h++)
+        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
+    return z;
+}
+
+// Penalised value of token x from its raw stored element.
+__device__ __forceinline__ float elem_z_raw(const Ctx &S, uint16_t raw, int x) {
+    float z = __uint_as_float((uint32_t)raw << 16);
+    for (int h = 0; h < S.npen; h++)
+        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
+    return z;
+}
+__device__ __forceinline__ float elem_z_raw(const Ctx &S, float raw, int x) {
+    float z = raw;
     for (int h = 0; h < S.npen; h++)
         if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
     return z;
@@ -262,6 +281,69 @@ __device__ __forceinline__ void find_count_bin(Ctx &S, const uint32_t *cnt, int 
         S.sel_digit = dsel;
         S.sel_below = c;
     }
+}
+
+// Warp 0 finds, in a 256-bin count histogram scanned from the top, the bin holding the
+// need-th largest element; 8 bins per lane.  Writes S.sel_digit and S.sel_below.
+__device__ __forceinline__ void find_count_bin256(Ctx &S, const uint32_t *cnt, long long need) {
+    if (warp_id() != 0) return;
+    const int lane = lane_id();
+    const int top = 256 - lane * 8;
+    uint32_t c8[8];
+    long long tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        c8[j] = cnt[top - 1 - j];
+        tot += c8[j];
+    }
+    long long incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    long long excl = incl - tot;
+    unsigned msk = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+    int owner = msk ? __ffs(msk) - 1 : 31;
+    if (lane == owner) {
+        long long c = excl;
+        int dsel = top - 8;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            if (c + (long long)c8[j] >= need) {
+                dsel = top - 1 - j;
+                break;
+            }
+            c += c8[j];
+        }
+        S.sel_digit = dsel;
+        S.sel_below = c;
+    }
+}
+
+// A lower bound on the need-th largest of n float keys in shared memory: the top 16 bits of
+// that key (two 8-bit radix rounds) with the low 16 bits cleared.  At least `need` keys are
+// >= the bound, and every key above it shares the bound's 16-bit prefix or exceeds it.
+__device__ uint32_t select_bound16(Ctx &S, const float *vals, int n, int need, uint32_t *cnt) {
+    uint32_t prefix = 0;
+    long long nd = need;
+    for (int round = 0; round < 2; round++) {
+        const int shift = 24 - 8 * round;
+        const uint32_t mask = round == 0 ? 0u : 0xFF000000u;
+        for (int d = threadIdx.x; d < 256; d += NT) cnt[d] = 0;
+        __syncthreads();
+        for (int j = threadIdx.x; j < n; j += NT) {
+            uint32_t key = fkey(vals[j]);
+            if ((key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        find_count_bin256(S, cnt, nd);
+        __syncthreads();
+        prefix |= (uint32_t)S.sel_digit << shift;
+        nd -= S.sel_below;
+        __syncthreads();
+    }
+    return prefix;
 }
 
 // The need-th largest (1-based) of n float keys fkey(vals[j]) held in shared memory.

@@ -42,8 +42,8 @@ MUTATIONS = [
      [lambda o: pins.test_softmax_against_numpy(o)]),
     ("top-k off by one", "tau = zs[K - 1];", "tau = zs[K];",
      [lambda o: pins.test_filters_brute_force(o, 0), lambda o: pins.test_filters_edge_cases(o)]),
-    ("top-p counts the level's own mass", "if (above / ZK < P) {",
-     "if ((above + (double)c * exp(level - m)) / ZK < P) {",
+    ("top-p counts the level's own mass", "if (!cut && above / ZK < P) {",
+     "if (!cut && (above + lm) / ZK < P) {",
      [lambda o: pins.test_filters_brute_force(o, s) for s in range(8)]),
     ("top-p normalised over the unfiltered row", "ZK += (p[v] >= tau) ? exp(p[v] - m) : 0.0;",
      "ZK += exp(p[v] - m);", [lambda o: pins.test_filters_edge_cases(o)]),
