@@ -62,7 +62,8 @@ enum {
     SV_DEV_BAD_TEMPERATURE = 3,
     SV_DEV_BAD_TOP_P = 4,
     SV_DEV_BAD_UNIFORM = 5,
-    SV_DEV_BAD_PENALTY = 6
+    SV_DEV_BAD_PENALTY = 6,
+    SV_DEV_TIMEOUT = 7        /* a row's bulk copy did not complete within 2 s (bounded wait)  */
 };
 
 /* Per-request sampling parameters: structure of device arrays, each of length B. */

@@ -37,11 +37,12 @@ struct Dyn {
     unsigned long long *cand;    // CAP keys: (order key << 32) | ~token, later (~token << 32) | key
     float *aux, *aux2;           // CAP floats each
     unsigned long long *sorted;  // WCAP keys (aliases aux/aux2)
+    unsigned char *ring;         // NS x SB bytes of streamed row data (aliases cand/aux/aux2)
     uint32_t *hcnt;              // radix histogram (aliases cand/aux)
     unsigned long long *hmass;   // fixed-point mass histogram (aliases)
 };
 
-__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 3) & ~3; }
+__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }   // keeps the ring 128-byte aligned
 __host__ __device__ inline size_t dyn_bytes(int nseg) {
     return size_t(3) * nseg_pad(nseg) * 4 + size_t(CAP) * 8 + size_t(CAP) * 4 * 2;
 }
@@ -57,10 +58,22 @@ __device__ __forceinline__ Dyn carve(unsigned char *base, int nseg) {
     d.aux = reinterpret_cast<float *>(area + size_t(CAP) * 8);
     d.aux2 = d.aux + CAP;
     d.sorted = reinterpret_cast<unsigned long long *>(d.aux);
+    d.ring = area;
     d.hmass = reinterpret_cast<unsigned long long *>(area);                     // HB * 8 bytes
     d.hcnt = reinterpret_cast<uint32_t *>(area + size_t(HB) * 8);               // HB * 4 bytes
     return d;
 }
+
+#ifdef SV_TIMING
+#define SV_MARK(A, r, j)                                                  \
+    do {                                                                  \
+        if (threadIdx.x == 0) (A).timing[(size_t)(r) * NTIME + (j)] = global_ns(); \
+    } while (0)
+#else
+#define SV_MARK(A, r, j) \
+    do {                 \
+    } while (0)
+#endif
 
 __device__ __forceinline__ void record_error(const Args &A, int code, int b) {
     atomicCAS(A.hdr, 0, code);
@@ -168,7 +181,9 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
     const float m = S.m, s = S.s;
     // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
     uint32_t tkey = 0;
+    SV_MARK(A, row_idx, 8);
     if (nseg >= K) tkey = select_bound16(S, D.segA, nseg, K, D.hcnt);
+    SV_MARK(A, row_idx, 9);
     // the segments holding a token at or above the bound, re-read (from L2) four at a time
     int *segl = reinterpret_cast<int *>(D.segC);
     if (tid == 0) {
@@ -180,6 +195,7 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
         if (fkey(D.segA[j]) >= tkey) segl[atomicAdd(&S.nsel, 1)] = j;
     __syncthreads();
     const int nsel = S.nsel;
+    SV_MARK(A, row_idx, 10);
     constexpr int U = 4;
     for (int j0 = warp; j0 < nsel; j0 += NWARP * U) {
         Raw8<E> raw[U];
@@ -202,6 +218,7 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
     }
     __syncthreads();
     const int n = S.ncand;
+    SV_MARK(A, row_idx, 11);
     if (n > CAP || n < 1) return false;
 
     if (n <= WCAP) {
@@ -214,8 +231,10 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
             srt[r] = c;
         }
         __syncthreads();
+        SV_MARK(A, row_idx, 12);
         if (warp == 0) warp_cut(S, srt, n, K, m, s, S.topp_on, S.P);
         __syncthreads();
+        SV_MARK(A, row_idx, 13);
         const int n2 = S.n2;
         const float Z = S.zk;
         st.Z = Z;
@@ -237,6 +256,7 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
         __syncthreads();
         int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
         for (int j = tid; j < n2; j += NT) L[j] = make_int2(ltok[j], __float_as_int(lw[j]));
+        SV_MARK(A, row_idx, 14);
         if (want_bonus) {
             if (warp == 0) {
                 const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
@@ -249,6 +269,7 @@ __device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const 
             __syncthreads();
             st.bonus = S.tok;
         }
+        SV_MARK(A, row_idx, 15);
         return true;
     }
 
@@ -371,13 +392,25 @@ __device__ void row_phase(const Args &A, Ctx &S, const Dyn &D, const int row_idx
     }
     __syncthreads();
     const bool need_sum = sampled && !S.topk_on && !S.topp_on;
-    pass_stats<E, VEC>(S, row, V, nseg, D.segA, D.segB, need_sum, s);
+    bool streamed = true;
+    if (VEC) streamed = pass_stats_ring<E>(S, D.ring, row, V, nseg, D.segA, D.segB, need_sum, s);
+    else pass_stats<E, VEC>(S, row, V, nseg, D.segA, D.segB, need_sum, s);
     if (tid == NT - 1) {
         S.xtok = xtok;
         S.zx = elem_z_raw(S, zraw, xtok);
         S.qx = qx;
     }
     __syncthreads();
+    SV_MARK(A, row_idx, 2);
+    if (!streamed) {
+        // a bounded wait expired: fail the row (its request's outputs become -1)
+        if (tid == 0) {
+            record_error(A, SV_DEV_TIMEOUT, S.b);
+            st.kind = KIND_FAIL;
+            A.stats[row_idx] = st;
+        }
+        return;
+    }
     float mx = -INFINITY;
     for (int j = tid; j < nseg; j += NT) mx = fmaxf(mx, D.segA[j]);
     const float m = block_max(mx, S.redf);
@@ -432,6 +465,7 @@ __device__ void row_phase(const Args &A, Ctx &S, const Dyn &D, const int row_idx
         if (!done) kept_by_select<E, VEC>(A, S, D, row, st, row_idx, want_bonus);
     }
 
+    SV_MARK(A, row_idx, 3);
     // the draft of this row: p(x_i) and q(x_i)
     if (tid == 0 && i < S.k) {
         const int x = S.xtok;
@@ -488,11 +522,12 @@ __device__ void finalize(const Args &A, Ctx &S, const Dyn &D) {
         int a = -1, tok = -1, need = 0;
         if (status == 0) {
             const bool greedy = S.greedy;
-            bool badtok = false, baduni = false;
+            bool badtok = false, baduni = false, badrow = false;
             a = k;
             for (int i0 = 0; i0 <= k; i0 += 32) {
                 const int i = i0 + lane;
                 bool rej = false;
+                if (i <= k && __ldcg(&A.stats[r0 + i].kind) == KIND_FAIL) badrow = true;
                 if (i < k) {
                     const int x = __ldg(A.tokens + d0 + i);
                     if (x < 0 || x >= V) badtok = true;
@@ -513,8 +548,10 @@ __device__ void finalize(const Args &A, Ctx &S, const Dyn &D) {
             }
             badtok = __any_sync(0xffffffffu, badtok);
             baduni = __any_sync(0xffffffffu, baduni);
-            if (badtok) status = 2;
-            else if (baduni) status = 5;
+            badrow = __any_sync(0xffffffffu, badrow);
+            if (badtok) status = SV_DEV_BAD_TOKEN;
+            else if (baduni) status = SV_DEV_BAD_UNIFORM;
+            else if (badrow) status = SV_DEV_TIMEOUT;
             if (status == 0) {
                 if (greedy) tok = __ldcg(&A.stats[r0 + a].argmax);
                 else if (a == k) tok = __ldcg(&A.stats[r0 + k].bonus);
@@ -605,11 +642,22 @@ __device__ __forceinline__ void fail_request(const Args &A, int b) {
 
 template <typename E, bool VEC, bool QVEC>
 __global__ void __launch_bounds__(NT, 4) verify_kernel(const Args A) {
-    extern __shared__ __align__(16) unsigned char dsm[];
+    extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ Ctx S;
     const int tid = threadIdx.x;
     const int r = blockIdx.x;
     const Dyn D = carve(dsm, A.nseg);
+    SV_MARK(A, r, 0);
+#ifdef SV_TIMING
+    if (tid == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        A.timing[(size_t)r * NTIME + 6] = smid;
+        A.timing[(size_t)r * NTIME + 7] = 0;
+    }
+#endif
+    // start streaming this CTA's row right away; the request lookup overlaps the first copies
+    if (VEC && tid == 0) ring_start(S, D.ring, reinterpret_cast<const E *>(A.logits) + (size_t)r * A.V, A.V, (int)sizeof(E));
 
     // locate the row: request b, row i within it
     if (tid < 32) {
@@ -643,6 +691,11 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const Args A) {
         }
     }
     __syncthreads();
+    SV_MARK(A, r, 1);
+    if (VEC && !S.active) {   // nothing to compute: let the speculative copies land first
+        if (tid == 0) ring_drain(S);
+        __syncthreads();
+    }
     if (S.b < 0) return;   // row outside every request: nothing to count
 
     // requests with no rows (row_offsets[j] == row_offsets[j+1]) are failed by the first row
@@ -659,6 +712,7 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const Args A) {
         __syncthreads();
         row_phase<E, VEC>(A, S, D, r);
     }
+    SV_MARK(A, r, 4);
 
     // arrival: the CTA that brings the count to the request's row count finalises it
     __syncthreads();
@@ -671,7 +725,11 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const Args A) {
     if (S.last) {
         __threadfence();
         finalize<E, VEC, QVEC>(A, S, D);
+#ifdef SV_TIMING
+        if (tid == 0) A.timing[(size_t)r * NTIME + 7] = 1;
+#endif
     }
+    SV_MARK(A, r, 5);
 }
 
 __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *nd, int B, int32_t *hdr) {
@@ -765,6 +823,7 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
     A.stats = reinterpret_cast<RowStat *>(ws + L.stats);
     A.pq = reinterpret_cast<float *>(ws + L.pq);
     A.lists = reinterpret_cast<int32_t *>(ws + L.lists);
+    A.timing = reinterpret_cast<unsigned long long *>(ws + L.timing);
     A.B = B;
     A.k_max = k_max;
     A.V = V;

@@ -15,6 +15,9 @@ constexpr int KCAP = 512;             // top-k up to this goes through the candi
 constexpr int WCAP = 256;             // candidate sets up to this are cut and drawn by one warp
 constexpr int LCAP = 256;             // kept-list entries stored per row for the residual draw
 constexpr int HB = 2048;              // radix histogram bins (11-bit digits)
+constexpr int NS = 4;                 // stages of the shared-memory row ring (bulk copies in flight)
+constexpr int SB = 8192;              // bytes per ring stage
+constexpr unsigned long long WAIT_NS = 2000000000ull;   // give up on an mbarrier after 2 s
 constexpr int MAXK = 64;              // largest k_max
 constexpr int MAXV = 1 << 21;         // largest vocabulary
 constexpr float LOG2E = 1.4426950408889634f;
@@ -26,7 +29,8 @@ enum : int32_t {
     KIND_GREEDY = 1,   // greedy request: argmax only
     KIND_FULL = 2,     // sampled, no filter: every token kept
     KIND_LIST = 3,     // sampled, kept set small: stored as a list (token, weight) in token order
-    KIND_THRESH = 4    // sampled, kept set = {z >= tau}, too large for a list
+    KIND_THRESH = 4,   // sampled, kept set = {z >= tau}, too large for a list
+    KIND_FAIL = 5      // the row's stream did not complete (bounded wait expired)
 };
 
 // Per-row statistics written by the row CTA and read by the request's finalising CTA.
@@ -46,8 +50,14 @@ struct __align__(16) RowStat {
 };
 
 struct WsLayout {
-    size_t counters, stats, pq, lists, total;
+    size_t counters, stats, pq, lists, timing, total;
 };
+
+// Phase timestamps (globaltimer ns) per row CTA, recorded only in builds with SV_TIMING:
+// [0] start, [1] request located, [2] row streamed, [3] kept set done, [4] row written,
+// [5] finalised, [6] SM id, [7] 1 if this CTA finalised its request, [8..15] steps of the
+// candidate path (bound, segment list, re-read, sort, cut, list, draw).
+constexpr int NTIME = 16;
 
 __host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -64,6 +74,10 @@ __host__ __device__ inline WsLayout ws_layout(int B, int R) {
     o = up256(o + size_t(R > B ? R - B : 0) * 8);
     L.lists = o;
     o = up256(o + size_t(R) * LCAP * 8);
+    L.timing = o;
+#ifdef SV_TIMING
+    o = up256(o + size_t(R) * NTIME * 8);
+#endif
     L.total = o;
     return L;
 }
@@ -89,6 +103,7 @@ struct Args {
     RowStat *stats;
     float *pq;
     int32_t *lists;
+    unsigned long long *timing;   // SV_TIMING builds only
     int B, k_max, V, R, nseg;
     int q_vec;                // draft-prob rows are 16-byte aligned
 };

@@ -17,6 +17,9 @@ namespace sv {
 
 // Static shared state of one row CTA.
 struct Ctx {
+    unsigned long long full[NS];    // ring stage holds its chunk (transaction-count barrier)
+    unsigned long long empty[NS];   // every warp is done with the stage
+    int issued, ring_fail;
     int b, i, k, r0, d0, nrows, status, active, greedy;
     int K, topk_on, topp_on;
     float T, P, pres, freq, s, m;
@@ -236,6 +239,120 @@ __device__ __forceinline__ void pass_stats(const Ctx &S, const E *row, int V, in
             }
         }
     }
+}
+
+// ------------------------------------------------------------------------------------------
+// pass 1 through a shared-memory ring fed by bulk copies (16-byte aligned rows)
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ int ring_chunks(int V, int esize) {
+    const uint32_t RB = (uint32_t)V * esize;
+    return (int)((RB + SB - 1) / SB);
+}
+
+// Thread 0: copy chunk c (SB bytes, the last one shorter) of the row into its ring stage.
+__device__ __forceinline__ void ring_issue(Ctx &S, unsigned char *ring, const void *row, uint32_t RB, int c) {
+    const int st = c % NS;
+    const uint32_t off = (uint32_t)c * SB;
+    const uint32_t bytes = min((uint32_t)SB, RB - off);
+    mbar_expect_tx(&S.full[st], bytes);
+    bulk_g2s(ring + st * SB, reinterpret_cast<const unsigned char *>(row) + off, bytes, &S.full[st]);
+    S.issued = c + 1;
+}
+
+// Thread 0: set up the ring barriers and start the first NS chunks of the row.
+__device__ __forceinline__ void ring_start(Ctx &S, unsigned char *ring, const void *row, int V, int esize) {
+    for (int s = 0; s < NS; s++) {
+        mbar_init(&S.full[s], 1);
+        mbar_init(&S.empty[s], NWARP);
+    }
+    mbar_fence_init();
+    S.issued = 0;
+    S.ring_fail = 0;
+    const uint32_t RB = (uint32_t)V * esize;
+    const int nc = ring_chunks(V, esize);
+    for (int c = 0; c < NS && c < nc; c++) ring_issue(S, ring, row, RB, c);
+}
+
+// Thread 0: wait (bounded) for the latest chunk of every stage, so that no copy into shared
+// memory is still in flight when the CTA moves on or exits.
+__device__ __forceinline__ void ring_drain(Ctx &S) {
+    for (int c = max(0, S.issued - NS); c < S.issued; c++) mbar_wait(&S.full[c % NS], (uint32_t)(c / NS) & 1u);
+}
+
+template <typename E>
+__device__ __forceinline__ void ring_values(const unsigned char *buf, int j, float v[8]);
+template <>
+__device__ __forceinline__ void ring_values<uint16_t>(const unsigned char *buf, int j, float v[8]) {
+    Raw8<uint16_t> r;
+    r.a = *reinterpret_cast<const uint4 *>(buf + j * SEG * 2 + lane_id() * 16);
+    unpack8(r, v);
+}
+template <>
+__device__ __forceinline__ void ring_values<float>(const unsigned char *buf, int j, float v[8]) {
+    Raw8<float> r;
+    const uint4 *p = reinterpret_cast<const uint4 *>(buf + j * SEG * 4 + lane_id() * 32);
+    r.a = p[0];
+    r.b = p[1];
+    unpack8(r, v);
+}
+
+// Pass 1 over the ring: per-segment max (and weight sums), same results as pass_stats.
+// Thread 0 refills a stage once all warps released it.  Returns false if a bounded wait
+// expired (the caller fails the row).
+template <typename E>
+__device__ bool pass_stats_ring(Ctx &S, unsigned char *ring, const E *row, int V, int nseg, float *segmax,
+                                float *segsum, bool need_sum, float s) {
+    const int warp = warp_id(), lane = lane_id();
+    const uint32_t RB = (uint32_t)V * sizeof(E);
+    const int nc = ring_chunks(V, (int)sizeof(E));
+    constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
+    int c = 0;
+    for (; c < nc; c++) {
+        const int st = c % NS;
+        const uint32_t par = (uint32_t)(c / NS) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&S.full[st], par))) break;
+        const unsigned char *buf = ring + st * SB;
+        for (int j = warp; j < SPC; j += NWARP) {
+            const int seg = c * SPC + j;
+            if (seg >= nseg) break;
+            float v[8];
+            ring_values<E>(buf, j, v);
+            const int base = seg * SEG + lane * 8;
+            if (base + 8 > V) {
+#pragma unroll
+                for (int t = 0; t < 8; t++)
+                    if (base + t >= V) v[t] = -INFINITY;
+            }
+            patch_seg(S, seg * SEG, v);
+            const float mx = warp_max(max8(v));
+            float sum = 0.f;
+            if (need_sum && mx > -INFINITY) {
+                const float ms = __fmul_rn(mx, s);
+#pragma unroll
+                for (int t = 0; t < 8; t++) sum += ex2(fmaf(v[t], s, -ms));
+                sum = warp_sum(sum);
+            }
+            if (lane == 0) {
+                segmax[seg] = mx;
+                segsum[seg] = sum;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[st]);
+        if (threadIdx.x == 0 && c + NS < nc) {
+            if (mbar_wait(&S.empty[st], par)) ring_issue(S, ring, row, RB, c + NS);
+            else S.ring_fail = 1;
+        }
+    }
+    if (c < nc) atomicOr(&S.ring_fail, 1);
+    __syncthreads();
+    if (S.ring_fail) {
+        if (threadIdx.x == 0) ring_drain(S);
+        __syncthreads();
+        return false;
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------------------------------
