@@ -1,21 +1,21 @@
 // spec_verify.cu -- batched speculative-decoding verification for GB300 (sm_103a): the
-// C-ABI entry points and the fused verify kernel.
+// C-ABI entry points and the two verify kernels.
 //
-// One CTA per target row streams the row once from HBM (128-bit loads, 8 tokens per lane,
-// 256-token segments per warp step) and reduces it to per-segment maxima and weight sums.
-// From those it builds the row's kept set:
-//   - no filter: p = e / Z with Z from the segment sums (no second pass);
-//   - top-k (k <= KCAP): the k-th largest segment maximum bounds the k-th largest token from
-//     below, so only the segments whose maximum reaches it are re-read (from L2) to collect
-//     candidates; the exact top-k and top-p cut is made on the sorted candidates in shared
-//     memory;
-//   - otherwise (top-p alone, large top-k, candidate overflow): radix select with 11-bit
-//     digits over the row, counts for top-k and fixed-point masses for top-p.
-// It then gathers p(x_i) and q(x_i) for the row's draft, and on a request's last row also
-// draws the extra token.  The CTA that completes the last row of a request (arrival counter
-// per request; no CTA ever waits on another) runs the first-rejection scan and, at a
-// rejection, draws from max(0, p - q) of the rejected row: over the stored kept list when it
-// is small, else in one pass over the row and its draft row.
+// Persistent kernel (16-byte aligned rows; the fast path).  A grid of two CTAs per SM claims
+// target rows from a counter in the workspace.  Inside a CTA the warps specialise:
+//   warp 0     issues cp.async.bulk copies of row after row into a 6 x 8 KB shared-memory
+//              ring (completion on mbarriers with transaction counts);
+//   warp 1     claims the next rows and prepares them: request lookup, sampling
+//              parameters, penalties of the earlier drafts, and the row's draft gathers
+//              (x_i, z(x_i), q(x_i)), up to NRB rows ahead;
+//   warps 2-9  reduce each streamed 256-token segment to its max (and weight sum);
+//   warps 10-13 turn a finished row's segment statistics into its kept set, draws and
+//              draft probabilities while the next row streams, and finalise a request when
+//              its last row is done.
+// Every mbarrier wait is bounded in time; on expiry the row fails with SV_DEV_TIMEOUT.
+//
+// Row kernel (any alignment).  One CTA per row streams it with plain 128-bit or scalar loads
+// and then runs the same selection and finalisation code.
 //
 // Method: "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust"
 // ("The Memory Bandwidth Wall and Speculative Math", "The Verification Algorithm",
@@ -27,709 +27,296 @@
 #include <stdint.h>
 
 #include "../../include/spec_verify.h"
-#include "sv_row.cuh"
+#include "sv_select.cuh"
+#include "sv_stream.cuh"
 
 namespace sv {
 
-// Shared-memory carve-up of one CTA (dynamic part).
-struct Dyn {
-    float *segA, *segB, *segC;   // per-segment max / weight sums
-    unsigned long long *cand;    // CAP keys: (order key << 32) | ~token, later (~token << 32) | key
-    float *aux, *aux2;           // CAP floats each
-    unsigned long long *sorted;  // WCAP keys (aliases aux/aux2)
-    unsigned char *ring;         // NS x SB bytes of streamed row data (aliases cand/aux/aux2)
-    uint32_t *hcnt;              // radix histogram (aliases cand/aux)
-    unsigned long long *hmass;   // fixed-point mass histogram (aliases)
-};
+// ------------------------------------------------------------------------------------------
+// row kernel: one CTA per row, any alignment
+// ------------------------------------------------------------------------------------------
 
-__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }   // keeps the ring 128-byte aligned
-__host__ __device__ inline size_t dyn_bytes(int nseg) {
-    return size_t(3) * nseg_pad(nseg) * 4 + size_t(CAP) * 8 + size_t(CAP) * 4 * 2;
+// Bytes of one row's segment statistics: max, second/sum and lane arrays plus the histogram.
+__host__ __device__ inline size_t segstats_bytes(int np) { return size_t(3) * np * 4 + 256 * 4; }
+
+__device__ __forceinline__ SegStats carve_segstats(unsigned char *p, int np) {
+    SegStats o;
+    o.mx = reinterpret_cast<float *>(p);
+    o.b = o.mx + np;
+    o.lane = reinterpret_cast<int *>(o.b + np);
+    o.hist = reinterpret_cast<uint32_t *>(o.lane + np);
+    return o;
 }
 
-__device__ __forceinline__ Dyn carve(unsigned char *base, int nseg) {
-    Dyn d;
+__host__ __device__ inline size_t rows_smem(int nseg) {
     const int np = nseg_pad(nseg);
-    d.segA = reinterpret_cast<float *>(base);
-    d.segB = d.segA + np;
-    d.segC = d.segB + np;
-    unsigned char *area = reinterpret_cast<unsigned char *>(d.segC + np);
-    d.cand = reinterpret_cast<unsigned long long *>(area);
-    d.aux = reinterpret_cast<float *>(area + size_t(CAP) * 8);
-    d.aux2 = d.aux + CAP;
-    d.sorted = reinterpret_cast<unsigned long long *>(d.aux);
-    d.ring = area;
-    d.hmass = reinterpret_cast<unsigned long long *>(area);                     // HB * 8 bytes
-    d.hcnt = reinterpret_cast<uint32_t *>(area + size_t(HB) * 8);               // HB * 4 bytes
-    return d;
-}
-
-#ifdef SV_TIMING
-#define SV_MARK(A, r, j)                                                  \
-    do {                                                                  \
-        if (threadIdx.x == 0) (A).timing[(size_t)(r) * NTIME + (j)] = global_ns(); \
-    } while (0)
-#else
-#define SV_MARK(A, r, j) \
-    do {                 \
-    } while (0)
-#endif
-
-__device__ __forceinline__ void record_error(const Args &A, int code, int b) {
-    atomicCAS(A.hdr, 0, code);
-    atomicMax(A.hdr + 1, INT_MAX - b);
-}
-
-// ------------------------------------------------------------------------------------------
-// the row phase
-// ------------------------------------------------------------------------------------------
-
-// Appends this lane's tokens of segment seg whose key reaches tkey to the candidate buffer
-// (warp-aggregated; entries beyond CAP are counted but not stored).
-__device__ __forceinline__ void append_candidates(Ctx &S, const Dyn &D, int seg, const float v[8], uint32_t tkey,
-                                                  int V) {
-    const int lane = lane_id();
-    int c = 0;
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-        int idx = seg * SEG + lane * 8 + j;
-        c += (idx < V && fkey(v[j]) >= tkey) ? 1 : 0;
-    }
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int base = 0;
-    if (lane == 0 && total) base = atomicAdd(&S.ncand, total);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    int pos = base + incl - c;
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-        int idx = seg * SEG + lane * 8 + j;
-        uint32_t key = fkey(v[j]);
-        if (idx < V && key >= tkey) {
-            if (pos < CAP) D.cand[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)idx);
-            pos++;
-        }
-    }
-}
-
-// Warp 0: top-k cut, top-p cut and kept mass over n <= WCAP candidates sorted by value
-// (descending), 8 per lane.  Writes S.n2 (kept count), S.zk (kept mass), S.cutkey.
-__device__ __forceinline__ void warp_cut(Ctx &S, const unsigned long long *srt, int n, int K, float m, float s,
-                                         bool topp, float P) {
-    const int lane = lane_id(), base = lane * 8;
-    const int kk = min(K, n);
-    const uint32_t kkey = (uint32_t)(srt[kk - 1] >> 32);
-    uint32_t key[8];
-    int c1 = 0;
-#pragma unroll
-    for (int t = 0; t < 8; t++) {
-        const int idx = base + t;
-        key[t] = idx < n ? (uint32_t)(srt[idx] >> 32) : 0u;
-        c1 += (idx < n && key[t] >= kkey) ? 1 : 0;
-    }
-    const int n1 = warp_sum_i(c1);
-    float pre[8], loc = 0.f;
-#pragma unroll
-    for (int t = 0; t < 8; t++) {
-        loc += (base + t < n1) ? weight(key2f(key[t]), m, s) : 0.f;
-        pre[t] = loc;
-    }
-    float Z1;
-    const float ex = warp_excl_scan(loc, Z1);
-#pragma unroll
-    for (int t = 0; t < 8; t++) pre[t] += ex;
-    int n2 = n1;
-    if (topp) {
-        // a value level is cut when the mass strictly above it reaches P * Z1
-        const float PZ = __fmul_rn(P, Z1);
-        int cut = 0x7fffffff;
-        uint32_t prevkey = base > 0 ? (uint32_t)(srt[base - 1] >> 32) : 0u;
-        float prevpre = ex;
-#pragma unroll
-        for (int t = 0; t < 8; t++) {
-            const int idx = base + t;
-            if (idx > 0 && idx < n1 && key[t] != prevkey && prevpre >= PZ) cut = min(cut, idx);
-            prevkey = key[t];
-            prevpre = pre[t];
-        }
-        cut = warp_min_i(cut);
-        if (cut != 0x7fffffff) n2 = cut;
-    }
-    float zsel = 0.f;
-#pragma unroll
-    for (int t = 0; t < 8; t++)
-        if (base + t == n2 - 1) zsel = pre[t];
-    const float Z = __shfl_sync(0xffffffffu, zsel, (n2 - 1) >> 3);
-    if (lane == 0) {
-        S.n2 = n2;
-        S.zk = Z;
-        S.cutkey = (uint32_t)(srt[n2 - 1] >> 32);
-    }
-}
-
-// Kept set of a sampled row from the top-k candidates.  Returns false on candidate overflow.
-template <typename E, bool VEC>
-__device__ bool kept_from_candidates(const Args &A, Ctx &S, const Dyn &D, const E *row, RowStat &st, int row_idx,
-                                     bool want_bonus) {
-    const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
-    const int V = A.V, nseg = A.nseg, K = S.K;
-    const float m = S.m, s = S.s;
-    // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
-    uint32_t tkey = 0;
-    SV_MARK(A, row_idx, 8);
-    if (nseg >= K) tkey = select_bound16(S, D.segA, nseg, K, D.hcnt);
-    SV_MARK(A, row_idx, 9);
-    // the segments holding a token at or above the bound, re-read (from L2) four at a time
-    int *segl = reinterpret_cast<int *>(D.segC);
-    if (tid == 0) {
-        S.nsel = 0;
-        S.ncand = 0;
-    }
-    __syncthreads();
-    for (int j = tid; j < nseg; j += NT)
-        if (fkey(D.segA[j]) >= tkey) segl[atomicAdd(&S.nsel, 1)] = j;
-    __syncthreads();
-    const int nsel = S.nsel;
-    SV_MARK(A, row_idx, 10);
-    constexpr int U = 4;
-    for (int j0 = warp; j0 < nsel; j0 += NWARP * U) {
-        Raw8<E> raw[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int j = j0 + u * NWARP;
-            if (j < nsel) raw[u] = load_raw8<VEC>(row, segl[j] * SEG + lane * 8, V);
-        }
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int j = j0 + u * NWARP;
-            if (j < nsel) {
-                const int seg = segl[j];
-                float v[8];
-                unpack8(raw[u], v);
-                patch_seg(S, seg * SEG, v);
-                append_candidates(S, D, seg, v, tkey, V);
-            }
-        }
-    }
-    __syncthreads();
-    const int n = S.ncand;
-    SV_MARK(A, row_idx, 11);
-    if (n > CAP || n < 1) return false;
-
-    if (n <= WCAP) {
-        // rank sort by (value desc, token asc): keys are distinct, so ranks are a permutation
-        unsigned long long *srt = D.sorted;
-        for (int j = tid; j < n; j += NT) {
-            const unsigned long long c = D.cand[j];
-            int r = 0;
-            for (int i = 0; i < n; i++) r += D.cand[i] > c ? 1 : 0;
-            srt[r] = c;
-        }
-        __syncthreads();
-        SV_MARK(A, row_idx, 12);
-        if (warp == 0) warp_cut(S, srt, n, K, m, s, S.topp_on, S.P);
-        __syncthreads();
-        SV_MARK(A, row_idx, 13);
-        const int n2 = S.n2;
-        const float Z = S.zk;
-        st.Z = Z;
-        st.invZ = __frcp_rn(Z);
-        st.taukey = S.cutkey;
-        st.tau = key2f(S.cutkey);
-        st.kind = KIND_LIST;
-        st.nlist = n2;
-        // the kept set in token order (rank by token id), stored for the residual draw
-        int *ltok = reinterpret_cast<int *>(D.cand);
-        float *lw = reinterpret_cast<float *>(D.cand) + WCAP;
-        for (int j = tid; j < n2; j += NT) {
-            const uint32_t tj = ~(uint32_t)srt[j];
-            int r = 0;
-            for (int i = 0; i < n2; i++) r += (~(uint32_t)srt[i]) < tj ? 1 : 0;
-            ltok[r] = (int)tj;
-            lw[r] = weight(key2f((uint32_t)(srt[j] >> 32)), m, s);
-        }
-        __syncthreads();
-        int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
-        for (int j = tid; j < n2; j += NT) L[j] = make_int2(ltok[j], __float_as_int(lw[j]));
-        SV_MARK(A, row_idx, 14);
-        if (want_bonus) {
-            if (warp == 0) {
-                const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
-                float w8[8];
-#pragma unroll
-                for (int t = 0; t < 8; t++) w8[t] = (lane * 8 + t < n2) ? lw[lane * 8 + t] : 0.f;
-                const int j = warp_draw8(w8, n2, u);
-                if (lane == 0) S.tok = j >= 0 ? ltok[j] : -1;
-            }
-            __syncthreads();
-            st.bonus = S.tok;
-        }
-        SV_MARK(A, row_idx, 15);
-        return true;
-    }
-
-    // larger candidate sets: block-wide bitonic sort and scans
-    const int np = pow2_at_least(n);
-    for (int j = n + tid; j < np; j += NT) D.cand[j] = 0ull;
-    __syncthreads();
-    block_sort_desc(D.cand, np);
-    const int kk = min(K, n);
-    const uint32_t kkey = (uint32_t)(D.cand[kk - 1] >> 32);
-    int c1 = 0;
-    for (int j = tid; j < n; j += NT) c1 += ((uint32_t)(D.cand[j] >> 32) >= kkey) ? 1 : 0;
-    const int n1 = block_sum_i(c1, S.redi);
-    for (int j = tid; j < n1; j += NT) D.aux[j] = weight(key2f((uint32_t)(D.cand[j] >> 32)), m, s);
-    __syncthreads();
-    for (int j = tid; j < n1; j += NT) D.aux2[j] = D.aux[j];
-    __syncthreads();
-    block_scan_incl(D.aux2, n1, S.redf);
-    int n2 = n1;
-    if (S.topp_on) {
-        const float PZ = __fmul_rn(S.P, D.aux2[n1 - 1]);
-        int cut = 0x7fffffff;
-        for (int j = tid; j < n1; j += NT) {
-            if (j > 0 && (uint32_t)(D.cand[j] >> 32) != (uint32_t)(D.cand[j - 1] >> 32) && D.aux2[j - 1] >= PZ)
-                cut = min(cut, j);
-        }
-        cut = block_min_i(cut, S.redi);
-        if (cut != 0x7fffffff) n2 = cut;
-    }
-    const float Z = D.aux2[n2 - 1];
-    const uint32_t taukey = (uint32_t)(D.cand[n2 - 1] >> 32);
-    st.Z = Z;
-    st.invZ = __frcp_rn(Z);
-    st.taukey = taukey;
-    st.tau = key2f(taukey);
-    st.kind = n2 <= LCAP ? KIND_LIST : KIND_THRESH;
-    st.nlist = n2 <= LCAP ? n2 : 0;
-    __syncthreads();
-    if (n2 <= LCAP || want_bonus) {
-        const int np2 = pow2_at_least(n2);
-        for (int j = tid; j < np2; j += NT) {
-            unsigned long long c = D.cand[j];
-            D.cand[j] = j < n2 ? ((c << 32) | (c >> 32)) : 0ull;
-        }
-        __syncthreads();
-        block_sort_desc(D.cand, np2);
-        for (int j = tid; j < n2; j += NT) D.aux[j] = weight(key2f((uint32_t)D.cand[j]), m, s);
-        __syncthreads();
-        if (n2 <= LCAP) {
-            int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
-            for (int j = tid; j < n2; j += NT)
-                L[j] = make_int2((int32_t)(~(uint32_t)(D.cand[j] >> 32)), __float_as_int(D.aux[j]));
-        }
-        if (want_bonus) {
-            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
-            int j = draw_small(D.aux, D.aux2, n2, u, S);
-            st.bonus = j >= 0 ? (int32_t)(~(uint32_t)(D.cand[j] >> 32)) : -1;
-        }
-    }
-    __syncthreads();
-    return true;
-}
-
-// Kept set by radix select over the whole row (any top-k / top-p).
-template <typename E, bool VEC>
-__device__ void kept_by_select(const Args &A, Ctx &S, const Dyn &D, const E *row, RowStat &st, int row_idx,
-                               bool want_bonus) {
-    const int V = A.V, nseg = A.nseg;
-    const float m = S.m, s = S.s;
-    uint32_t key_lo = 0;
-    if (S.topk_on) key_lo = select_kth_row<E, VEC>(S, row, V, nseg, S.K, D.hcnt);
-    if (S.topp_on) key_lo = select_mass_row<E, VEC>(S, row, V, nseg, key_lo, m, s, S.P, D.hmass);
-    WKept wk{m, s, key_lo};
-    seg_sums<E, VEC, false>(S, row, nullptr, V, nseg, D.segB, wk, nullptr, wk);
-    float part = 0.f;
-    for (int j = threadIdx.x; j < nseg; j += NT) part += D.segB[j];
-    const float Z = block_sum(part, S.redf);
-    st.Z = Z;
-    st.invZ = __frcp_rn(Z);
-    st.taukey = key_lo;
-    st.tau = key_lo ? key2f(key_lo) : -INFINITY;
-    st.kind = KIND_THRESH;
-    st.nlist = 0;
-    if (want_bonus) {
-        const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
-        st.bonus = draw_by_segments<E, VEC, false>(S, row, nullptr, V, nseg, D.segB, u, wk);
-    }
-}
-
-template <typename E, bool VEC>
-__device__ void row_phase(const Args &A, Ctx &S, const Dyn &D, const int row_idx) {
-    const int tid = threadIdx.x;
-    const int V = A.V, nseg = A.nseg;
-    const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)row_idx * V;
-    RowStat st;
-    st.m = 0.f; st.s = 0.f; st.tau = -INFINITY; st.Z = 1.f; st.invZ = 1.f; st.taukey = 0;
-    st.argmax = -1; st.bonus = -1; st.kind = KIND_SKIP; st.nlist = 0; st.pad0 = 0; st.pad1 = 0;
-
-    const bool sampled = !S.greedy;
-    const int i = S.i;
-    const bool want_bonus = sampled && i == S.k;
-    float s = 0.f;
-    if (sampled) s = __fdiv_rn(LOG2E, S.T);
-    if (tid == 0) {
-        S.s = s;
-        S.topk_on = sampled && S.K > 0 && S.K < V;
-        S.topp_on = sampled && S.P < 1.f;
-    }
-    // The last thread prefetches this row's draft token x and the values z_x, q(x) that the
-    // accept test needs; they land while the row streams and are used after it.
-    int xtok = -1;
-    E zraw = E(0);
-    float qx = 0.f;
-    if (tid == NT - 1 && i < S.k) {
-        xtok = __ldg(A.tokens + S.d0 + i);
-        if (xtok >= 0 && xtok < V) {
-            zraw = __ldg(row + xtok);
-            if (sampled) qx = __ldg(A.q + (size_t)(S.d0 + i) * V + xtok);
-        }
-    }
-    __syncthreads();
-    const bool need_sum = sampled && !S.topk_on && !S.topp_on;
-    bool streamed = true;
-    if (VEC) streamed = pass_stats_ring<E>(S, D.ring, row, V, nseg, D.segA, D.segB, need_sum, s);
-    else pass_stats<E, VEC>(S, row, V, nseg, D.segA, D.segB, need_sum, s);
-    if (tid == NT - 1) {
-        S.xtok = xtok;
-        S.zx = elem_z_raw(S, zraw, xtok);
-        S.qx = qx;
-    }
-    __syncthreads();
-    SV_MARK(A, row_idx, 2);
-    if (!streamed) {
-        // a bounded wait expired: fail the row (its request's outputs become -1)
-        if (tid == 0) {
-            record_error(A, SV_DEV_TIMEOUT, S.b);
-            st.kind = KIND_FAIL;
-            A.stats[row_idx] = st;
-        }
-        return;
-    }
-    float mx = -INFINITY;
-    for (int j = tid; j < nseg; j += NT) mx = fmaxf(mx, D.segA[j]);
-    const float m = block_max(mx, S.redf);
-    if (tid == 0) S.m = m;
-    __syncthreads();
-    st.m = m;
-    st.s = s;
-
-    if (!sampled) {
-        // greedy: lowest id of the maximum -- first segment holding it, then first lane slot
-        int first = 0x7fffffff;
-        for (int j = tid; j < nseg; j += NT)
-            if (D.segA[j] == m) first = min(first, j);
-        first = block_min_i(first, S.redi);
-        if (warp_id() == 0) {
-            int best = 0x7fffffff;
-            if (first != 0x7fffffff) {
-                float v[8];
-                seg_values<E, VEC>(S, row, V, first, v);
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    int idx = first * SEG + lane_id() * 8 + j;
-                    if (idx < V && v[j] == m) best = min(best, idx);
-                }
-            }
-            best = warp_min_i(best);
-            if (lane_id() == 0) S.tok = best == 0x7fffffff ? 0 : best;
-        }
-        __syncthreads();
-        st.argmax = S.tok;
-        st.kind = KIND_GREEDY;
-    } else if (need_sum) {
-        // no filter: Z from the segment sums rescaled to the row max (fixed order)
-        float part = 0.f;
-        for (int j = tid; j < nseg; j += NT) {
-            float w = D.segA[j] > -INFINITY ? __fmul_rn(D.segB[j], weight(D.segA[j], m, s)) : 0.f;
-            D.segB[j] = w;
-            part += w;
-        }
-        const float Z = block_sum(part, S.redf);
-        st.Z = Z;
-        st.invZ = __frcp_rn(Z);
-        st.kind = KIND_FULL;
-        if (want_bonus) {
-            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
-            WKept wk{m, s, 0u};
-            st.bonus = draw_by_segments<E, VEC, false>(S, row, nullptr, V, nseg, D.segB, u, wk);
-        }
-    } else {
-        bool done = false;
-        if (S.topk_on && S.K <= KCAP) done = kept_from_candidates<E, VEC>(A, S, D, row, st, row_idx, want_bonus);
-        if (!done) kept_by_select<E, VEC>(A, S, D, row, st, row_idx, want_bonus);
-    }
-
-    SV_MARK(A, row_idx, 3);
-    // the draft of this row: p(x_i) and q(x_i)
-    if (tid == 0 && i < S.k) {
-        const int x = S.xtok;
-        float p = 0.f, q = 0.f;
-        if (!sampled) {
-            p = NAN;
-            q = NAN;
-        } else if (x >= 0 && x < V) {
-            const float z = S.zx;
-            p = fkey(z) >= st.taukey ? __fmul_rn(weight(z, m, s), st.invZ) : 0.f;
-            q = S.qx;
-        }
-        A.pq[(size_t)(S.d0 + i) * 2] = p;
-        A.pq[(size_t)(S.d0 + i) * 2 + 1] = q;
-        if (A.out_pq) {
-            A.out_pq[(size_t)(S.d0 + i) * 2] = p;
-            A.out_pq[(size_t)(S.d0 + i) * 2 + 1] = q;
-        }
-    }
-    if (tid == 0) A.stats[row_idx] = st;
-}
-
-// ------------------------------------------------------------------------------------------
-// the request phase (run by the CTA that completes the request's last row)
-// ------------------------------------------------------------------------------------------
-
-__device__ __forceinline__ RowStat load_stat(const RowStat *p) {
-    const int4 *q = reinterpret_cast<const int4 *>(p);
-    int4 a = __ldcg(q), b = __ldcg(q + 1), c = __ldcg(q + 2);
-    RowStat st;
-    st.m = __int_as_float(a.x); st.s = __int_as_float(a.y); st.tau = __int_as_float(a.z); st.Z = __int_as_float(a.w);
-    st.invZ = __int_as_float(b.x); st.taukey = (uint32_t)b.y; st.argmax = b.z; st.bonus = b.w;
-    st.kind = c.x; st.nlist = c.y; st.pad0 = c.z; st.pad1 = c.w;
-    return st;
-}
-
-// Accept test of one draft ("Speculative Decoding in Custom LLM Servicing...", "The Memory
-// Bandwidth Wall and Speculative Math"): accept with probability min(1, p/q), i.e. iff
-// u < min(1, p/q); q == 0 < p accepts and p == 0 rejects.
-__device__ __forceinline__ bool accept_test(float p, float q, float u) {
-    if (!(p > 0.f)) return false;
-    if (q == 0.f) return true;
-    const float ratio = __fdiv_rn(p, q);
-    return u < (ratio < 1.f ? ratio : 1.f);
+    return segstats_bytes(np) + scratch_bytes(np);
 }
 
 template <typename E, bool VEC, bool QVEC>
-__device__ void finalize(const Args &A, Ctx &S, const Dyn &D) {
-    const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
-    const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
-    if (warp == 0) {
-        // one lane per draft: validate, test, and find the first rejection by ballot
-        int status = S.status;
-        int a = -1, tok = -1, need = 0;
-        if (status == 0) {
-            const bool greedy = S.greedy;
-            bool badtok = false, baduni = false, badrow = false;
-            a = k;
-            for (int i0 = 0; i0 <= k; i0 += 32) {
-                const int i = i0 + lane;
-                bool rej = false;
-                if (i <= k && __ldcg(&A.stats[r0 + i].kind) == KIND_FAIL) badrow = true;
-                if (i < k) {
-                    const int x = __ldg(A.tokens + d0 + i);
-                    if (x < 0 || x >= V) badtok = true;
-                    if (greedy) {
-                        rej = x != __ldcg(&A.stats[r0 + i].argmax);
-                    } else {
-                        const float p = __ldcg(A.pq + (size_t)(d0 + i) * 2);
-                        const float q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
-                        rej = !accept_test(p, q, __ldg(A.uni + (size_t)(r0 + i) * 2));
-                    }
-                }
-                if (!greedy && i <= k) {
-                    const float u0 = __ldg(A.uni + (size_t)(r0 + i) * 2), u1 = __ldg(A.uni + (size_t)(r0 + i) * 2 + 1);
-                    if (!(u0 >= 0.f && u0 < 1.f) || !(u1 >= 0.f && u1 < 1.f)) baduni = true;
-                }
-                const unsigned msk = __ballot_sync(0xffffffffu, rej);
-                if (msk && a == k) a = i0 + __ffs(msk) - 1;
-            }
-            badtok = __any_sync(0xffffffffu, badtok);
-            baduni = __any_sync(0xffffffffu, baduni);
-            badrow = __any_sync(0xffffffffu, badrow);
-            if (badtok) status = SV_DEV_BAD_TOKEN;
-            else if (baduni) status = SV_DEV_BAD_UNIFORM;
-            else if (badrow) status = SV_DEV_TIMEOUT;
-            if (status == 0) {
-                if (greedy) tok = __ldcg(&A.stats[r0 + a].argmax);
-                else if (a == k) tok = __ldcg(&A.stats[r0 + k].bonus);
-                else need = 1;
-            } else {
-                a = -1;
-            }
-        }
-        if (lane == 0) {
-            if (status) record_error(A, status, b);
-            S.a = a;
-            S.tok = tok;
-            S.need_resid = need;
-        }
-    }
-    __syncthreads();
-    if (S.need_resid) {
-        // residual max(0, p - q) at the rejected row a ("Speculative Decoding in Custom LLM
-        // Servicing...", "The Memory Bandwidth Wall and Speculative Math")
-        const int a = S.a;
-        const RowStat st = load_stat(A.stats + r0 + a);
-        const float *qrow = A.q + (size_t)(d0 + a) * V;
-        const float u = __ldg(A.uni + (size_t)(r0 + a) * 2 + 1);
-        if (st.kind == KIND_LIST) {
-            // p is zero outside the stored kept list, so r is too: gather q on the list only
-            if (warp == 0) {
-                const int n = st.nlist;
-                const int2 *L = reinterpret_cast<const int2 *>(A.lists + (size_t)(r0 + a) * LCAP * 2);
-                int tk[8];
-                float pw[8], rw[8];
-#pragma unroll
-                for (int t = 0; t < 8; t++) {
-                    const int idx = lane * 8 + t;
-                    int2 e = idx < n ? __ldcg(L + idx) : make_int2(-1, 0);
-                    tk[t] = e.x;
-                    pw[t] = idx < n ? __fmul_rn(__int_as_float(e.y), st.invZ) : 0.f;
-                }
-#pragma unroll
-                for (int t = 0; t < 8; t++) {
-                    const float q = tk[t] >= 0 ? __ldg(qrow + tk[t]) : 0.f;
-                    rw[t] = tk[t] >= 0 ? fmaxf(__fsub_rn(pw[t], q), 0.f) : 0.f;
-                }
-                int j = warp_draw8(rw, n, u);
-                if (j < 0) j = warp_draw8(pw, n, u);      // empty residual: draw from p
-                int sel = -1;
-#pragma unroll
-                for (int t = 0; t < 8; t++)
-                    if (lane * 8 + t == j) sel = tk[t];
-                sel = __shfl_sync(0xffffffffu, sel, j >= 0 ? (j >> 3) : 0);
-                if (lane == 0) S.tok = j >= 0 ? sel : -1;
-            }
-            __syncthreads();
-        } else {
-            if (warp == 0) build_penalties(A, S, a);
-            __syncthreads();
-            const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)(r0 + a) * V;
-            WResid wr{st.m, st.s, st.invZ, st.taukey};
-            WProb wp{st.m, st.s, st.invZ, st.taukey};
-            seg_sums<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, wr, D.segC, wp);
-            int tok = draw_by_segments<E, VEC, QVEC>(S, row, qrow, V, A.nseg, D.segB, u, wr);
-            if (tok < 0) tok = draw_by_segments<E, VEC, QVEC>(S, row, nullptr, V, A.nseg, D.segC, u, wp);
-            if (tid == 0) S.tok = tok;
-            __syncthreads();
-        }
-    }
-    // outputs: accepted drafts, the final token, -1 padding
-    const int a = S.a, kw = A.k_max + 1;
-    for (int j = tid; j < kw; j += NT) {
-        int v = -1;
-        if (a >= 0) v = j < a ? __ldg(A.tokens + d0 + j) : (j == a ? S.tok : -1);
-        A.out_tok[(size_t)b * kw + j] = v;
-    }
-    if (tid == 0) {
-        A.acc[b] = a;
-        A.counters[b] = 0;
-    }
-}
-
-// Writes -1 outputs for a request that owns no rows (inconsistent row_offsets).
-__device__ __forceinline__ void fail_request(const Args &A, int b) {
-    const int kw = A.k_max + 1;
-    for (int j = threadIdx.x; j < kw; j += NT) A.out_tok[(size_t)b * kw + j] = -1;
-    if (threadIdx.x == 0) {
-        A.acc[b] = -1;
-        record_error(A, 1, b);
-    }
-}
-
-template <typename E, bool VEC, bool QVEC>
-__global__ void __launch_bounds__(NT, 4) verify_kernel(const Args A) {
+__global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ Ctx S;
-    const int tid = threadIdx.x;
+    __shared__ RowCtx S;
+    const Grp<RT, 0> g(threadIdx.x);
     const int r = blockIdx.x;
-    const Dyn D = carve(dsm, A.nseg);
+    const int np = nseg_pad(A.nseg);
+    const SegStats o = carve_segstats(dsm, np);
+    const Scratch X = carve_scratch(dsm + segstats_bytes(np), np);
     SV_MARK(A, r, 0);
-#ifdef SV_TIMING
-    if (tid == 0) {
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        A.timing[(size_t)r * NTIME + 6] = smid;
-        A.timing[(size_t)r * NTIME + 7] = 0;
-    }
-#endif
-    // start streaming this CTA's row right away; the request lookup overlaps the first copies
-    if (VEC && tid == 0) ring_start(S, D.ring, reinterpret_cast<const E *>(A.logits) + (size_t)r * A.V, A.V, (int)sizeof(E));
-
-    // locate the row: request b, row i within it
-    if (tid < 32) {
-        int b, r0, nrows;
-        bool ok = true;
-        if (A.row_off) {
-            b = find_request(A.row_off, A.B, r);
-            ok = b >= 0 && b < A.B;
-            r0 = ok ? __ldg(A.row_off + b) : 0;
-            int r1 = ok ? __ldg(A.row_off + b + 1) : 0;
-            ok = ok && r0 <= r && r < r1;
-            nrows = r1 - r0;
-        } else {
-            b = r / (A.k_max + 1);
-            r0 = b * (A.k_max + 1);
-            nrows = A.k_max + 1;
-        }
-        if (tid == 0) {
-            S.r0 = r0;
-            S.nrows = nrows;
-            S.i = r - r0;
-            S.d0 = r0 - b;
-            if (ok) {
-                load_request(A, S, b);
-            } else {
-                S.b = -1;
-                S.status = 1;
-                record_error(A, 1, b < 0 ? 0 : (b >= A.B ? A.B - 1 : b));
-            }
-            S.active = ok && S.status == 0 && S.i <= S.k;
-        }
-    }
-    __syncthreads();
-    SV_MARK(A, r, 1);
-    if (VEC && !S.active) {   // nothing to compute: let the speculative copies land first
-        if (tid == 0) ring_drain(S);
-        __syncthreads();
-    }
-    if (S.b < 0) return;   // row outside every request: nothing to count
-
-    // requests with no rows (row_offsets[j] == row_offsets[j+1]) are failed by the first row
-    // of the nearest non-empty request before them; leading ones by the request of row 0
-    if (A.row_off && S.i == 0) {
-        if (r == 0) {
-            for (int j = S.b - 1; j >= 0; j--) fail_request(A, j);
-        }
-        for (int j = S.b + 1; j < A.B && __ldg(A.row_off + j) == __ldg(A.row_off + j + 1); j++) fail_request(A, j);
-    }
-
+    if (g.warp() == 0) locate_row(A, S, r);
+    g.sync();
+    if (S.b < 0) return;   // a row outside every request: nothing to count
+    fail_empty_requests(g, A, S);
     if (S.active) {
-        if (tid < 32) build_penalties(A, S, S.i);
-        __syncthreads();
-        row_phase<E, VEC>(A, S, D, r);
+        const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)r * A.V;
+        if (g.warp() == 0) build_penalties(A, S, S.i);
+        for (int d = g.t; d < 256; d += RT) o.hist[d] = 0;
+        g.sync();
+        SV_MARK(A, r, 1);
+        // the last thread prefetches the row's draft gathers while the row streams
+        int x = -1;
+        E zraw = E(0);
+        float qx = 0.f;
+        if (g.t == RT - 1 && S.i < S.k) {
+            x = __ldg(A.tokens + S.d0 + S.i);
+            if (x >= 0 && x < A.V) {
+                zraw = __ldg(row + x);
+                if (!S.greedy) qx = __ldg(A.q + (size_t)(S.d0 + S.i) * A.V + x);
+            }
+        }
+        pass_stats<E, VEC>(g, S, row, A.V, A.nseg, o);
+        if (g.t == RT - 1) {
+            S.xtok = x;
+            S.zx = elem_z_raw(S, zraw, x);
+            S.qx = qx;
+        }
+        g.sync();
+        SV_MARK(A, r, 2);
+        select_row<E, VEC>(g, A, S, X, o);
     }
     SV_MARK(A, r, 4);
-
-    // arrival: the CTA that brings the count to the request's row count finalises it
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        int old = atomicAdd(A.counters + S.b, 1);
-        S.last = (old == S.nrows - 1);
-    }
-    __syncthreads();
-    if (S.last) {
-        __threadfence();
-        finalize<E, VEC, QVEC>(A, S, D);
-#ifdef SV_TIMING
-        if (tid == 0) A.timing[(size_t)r * NTIME + 7] = 1;
-#endif
-    }
+    arrive_and_finalize<E, VEC, QVEC>(g, A, S, X);
     SV_MARK(A, r, 5);
+}
+
+// ------------------------------------------------------------------------------------------
+// persistent kernel: 16-byte aligned rows
+// ------------------------------------------------------------------------------------------
+
+struct PShared {
+    unsigned long long full[PNS_MAX];   // ring stage holds its chunk (transaction count)
+    unsigned long long empty[PNS_MAX];  // every streamer warp released the stage
+    unsigned long long rb_desc[NRB];  // row buffer prepared by the scheduler
+    unsigned long long rb_stats[NRB]; // row buffer's segment statistics complete
+    unsigned long long rb_free[NRB];  // selector done with the row buffer
+    int fail;
+    RowCtx rc[NRB];
+};
+
+// Per row buffer of the persistent kernel: segment max, second value / weight sum, lane of the
+// max, and a bitmask of the segments holding a penalised token; rounded to 128 bytes so that
+// every buffer after it (and the 8-byte candidate keys of the scratch) stays aligned.
+__host__ __device__ inline size_t pstats_bytes(int np) { return ((size_t(3) * np + np / 32) * 4 + 127) & ~size_t(127); }
+
+__device__ __forceinline__ SegStats carve_pstats(unsigned char *p, int np, uint32_t *&dmask) {
+    SegStats o;
+    o.mx = reinterpret_cast<float *>(p);
+    o.b = o.mx + np;
+    o.lane = reinterpret_cast<int *>(o.b + np);
+    o.hist = nullptr;
+    dmask = reinterpret_cast<uint32_t *>(o.lane + np);
+    return o;
+}
+
+__host__ __device__ inline size_t persistent_smem(int nseg, int pns) {
+    const int np = nseg_pad(nseg);
+    return size_t(pns) * SB + size_t(NRB) * pstats_bytes(np) + scratch_bytes(np);
+}
+
+__device__ __forceinline__ void pfail(const Args &A, PShared &P, int b) {
+    P.fail = 1;
+    record_error(A, 7, b < 0 ? 0 : b);
+}
+
+template <typename E, bool QVEC>
+__global__ void __launch_bounds__(PT, PCTA) verify_persistent_kernel(const Args A) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ PShared P;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int V = A.V, nseg = A.nseg, np = nseg_pad(nseg), PNS = A.pns;
+    const uint32_t RB = (uint32_t)V * sizeof(E);
+    const int nc = (int)((RB + SB - 1) / SB);
+    constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
+    unsigned char *ring = dsm;
+    unsigned char *rbstats = dsm + size_t(PNS) * SB;   // after the ring
+    const Scratch X = carve_scratch(rbstats + size_t(NRB) * pstats_bytes(np), np);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PNS; s++) {
+            mbar_init(&P.full[s], 1);
+            mbar_init(&P.empty[s], PSTREAM);
+        }
+        for (int s = 0; s < NRB; s++) {
+            mbar_init(&P.rb_desc[s], 1);
+            mbar_init(&P.rb_stats[s], PSTREAM);
+            mbar_init(&P.rb_free[s], 1);
+        }
+        P.fail = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---- issuer: bulk copies of each prepared row, chunk by chunk, through the ring
+        if (lane != 0) return;
+        const unsigned long long pol = l2_evict_last();
+        int q = 0;
+        RingPos rp{0, 0u};
+        for (int j = 0;; j++) {
+            const int slot = j % NRB;
+            if (!mbar_wait(&P.rb_desc[slot], (uint32_t)(j / NRB) & 1u)) {
+                pfail(A, P, -1);
+                return;
+            }
+            const RowCtx &R = P.rc[slot];
+            if (R.r < 0) return;
+            const unsigned char *src = reinterpret_cast<const unsigned char *>(A.logits) + (size_t)R.r * RB;
+            for (int c = 0; c < R.nchunks; c++, q++) {
+                const int st = rp.st;
+#ifdef SV_TIMING
+                const unsigned long long tw = global_ns();
+#endif
+                // the stage's previous fill (one lap earlier) must have been released
+                if (q >= PNS && !mbar_wait(&P.empty[st], rp.ph ^ 1u)) {
+                    pfail(A, P, R.b);
+                    return;
+                }
+#ifdef SV_TIMING
+                A.timing[(size_t)R.r * NTIME + 11] += global_ns() - tw;
+#endif
+                const uint32_t off = (uint32_t)c * SB;
+                const uint32_t bytes = min((uint32_t)SB, RB - off);
+                mbar_expect_tx(&P.full[st], bytes);
+                bulk_g2s(ring + st * SB, src + off, bytes, &P.full[st], pol);
+                rp.next(PNS);
+            }
+        }
+    } else if (warp == 1) {
+        // ---- scheduler: claim rows and prepare their descriptors up to NRB rows ahead
+        for (int j = 0;; j++) {
+            const int slot = j % NRB;
+            bool ok = true;
+            if (j >= NRB) ok = mbar_wait_idle(&P.rb_free[slot], (uint32_t)(j / NRB - 1) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) pfail(A, P, -1);
+                return;
+            }
+            RowCtx &R = P.rc[slot];
+            int r = 0;
+            if (lane == 0) r = atomicAdd(A.hdr + 2, 1);
+            r = __shfl_sync(0xffffffffu, r, 0);
+            if (r >= A.R) {
+                if (lane == 0) {
+                    R.r = -1;
+                    mbar_arrive(&P.rb_desc[slot]);
+                }
+                return;
+            }
+            SV_MARK(A, r, 0);
+#ifdef SV_TIMING
+            if (lane == 0) {
+                unsigned smid;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                A.timing[(size_t)r * NTIME + 6] = ((unsigned long long)blockIdx.x << 32) | smid;
+                A.timing[(size_t)r * NTIME + 7] = 0;
+                A.timing[(size_t)r * NTIME + 10] = 0;
+                A.timing[(size_t)r * NTIME + 11] = 0;
+            }
+#endif
+            locate_row(A, R, r);
+            if (R.active) build_penalties(A, R, R.i);
+            __syncwarp();
+            if (R.active && R.npen > 0) {
+                // segments holding a penalised token take the streamers' slow path
+                uint32_t *dmask;
+                carve_pstats(rbstats + size_t(slot) * pstats_bytes(np), np, dmask);
+                for (int w = lane; w < np / 32; w += 32) dmask[w] = 0u;
+                __syncwarp();
+                for (int h = lane; h < R.npen; h += 32) {
+                    const int x = R.pid[h];
+                    if (x >= 0 && x < V) atomicOr(&dmask[(x / SEG) >> 5], 1u << ((x / SEG) & 31));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                prefetch_draft<E>(A, R, reinterpret_cast<const E *>(A.logits) + (size_t)r * V);
+                R.nchunks = R.active ? nc : 0;
+                SV_MARK(A, r, 1);
+                mbar_arrive(&P.rb_desc[slot]);
+            }
+            __syncwarp();
+        }
+    } else if (warp < 2 + PSTREAM) {
+        // ---- streamers: per-segment statistics of each row from the ring
+        const int sw = warp - 2;
+        RingPos rp{0, 0u};
+        for (int j = 0;; j++) {
+            const int slot = j % NRB;
+            if (!__all_sync(0xffffffffu, mbar_wait(&P.rb_desc[slot], (uint32_t)(j / NRB) & 1u))) {
+                if (lane == 0) pfail(A, P, -1);
+                return;
+            }
+            const RowCtx &R = P.rc[slot];
+            if (R.r < 0) return;
+            uint32_t *dmask;
+            const SegStats o = carve_pstats(rbstats + size_t(slot) * pstats_bytes(np), np, dmask);
+            unsigned long long *tslot = nullptr;
+#ifdef SV_TIMING
+            tslot = A.timing + (size_t)R.r * NTIME;
+#endif
+            if (!stream_row_any<E>(P.full, P.empty, ring, PNS, rp, R.nchunks, nseg, V, sw, R, o, dmask, tslot)) {
+                if (lane == 0) pfail(A, P, R.b);
+                return;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (sw == 0) SV_MARK(A, R.r, 2);
+                mbar_arrive(&P.rb_stats[slot]);
+            }
+        }
+    } else {
+        // ---- selectors: kept set, draws and gathers of each finished row; finalisation
+        const Grp<PSEL * 32, 1> g(threadIdx.x - 32 * (2 + PSTREAM));
+        for (int j = 0;; j++) {
+            const int slot = j % NRB;
+            const uint32_t par = (uint32_t)(j / NRB) & 1u;
+            const bool ok = mbar_wait_idle(&P.rb_desc[slot], par);
+            RowCtx &R = P.rc[slot];
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) pfail(A, P, -1);
+            }
+            g.sync();
+            if (P.fail || R.r < 0) return;
+            const bool ok2 = mbar_wait_idle(&P.rb_stats[slot], par);
+            if (!__all_sync(0xffffffffu, ok2)) {
+                if (lane == 0) pfail(A, P, R.b);
+            }
+            g.sync();
+            if (P.fail) return;
+            SV_MARK(A, R.r, 9);
+            if (R.b >= 0) {
+                fail_empty_requests(g, A, R);
+                uint32_t *dmask;
+                const SegStats o = carve_pstats(rbstats + size_t(slot) * pstats_bytes(np), np, dmask);
+                if (R.active) select_row<E, true>(g, A, R, X, o);
+                SV_MARK(A, R.r, 4);
+                arrive_and_finalize<E, true, QVEC>(g, A, R, X);
+                SV_MARK(A, R.r, 5);
+            }
+            g.sync();
+            if (g.t == 0) mbar_arrive(&P.rb_free[slot]);
+        }
+    }
 }
 
 __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *nd, int B, int32_t *hdr) {
@@ -749,17 +336,59 @@ __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *
 // host side
 // ------------------------------------------------------------------------------------------
 
-template <typename E, bool VEC, bool QVEC>
-static cudaError_t launch(const Args &A, cudaStream_t stream) {
-    static size_t smem_set = 0;   // largest dynamic shared memory size enabled so far
-    const size_t smem = dyn_bytes(A.nseg);
-    auto kern = verify_kernel<E, VEC, QVEC>;
-    if (smem > 48 * 1024 && smem > smem_set) {
+template <typename K>
+static cudaError_t ensure_smem(K kern, size_t smem, size_t &enabled) {
+    if (smem > 48 * 1024 && smem > enabled) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        smem_set = smem;
+        enabled = smem;
     }
-    kern<<<A.R, NT, smem, stream>>>(A);
+    return cudaSuccess;
+}
+
+template <typename E, bool VEC, bool QVEC>
+static cudaError_t launch_rows(const Args &A, cudaStream_t stream) {
+    static size_t enabled = 0;
+    const size_t smem = rows_smem(A.nseg);
+    auto kern = verify_rows_kernel<E, VEC, QVEC>;
+    cudaError_t e = ensure_smem(kern, smem, enabled);
+    if (e != cudaSuccess) return e;
+    kern<<<A.R, RT, smem, stream>>>(A);
+    return cudaGetLastError();
+}
+
+// Launches the persistent kernel with (SMs x resident CTAs) CTAs; returns cudaErrorNotSupported
+// (nothing launched) when it cannot be resident for this vocabulary.
+template <typename E, bool QVEC>
+static cudaError_t launch_persistent(const Args &A, cudaStream_t stream) {
+    static size_t enabled = 0;
+    static int sms[64] = {0};
+    static int occ_for_nseg[64] = {0};
+    static int occ_val[64] = {0};
+    // the deepest ring (3..PNS_MAX stages) that still lets two CTAs share an SM
+    Args B = A;
+    B.pns = PNS_MAX;
+    while (B.pns > 3 && PCTA * (persistent_smem(A.nseg, B.pns) + sizeof(PShared) + 1024) > 228 * 1024) B.pns--;
+    const size_t smem = persistent_smem(A.nseg, B.pns);
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    auto kern = verify_persistent_kernel<E, QVEC>;
+    cudaError_t e = ensure_smem(kern, smem, enabled);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+    if (!sms[dev] && (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    if (occ_for_nseg[dev] != A.nseg) {
+        int occ = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, PT, smem)) != cudaSuccess) return e;
+        occ_val[dev] = occ;
+        occ_for_nseg[dev] = A.nseg;
+    }
+    const int occ = occ_val[dev];
+    if (occ < 1) return cudaErrorNotSupported;
+    const int grid = (int)((long long)sms[dev] * occ < (long long)A.R ? sms[dev] * occ : A.R);
+    kern<<<grid, PT, smem, stream>>>(B);
     return cudaGetLastError();
 }
 
@@ -797,7 +426,6 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
     if (!target_logits || !num_drafts || !uniforms || !out_tokens || !accept_len || !workspace) return SV_ERR_INVALID_ARG;
     if (D > 0 && (!draft_probs || !draft_tokens)) return SV_ERR_INVALID_ARG;
     if (!params.temperature || !params.top_k || !params.top_p || !params.greedy) return SV_ERR_INVALID_ARG;
-    if ((long long)total_rows * V > (1ll << 62)) return SV_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(B, total_rows);
     if (((uintptr_t)workspace & 255) != 0 || workspace_bytes < L.total) return SV_ERR_WORKSPACE;
 
@@ -829,21 +457,28 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
     A.V = V;
     A.R = total_rows;
     A.nseg = (V + SEG - 1) / SEG;
+    A.pns = 0;
     const size_t esz = logits_dtype == SV_BF16 ? 2 : 4;
     const bool vec = ((uintptr_t)target_logits % 16 == 0) && ((size_t)V * esz) % 16 == 0;
     const bool qvec = (!draft_probs || (uintptr_t)draft_probs % 16 == 0) && ((size_t)V * 4) % 16 == 0;
-    A.q_vec = qvec;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // clear the error word and the per-request arrival counters
+    // clear the error word, the row claim counter and the per-request arrival counters
     if (cudaMemsetAsync(ws, 0, L.counters + (size_t)B * 4, st) != cudaSuccess) return SV_ERR_CUDA;
-    cudaError_t e;
-    if (logits_dtype == SV_BF16) {
-        if (vec) e = qvec ? launch<uint16_t, true, true>(A, st) : launch<uint16_t, true, false>(A, st);
-        else e = qvec ? launch<uint16_t, false, true>(A, st) : launch<uint16_t, false, false>(A, st);
-    } else {
-        if (vec) e = qvec ? launch<float, true, true>(A, st) : launch<float, true, false>(A, st);
-        else e = qvec ? launch<float, false, true>(A, st) : launch<float, false, false>(A, st);
+    cudaError_t e = cudaErrorNotSupported;
+    if (vec) {
+        if (logits_dtype == SV_BF16) e = qvec ? launch_persistent<uint16_t, true>(A, st) : launch_persistent<uint16_t, false>(A, st);
+        else e = qvec ? launch_persistent<float, true>(A, st) : launch_persistent<float, false>(A, st);
+    }
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();   // clear a sticky "not supported" from the probe, if any
+        if (logits_dtype == SV_BF16) {
+            if (vec) e = qvec ? launch_rows<uint16_t, true, true>(A, st) : launch_rows<uint16_t, true, false>(A, st);
+            else e = qvec ? launch_rows<uint16_t, false, true>(A, st) : launch_rows<uint16_t, false, false>(A, st);
+        } else {
+            if (vec) e = qvec ? launch_rows<float, true, true>(A, st) : launch_rows<float, true, false>(A, st);
+            else e = qvec ? launch_rows<float, false, true>(A, st) : launch_rows<float, false, false>(A, st);
+        }
     }
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

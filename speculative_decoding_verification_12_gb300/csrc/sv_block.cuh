@@ -3,6 +3,8 @@
 // a shared-memory bitonic sort, vectorised row loads and the token-weight function.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "sv_common.cuh"
 
 namespace sv {
@@ -22,9 +24,10 @@ __device__ __forceinline__ float weight(float z, float m, float s) {
     return ex2(__fmul_rn(__fsub_rn(z, m), s));
 }
 
-// Order-preserving uint32 key of a float: a < b  <=>  fkey(a) < fkey(b) (for non-NaN).
+// Order-preserving uint32 key of a float: a < b  <=>  fkey(a) < fkey(b) (for non-NaN); -0 and
+// +0 share the key of +0, so equal values always tie.
 __device__ __forceinline__ uint32_t fkey(float z) {
-    uint32_t b = __float_as_uint(z);
+    uint32_t b = z == 0.f ? 0u : __float_as_uint(z);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 __device__ __forceinline__ float key2f(uint32_t k) {
@@ -41,6 +44,13 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+// Warp-wide max of a float in one instruction (redux.sync, sm_100 family).
+__device__ __forceinline__ float redux_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ int warp_min_i(int v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -57,66 +67,90 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     return v;
 }
 
-// Block-wide reductions over all NT threads; every thread gets the result.  `red` is a
-// shared scratch of NWARP words; the partials are combined in warp order (deterministic).
-__device__ __forceinline__ float block_max(float v, float *red) {
+// A group of NTH threads (whole warps) that synchronises on named barrier BAR (0: the whole
+// CTA via __syncthreads).  Reductions combine per-warp partials in warp order, so they are
+// deterministic.
+template <int NTH, int BAR>
+struct Grp {
+    static constexpr int kThreads = NTH;
+    static constexpr int kWarps = NTH / 32;
+    int t;   // thread index within the group
+    __device__ __forceinline__ explicit Grp(int t_) : t(t_) {}
+    __device__ __forceinline__ int warp() const { return t >> 5; }
+    __device__ __forceinline__ int lane() const { return t & 31; }
+    __device__ __forceinline__ void sync() const {
+        if constexpr (BAR == 0) {
+            __syncthreads();
+        } else {
+            asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NTH) : "memory");
+        }
+    }
+};
+
+template <class G>
+__device__ __forceinline__ float g_max(const G &g, float v, float *red) {
     v = warp_max(v);
-    if (lane_id() == 0) red[warp_id()] = v;
-    __syncthreads();
+    if (g.lane() == 0) red[g.warp()] = v;
+    g.sync();
     float r = red[0];
 #pragma unroll
-    for (int w = 1; w < NWARP; w++) r = fmaxf(r, red[w]);
-    __syncthreads();
+    for (int w = 1; w < G::kWarps; w++) r = fmaxf(r, red[w]);
+    g.sync();
     return r;
 }
-__device__ __forceinline__ float block_sum(float v, float *red) {
+template <class G>
+__device__ __forceinline__ float g_sum(const G &g, float v, float *red) {
     v = warp_sum(v);
-    if (lane_id() == 0) red[warp_id()] = v;
-    __syncthreads();
+    if (g.lane() == 0) red[g.warp()] = v;
+    g.sync();
     float r = red[0];
 #pragma unroll
-    for (int w = 1; w < NWARP; w++) r += red[w];
-    __syncthreads();
+    for (int w = 1; w < G::kWarps; w++) r += red[w];
+    g.sync();
     return r;
 }
-__device__ __forceinline__ int block_min_i(int v, int *red) {
+template <class G>
+__device__ __forceinline__ int g_min_i(const G &g, int v, int *red) {
     v = warp_min_i(v);
-    if (lane_id() == 0) red[warp_id()] = v;
-    __syncthreads();
+    if (g.lane() == 0) red[g.warp()] = v;
+    g.sync();
     int r = red[0];
 #pragma unroll
-    for (int w = 1; w < NWARP; w++) r = min(r, red[w]);
-    __syncthreads();
+    for (int w = 1; w < G::kWarps; w++) r = min(r, red[w]);
+    g.sync();
     return r;
 }
-__device__ __forceinline__ int block_max_i(int v, int *red) {
+template <class G>
+__device__ __forceinline__ int g_max_i(const G &g, int v, int *red) {
     v = warp_max_i(v);
-    if (lane_id() == 0) red[warp_id()] = v;
-    __syncthreads();
+    if (g.lane() == 0) red[g.warp()] = v;
+    g.sync();
     int r = red[0];
 #pragma unroll
-    for (int w = 1; w < NWARP; w++) r = max(r, red[w]);
-    __syncthreads();
+    for (int w = 1; w < G::kWarps; w++) r = max(r, red[w]);
+    g.sync();
     return r;
 }
-__device__ __forceinline__ int block_sum_i(int v, int *red) {
+template <class G>
+__device__ __forceinline__ int g_sum_i(const G &g, int v, int *red) {
     v = warp_sum_i(v);
-    if (lane_id() == 0) red[warp_id()] = v;
-    __syncthreads();
+    if (g.lane() == 0) red[g.warp()] = v;
+    g.sync();
     int r = 0;
 #pragma unroll
-    for (int w = 0; w < NWARP; w++) r += red[w];
-    __syncthreads();
+    for (int w = 0; w < G::kWarps; w++) r += red[w];
+    g.sync();
     return r;
 }
 
 // In-place inclusive prefix sum of a[0..n) in shared memory.  Thread t sums a contiguous
 // chunk; chunk totals are scanned across lanes and warps in a fixed order, so the result is
 // deterministic.  a[n-1] ends up holding the total.
-__device__ __forceinline__ void block_scan_incl(float *a, int n, float *red) {
-    const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
-    const int per = (n + NT - 1) / NT;
-    const int lo = min(n, tid * per), hi = min(n, lo + per);
+template <class G>
+__device__ __forceinline__ void g_scan_incl(const G &g, float *a, int n, float *red) {
+    const int lane = g.lane(), warp = g.warp();
+    const int per = (n + G::kThreads - 1) / G::kThreads;
+    const int lo = min(n, g.t * per), hi = min(n, lo + per);
     float t = 0.f;
     for (int j = lo; j < hi; j++) t += a[j];
     float incl = t;
@@ -128,7 +162,7 @@ __device__ __forceinline__ void block_scan_incl(float *a, int n, float *red) {
     float excl = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) excl = 0.f;
     if (lane == 31) red[warp] = incl;
-    __syncthreads();
+    g.sync();
     float run = 0.f;
     for (int w = 0; w < warp; w++) run += red[w];
     run += excl;
@@ -136,14 +170,15 @@ __device__ __forceinline__ void block_scan_incl(float *a, int n, float *red) {
         run += a[j];
         a[j] = run;
     }
-    __syncthreads();
+    g.sync();
 }
 
 // Sorts keys[0..np) (np a power of two) into descending order.
-__device__ __forceinline__ void block_sort_desc(unsigned long long *keys, int np) {
+template <class G>
+__device__ __forceinline__ void g_sort_desc(const G &g, unsigned long long *keys, int np) {
     for (int k = 2; k <= np; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int t = threadIdx.x; t < (np >> 1); t += NT) {
+            for (int t = g.t; t < (np >> 1); t += G::kThreads) {
                 int i1 = (t / j) * 2 * j + (t % j);
                 int i2 = i1 + j;
                 unsigned long long a = keys[i1], b = keys[i2];
@@ -153,7 +188,7 @@ __device__ __forceinline__ void block_sort_desc(unsigned long long *keys, int np
                     keys[i2] = a;
                 }
             }
-            __syncthreads();
+            g.sync();
         }
     }
 }
@@ -238,21 +273,67 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+#ifndef SV_WAIT_HINT
+#define SV_WAIT_HINT 10000
+#endif
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the phase is pending.
+__device__ __forceinline__ bool mbar_try_wait_for(unsigned long long *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase of `parity` to complete; false once WAIT_NS has passed without it.
+// The first polls skip the clock so that the common, short waits stay cheap.
 __device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity) {
+#if SV_WAIT_HINT > 0
     if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_for(bar, parity, SV_WAIT_HINT))
+        if (global_ns() - t0 > WAIT_NS) return false;
+    return true;
+#else
+    for (int i = 0; i < 256; i++)
+        if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
         if (global_ns() - t0 > WAIT_NS) return false;
     return true;
+#endif
+}
+// As mbar_wait, for waits that are usually long (a warp idle until the next row): between
+// polls the thread sleeps, so that it takes no issue slots from the warps doing work.
+__device__ __forceinline__ bool mbar_wait_idle(unsigned long long *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    unsigned ns = 64;
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(ns);
+        ns = ns < 1024 ? ns * 2 : 1024;
+        if (global_ns() - t0 > WAIT_NS) return false;
+    }
+    return true;
+}
+
+// L2 policy that keeps lines resident in preference to others (rows re-read shortly after
+// they stream stay in L2).
+__device__ __forceinline__ unsigned long long l2_evict_last() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 // One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16) that
-// completes `bytes` of transaction count on `bar`.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, unsigned long long *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
+// completes `bytes` of transaction count on `bar`, with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, unsigned long long *bar,
+                                         unsigned long long pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
 }
 
 // ------------------------------------------------------------------------------------------

@@ -1,5 +1,5 @@
-// sv_common.cuh -- constants, workspace layout and small device helpers shared by the
-// verification kernels (sm_103a).
+// sv_common.cuh -- constants, per-row statistics, workspace layout and kernel arguments shared
+// by the verification kernels (sm_103a).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -7,21 +7,51 @@
 
 namespace sv {
 
-constexpr int NT = 256;               // threads per row CTA
-constexpr int NWARP = NT / 32;
 constexpr int SEG = 256;              // elements per segment: one warp step of 32 lanes x 8
-constexpr int CAP = 2048;             // candidate buffer (top-k candidates, kept lists) per CTA
+constexpr int CAP = 1536;             // candidate buffer (top-k candidates, kept lists) per CTA
 constexpr int KCAP = 512;             // top-k up to this goes through the candidate buffer
 constexpr int WCAP = 256;             // candidate sets up to this are cut and drawn by one warp
 constexpr int LCAP = 256;             // kept-list entries stored per row for the residual draw
 constexpr int HB = 2048;              // radix histogram bins (11-bit digits)
-constexpr int NS = 4;                 // stages of the shared-memory row ring (bulk copies in flight)
-constexpr int SB = 8192;              // bytes per ring stage
+#ifndef SV_SB
+#define SV_SB 12288
+#endif
+constexpr int SB = SV_SB;             // bytes per ring stage (one bulk copy)
 constexpr unsigned long long WAIT_NS = 2000000000ull;   // give up on an mbarrier after 2 s
 constexpr int MAXK = 64;              // largest k_max
 constexpr int MAXV = 1 << 21;         // largest vocabulary
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr double FIXED_ONE = 1099511627776.0;   // 2^40: fixed-point scale of token weights
+
+// Row kernel (one CTA per row; any alignment): 256 threads, 8 warps.
+constexpr int RT = 256;
+
+// Persistent kernel (16-byte aligned rows): warp 0 issues bulk copies, warp 1 schedules rows,
+// PSTREAM warps reduce the streamed chunks, PSEL warps select the kept set and finalise.
+#ifndef SV_PSTREAM
+#define SV_PSTREAM 8
+#endif
+#ifndef SV_PCTA
+#define SV_PCTA 2
+#endif
+constexpr int PSTREAM = SV_PSTREAM;
+constexpr int PSEL = 4;
+constexpr int PCTA = SV_PCTA;         // resident CTAs per SM the kernel is built for
+constexpr int PT = 32 * (2 + PSTREAM + PSEL);
+#ifndef SV_PNS_MAX
+#define SV_PNS_MAX 8
+#endif
+constexpr int PNS_MAX = SV_PNS_MAX;   // ring stages at most (the launch picks what fits)
+constexpr int NRB = 3;                // row buffers (rows between scheduler and selector)
+
+// What the streaming pass records per 256-token segment of a row (besides its max).
+enum : int32_t {
+    MODE_MAX = 0,      // max only (rows whose kept set needs a radix select over the row)
+    MODE_ARG = 1,      // + the lowest lane holding the max (greedy rows)
+    MODE_TOP2 = 2,     // + that lane, the segment's second-largest value and a histogram of the
+                       //   top byte of the maxima's order keys (rows with a small top-k)
+    MODE_SUM = 3       // + sum of 2^((z - max) s) (rows that keep every token)
+};
 
 // How a row's kept set is represented once its statistics are known.
 enum : int32_t {
@@ -33,7 +63,7 @@ enum : int32_t {
     KIND_FAIL = 5      // the row's stream did not complete (bounded wait expired)
 };
 
-// Per-row statistics written by the row CTA and read by the request's finalising CTA.
+// Per-row statistics written by the row's selection and read by the request's finaliser.
 // Token weights are e_v = 2^((z_v - m) * s), s = log2(e) / T; p_v = [z_v >= tau] e_v / Z.
 struct __align__(16) RowStat {
     float m;        // max of z over the row (z = logit - penalty)
@@ -46,23 +76,22 @@ struct __align__(16) RowStat {
     int32_t bonus;  // token drawn from this row's p with slot-1 uniform (sampled rows), else -1
     int32_t kind;
     int32_t nlist;  // KIND_LIST: number of list entries
-    int32_t pad0, pad1;
+    int32_t resid;  // KIND_LIST rows with a draft: the residual draw should this draft be rejected
+    int32_t pad1;
 };
 
 struct WsLayout {
     size_t counters, stats, pq, lists, timing, total;
 };
 
-// Phase timestamps (globaltimer ns) per row CTA, recorded only in builds with SV_TIMING:
-// [0] start, [1] request located, [2] row streamed, [3] kept set done, [4] row written,
-// [5] finalised, [6] SM id, [7] 1 if this CTA finalised its request, [8..15] steps of the
-// candidate path (bound, segment list, re-read, sort, cut, list, draw).
-constexpr int NTIME = 16;
+// Phase timestamps (globaltimer ns) per row, recorded only in builds with SV_TIMING.
+constexpr int NTIME = 24;
 
 __host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: [header 256 B: error word, first bad request][per-request arrival counters]
-// [RowStat per row][(p, q) per draft][kept lists: LCAP x (token, weight) per row].
+// Workspace: [header 256 B: error word, first bad request, row claim counter]
+// [per-request arrival counters][RowStat per row][(p, q) per draft]
+// [kept lists: LCAP x (token, weight) per row][timing, SV_TIMING builds only].
 __host__ __device__ inline WsLayout ws_layout(int B, int R) {
     WsLayout L;
     size_t o = 256;
@@ -98,14 +127,14 @@ struct Args {
     int32_t *out_tok;
     int32_t *acc;
     float *out_pq;            // may be NULL
-    int32_t *hdr;             // [0] error code, [1] first bad request
+    int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] row claim counter
     int32_t *counters;
     RowStat *stats;
     float *pq;
     int32_t *lists;
     unsigned long long *timing;   // SV_TIMING builds only
     int B, k_max, V, R, nseg;
-    int q_vec;                // draft-prob rows are 16-byte aligned
+    int pns;                  // persistent kernel: ring stages
 };
 
 }  // namespace sv

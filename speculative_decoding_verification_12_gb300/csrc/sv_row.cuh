@@ -1,37 +1,40 @@
-// sv_row.cuh -- per-row work of the verify kernel: locating the row, building the
-// presence/frequency penalties of the drafts before it, streaming the row once for its
-// statistics, selecting the kept set (top-k / top-p) and drawing tokens by inverse CDF.
+// sv_row.cuh -- per-row work of the verify kernels: locating a row and its request, the
+// presence/frequency penalties of the drafts before it, the per-segment statistics of the
+// streamed row, the kept set (top-k / top-p), and draws by inverse CDF.
 //
 // Method ("Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust",
 // "The Verification Algorithm"; FreeToken PR #836, "Design"): each of a request's k+1 target
 // rows becomes p = softmax(z / T) over the tokens kept by top-k and then top-p, where
 // z = logit - presence*[c > 0] - frequency*c counts the drafts before the row.
 //
-// All sums that feed a decision use a fixed association (deterministic reductions), so
-// results are bitwise reproducible run to run.
+// Everything that works on a whole row is templated on a thread group G (sv_block.cuh), so
+// the same code serves the one-CTA-per-row kernel and the selector warps of the persistent
+// kernel.  Sums that feed a decision use a fixed association: results are bitwise
+// reproducible run to run.
 #pragma once
 
 #include "sv_block.cuh"
 
 namespace sv {
 
-// Static shared state of one row CTA.
-struct Ctx {
-    unsigned long long full[NS];    // ring stage holds its chunk (transaction-count barrier)
-    unsigned long long empty[NS];   // every warp is done with the stage
-    int issued, ring_fail;
-    int b, i, k, r0, d0, nrows, status, active, greedy;
-    int K, topk_on, topp_on;
-    float T, P, pres, freq, s, m;
+// One row and its request, plus the scratch the row's selection uses.
+struct RowCtx {
+    // the row
+    int r, b, i, k, r0, d0, nrows, status, active, greedy, K;
+    float T, P, pres, freq, s;
+    int topk_on, topp_on, need_sum, mode, nchunks;
     int npen;
     int pid[MAXK];
     float ppen[MAXK];
     int draft_raw[MAXK];
-    float redf[NWARP];
-    int redi[NWARP];
+    int xtok;       // the row's draft token (-1 if none), its penalised target value and q value
+    float zx, qx;
+    // selection scratch
+    float m;
+    float redf[16];
+    int redi[16];
     int ncand, nsel, n2;
-    float zx, qx, zk;
-    int xtok;
+    float zk;
     uint32_t cutkey;
     int sel_digit;
     long long sel_below;
@@ -39,6 +42,12 @@ struct Ctx {
     double sel_target;
     int last, a, tok, need_resid;
 };
+
+// Records a device-data error: the first code wins; the lowest request index is kept.
+__device__ __forceinline__ void record_error(const Args &A, int code, int b) {
+    atomicCAS(A.hdr, 0, code);
+    atomicMax(A.hdr + 1, 0x7fffffff - b);
+}
 
 // ------------------------------------------------------------------------------------------
 // locating a row and its request
@@ -64,25 +73,28 @@ __device__ __forceinline__ int find_request(const int32_t *off, int B, int r) {
     return ans;
 }
 
-// Request-level checks shared by every row of the request (thread 0 only).
-__device__ __forceinline__ void load_request(const Args &A, Ctx &S, int b) {
+// Request-level checks shared by every row of the request (one thread).
+__device__ __forceinline__ void load_request(const Args &A, RowCtx &S, int b) {
     S.b = b;
-    int k = __ldg(A.nd + b);
-    S.k = k;
-    int status = 0;
-    if (k < 0 || k > A.k_max || k > S.nrows - 1) status = 1;           // SV_DEV_BAD_LAYOUT
-    S.greedy = __ldg(A.greedy + b) != 0;
-    S.pres = A.pres ? __ldg(A.pres + b) : 0.f;
-    S.freq = A.freq ? __ldg(A.freq + b) : 0.f;
-    if (!isfinite(S.pres) || !isfinite(S.freq)) status = status ? status : 6;
+    const int k = __ldg(A.nd + b);
+    const int greedy = __ldg(A.greedy + b) != 0;
+    const float pres = A.pres ? __ldg(A.pres + b) : 0.f;
+    const float freq = A.freq ? __ldg(A.freq + b) : 0.f;
     // every field is loaded up front (one round trip); greedy requests ignore T, P and K
     const float T = __ldg(A.T + b);
     const float P = __ldg(A.topp + b);
     const int K = __ldg(A.topk + b);
+    int status = 0;
+    if (k < 0 || k > A.k_max || k > S.nrows - 1) status = 1;           // SV_DEV_BAD_LAYOUT
+    if (!isfinite(pres) || !isfinite(freq)) status = status ? status : 6;
+    S.k = k;
+    S.greedy = greedy;
+    S.pres = pres;
+    S.freq = freq;
     S.T = 1.f;
     S.P = 1.f;
     S.K = 0;
-    if (!S.greedy) {
+    if (!greedy) {
         if (!(T > 0.f) || !isfinite(T)) status = status ? status : 3;
         if (!(P > 0.f && P <= 1.f)) status = status ? status : 4;
         S.T = T;
@@ -92,13 +104,65 @@ __device__ __forceinline__ void load_request(const Args &A, Ctx &S, int b) {
     S.status = status;
 }
 
+// Everything about row r that does not depend on its data: request, validity, sampling
+// parameters and filter switches.  Run by one warp.
+__device__ __forceinline__ void locate_row(const Args &A, RowCtx &S, int r) {
+    const int lane = lane_id();
+    int b, r0, nrows;
+    bool ok = true;
+    if (A.row_off) {
+        b = find_request(A.row_off, A.B, r);
+        ok = b >= 0 && b < A.B;
+        r0 = ok ? __ldg(A.row_off + b) : 0;
+        const int r1 = ok ? __ldg(A.row_off + b + 1) : 0;
+        ok = ok && r0 <= r && r < r1;
+        nrows = r1 - r0;
+    } else {
+        b = r / (A.k_max + 1);
+        r0 = b * (A.k_max + 1);
+        nrows = A.k_max + 1;
+    }
+    if (lane == 0) {
+        S.r = r;
+        S.r0 = r0;
+        S.nrows = nrows;
+        S.i = r - r0;
+        S.d0 = r0 - b;
+        S.K = 0;
+        S.greedy = 0;
+        S.T = 1.f;
+        S.P = 1.f;
+        if (ok) {
+            load_request(A, S, b);
+        } else {
+            // a row outside every request (inconsistent row_offsets): nothing to count
+            S.b = -1;
+            S.k = 0;
+            S.status = 1;
+            record_error(A, 1, b < 0 ? 0 : (b >= A.B ? A.B - 1 : b));
+        }
+        S.active = ok && S.status == 0 && S.i <= S.k;
+        const bool sampled = !S.greedy;
+        S.s = sampled ? __fdiv_rn(LOG2E, S.T) : 0.f;
+        S.topk_on = sampled && S.K > 0 && S.K < A.V;
+        S.topp_on = sampled && S.P < 1.f;
+        S.need_sum = sampled && !S.topk_on && !S.topp_on;
+        S.mode = !sampled ? MODE_ARG : (S.need_sum ? MODE_SUM : ((S.topk_on && S.K <= KCAP) ? MODE_TOP2 : MODE_MAX));
+        S.xtok = -1;
+        S.zx = 0.f;
+        S.qx = 0.f;
+        S.npen = 0;
+    }
+    __syncwarp();
+}
+
 // Penalties of row i: the distinct drafts d_0..d_{i-1} with pen = presence + frequency * count
-// (FreeToken PR #836, "Design": earlier drafts count as already generated).  Run by warp 0.
-__device__ __forceinline__ void build_penalties(const Args &A, Ctx &S, int i) {
+// (FreeToken PR #836, "Design": earlier drafts count as already generated).  Run by one warp.
+__device__ __forceinline__ void build_penalties(const Args &A, RowCtx &S, int i) {
     const int lane = lane_id();
     if (lane == 0) S.npen = 0;
     __syncwarp();
-    if (i == 0 || (S.pres == 0.f && S.freq == 0.f)) return;
+    if (i <= 0 || (S.pres == 0.f && S.freq == 0.f)) return;
     for (int j = lane; j < i; j += 32) S.draft_raw[j] = __ldg(A.tokens + S.d0 + j);
     __syncwarp();
     for (int base = 0; base < i; base += 32) {
@@ -134,7 +198,7 @@ __device__ __forceinline__ void build_penalties(const Args &A, Ctx &S, int i) {
 
 // Applies the penalties to the 8 values this lane holds for the segment starting at seg_lo
 // (lane owns elements seg_lo + 8*lane .. +7).  Whole warp must call it.
-__device__ __forceinline__ void patch_seg(const Ctx &S, int seg_lo, float v[8]) {
+__device__ __forceinline__ void patch_seg(const RowCtx &S, int seg_lo, float v[8]) {
     const int npen = S.npen;
     if (npen == 0) return;
     const int lane = lane_id();
@@ -160,126 +224,184 @@ __device__ __forceinline__ void patch_seg(const Ctx &S, int seg_lo, float v[8]) 
     }
 }
 
-// Penalised value of a single token x of the row.
-template <typename E>
-__device__ __forceinline__ float elem_z(const Ctx &S, const E *row, int x);
-
-template <>
-__device__ __forceinline__ float elem_z<uint16_t>(const Ctx &S, const uint16_t *row, int x) {
-    float z = __uint_as_float((uint32_t)__ldg(row + x) << 16);
-    for (int h = 0; h < S.npen; h++)
-        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
-    return z;
-}
-template <>
-__device__ __forceinline__ float elem_z<float>(const Ctx &S, const float *row, int x) {
-    float z = __ldg(row + x);
-    for (int h = 0; h < S.npen; h++)
-        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
-    return z;
-}
-
 // Penalised value of token x from its raw stored element.
-__device__ __forceinline__ float elem_z_raw(const Ctx &S, uint16_t raw, int x) {
+__device__ __forceinline__ float elem_z_raw(const RowCtx &S, uint16_t raw, int x) {
     float z = __uint_as_float((uint32_t)raw << 16);
     for (int h = 0; h < S.npen; h++)
         if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
     return z;
 }
-__device__ __forceinline__ float elem_z_raw(const Ctx &S, float raw, int x) {
+__device__ __forceinline__ float elem_z_raw(const RowCtx &S, float raw, int x) {
     float z = raw;
     for (int h = 0; h < S.npen; h++)
         if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
     return z;
 }
 
-// Loads and penalises the 8 values of this lane in segment seg.
+// One thread: the row's draft token and, for a valid one, its penalised target value and q.
+template <typename E>
+__device__ __forceinline__ void prefetch_draft(const Args &A, RowCtx &S, const E *row) {
+    int x = -1;
+    float zx = 0.f, qx = 0.f;
+    if (S.active && S.i < S.k) {
+        x = __ldg(A.tokens + S.d0 + S.i);
+        if (x >= 0 && x < A.V) {
+            const E raw = __ldg(row + x);
+            if (!S.greedy) qx = __ldg(A.q + (size_t)(S.d0 + S.i) * A.V + x);
+            zx = elem_z_raw(S, raw, x);
+        }
+    }
+    S.xtok = x;
+    S.zx = zx;
+    S.qx = qx;
+}
+
+// Loads and penalises the 8 values of this lane in segment seg (global memory).
 template <typename E, bool VEC>
-__device__ __forceinline__ void seg_values(const Ctx &S, const E *row, int V, int seg, float v[8]) {
+__device__ __forceinline__ void seg_values(const RowCtx &S, const E *row, int V, int seg, float v[8]) {
     Raw8<E> raw = load_raw8<VEC>(row, seg * SEG + lane_id() * 8, V);
     unpack8(raw, v);
     patch_seg(S, seg * SEG, v);
 }
 
-// ------------------------------------------------------------------------------------------
-// pass 1: one streaming read of the row -> per-segment max (and weight sum)
-// ------------------------------------------------------------------------------------------
+// Per-segment statistics of a row, written by the streaming pass.
+struct SegStats {
+    float *mx;        // max of the segment
+    float *b;         // MODE_TOP2: second-largest value (ties count); MODE_SUM: sum of 2^((z - mx) s)
+    int *lane;        // MODE_ARG / MODE_TOP2: lowest lane whose 8 elements hold the max
+    uint32_t *hist;   // MODE_TOP2: 256-bin histogram of the top byte of the maxima's order keys
+};
 
+// Reduces one segment, whose raw elements this lane holds 8 at a time (elements
+// seg*SEG + 8*lane + t), to what the row's mode asks for; lane 0 writes it.  Warp-wide maxima
+// are single redux.sync instructions; bf16 rows without penalties work on packed pairs.
+template <typename E>
+__device__ __forceinline__ void seg_stats(const Raw8<E> &raw, int seg, int V, const RowCtx &S, const SegStats &o) {
+    const int lane = lane_id();
+    const int mode = S.mode;
+    float m1, m2 = -INFINITY, sum = 0.f;
+    bool done = false;
+    if constexpr (sizeof(E) == 2) {
+        if (mode != MODE_SUM && S.npen == 0 && seg * SEG + SEG <= V) {
+            const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw.a);
+            const __nv_bfloat162 a = __hmax2(p[0], p[1]), c = __hmax2(p[2], p[3]);
+            const __nv_bfloat162 M = __hmax2(a, c);
+            const float lo = __low2float(M), hi = __high2float(M);
+            m1 = fmaxf(lo, hi);
+            if (mode == MODE_TOP2) {
+                // second largest of the lane's 8: max of the smaller half-max and the halves' seconds
+                const __nv_bfloat162 b = __hmin2(p[0], p[1]), d = __hmin2(p[2], p[3]);
+                const __nv_bfloat162 Sd = __hmax2(__hmin2(a, c), __hmax2(b, d));
+                m2 = fmaxf(fminf(lo, hi), fmaxf(__low2float(Sd), __high2float(Sd)));
+            }
+            done = true;
+        }
+    }
+    float v[8];
+    if (!done) {
+        unpack8(raw, v);
+        const int base = seg * SEG + lane * 8;
+        if (base + 8 > V) {
+#pragma unroll
+            for (int t = 0; t < 8; t++)
+                if (base + t >= V) v[t] = -INFINITY;
+        }
+        patch_seg(S, seg * SEG, v);
+        if (mode == MODE_TOP2) {
+            m1 = v[0];
+#pragma unroll
+            for (int t = 1; t < 8; t++) {
+                m2 = fmaxf(m2, fminf(m1, v[t]));
+                m1 = fmaxf(m1, v[t]);
+            }
+        } else {
+            m1 = max8(v);
+        }
+    }
+    const float mx = redux_max(m1);
+    int at = 0;
+    float sec = 0.f;
+    if (mode == MODE_ARG || mode == MODE_TOP2) {
+        at = __ffs(__ballot_sync(0xffffffffu, m1 == mx)) - 1;
+        if (mode == MODE_TOP2) sec = redux_max(lane == at ? m2 : m1);
+    } else if (mode == MODE_SUM && mx > -INFINITY) {
+        const float ms = __fmul_rn(mx, S.s);
+#pragma unroll
+        for (int t = 0; t < 8; t++) sum += ex2(fmaf(v[t], S.s, -ms));
+        sum = warp_sum(sum);
+    }
+    if (lane == 0) {
+        o.mx[seg] = mx;
+        if (mode == MODE_ARG || mode == MODE_TOP2) o.lane[seg] = at;
+        if (mode == MODE_TOP2) {
+            o.b[seg] = sec;
+            atomicAdd(&o.hist[fkey(mx) >> 24], 1u);
+        }
+        if (mode == MODE_SUM) o.b[seg] = sum;
+    }
+}
+
+// One thread: token id of the first element equal to `target` among the 8 of `lane` in
+// segment seg (penalties applied), or -1.
 template <typename E, bool VEC>
-__device__ __forceinline__ void pass_stats(const Ctx &S, const E *row, int V, int nseg, float *segmax,
-                                           float *segsum, bool need_sum, float s) {
+__device__ __forceinline__ int find_in_lane(const RowCtx &S, const E *row, int V, int seg, int lane, float target) {
+    const int base = seg * SEG + lane * 8;
+    Raw8<E> raw = load_raw8<VEC>(row, base, V);
+    float v[8];
+    unpack8(raw, v);
+    for (int h = 0; h < S.npen; h++) {
+        const int d = S.pid[h] - base;
+#pragma unroll
+        for (int t = 0; t < 8; t++)
+            if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
+    }
+    int pos = -1;
+#pragma unroll
+    for (int t = 7; t >= 0; t--)
+        if (v[t] == target && base + t < V) pos = base + t;
+    return pos;
+}
+
+// One streaming read of the row by the group's warps with global loads (any alignment).
+template <typename E, bool VEC, class G>
+__device__ __forceinline__ void pass_stats(const G &g, const RowCtx &S, const E *row, int V, int nseg,
+                                           const SegStats &o) {
     constexpr int U = sizeof(E) == 2 ? 4 : 2;   // segments in flight per warp
-    const int warp = warp_id(), lane = lane_id();
-    for (int s0 = warp; s0 < nseg; s0 += NWARP * U) {
+    const int warp = g.warp(), lane = g.lane();
+    for (int s0 = warp; s0 < nseg; s0 += G::kWarps * U) {
         Raw8<E> raw[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            int seg = s0 + u * NWARP;
+            int seg = s0 + u * G::kWarps;
             if (seg < nseg) raw[u] = load_raw8<VEC>(row, seg * SEG + lane * 8, V);
         }
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            int seg = s0 + u * NWARP;
-            if (seg < nseg) {
-                float v[8];
-                unpack8(raw[u], v);
-                patch_seg(S, seg * SEG, v);
-                float mx = warp_max(max8(v));
-                float sum = 0.f;
-                if (need_sum && mx > -INFINITY) {
-                    float ms = __fmul_rn(mx, s);
-#pragma unroll
-                    for (int j = 0; j < 8; j++) sum += ex2(fmaf(v[j], s, -ms));
-                    sum = warp_sum(sum);
-                }
-                if (lane == 0) {
-                    segmax[seg] = mx;
-                    segsum[seg] = sum;
-                }
-            }
+            int seg = s0 + u * G::kWarps;
+            if (seg < nseg) seg_stats<E>(raw[u], seg, V, S, o);
         }
     }
 }
 
-// ------------------------------------------------------------------------------------------
-// pass 1 through a shared-memory ring fed by bulk copies (16-byte aligned rows)
-// ------------------------------------------------------------------------------------------
-
-__device__ __forceinline__ int ring_chunks(int V, int esize) {
-    const uint32_t RB = (uint32_t)V * esize;
-    return (int)((RB + SB - 1) / SB);
+// Raw elements of segment j of a ring stage for this lane (16-byte aligned rows).
+template <typename E>
+__device__ __forceinline__ Raw8<E> ring_raw(const unsigned char *buf, int j);
+template <>
+__device__ __forceinline__ Raw8<uint16_t> ring_raw<uint16_t>(const unsigned char *buf, int j) {
+    Raw8<uint16_t> r;
+    r.a = *reinterpret_cast<const uint4 *>(buf + j * SEG * 2 + lane_id() * 16);
+    return r;
+}
+template <>
+__device__ __forceinline__ Raw8<float> ring_raw<float>(const unsigned char *buf, int j) {
+    Raw8<float> r;
+    const uint4 *p = reinterpret_cast<const uint4 *>(buf + j * SEG * 4 + lane_id() * 32);
+    r.a = p[0];
+    r.b = p[1];
+    return r;
 }
 
-// Thread 0: copy chunk c (SB bytes, the last one shorter) of the row into its ring stage.
-__device__ __forceinline__ void ring_issue(Ctx &S, unsigned char *ring, const void *row, uint32_t RB, int c) {
-    const int st = c % NS;
-    const uint32_t off = (uint32_t)c * SB;
-    const uint32_t bytes = min((uint32_t)SB, RB - off);
-    mbar_expect_tx(&S.full[st], bytes);
-    bulk_g2s(ring + st * SB, reinterpret_cast<const unsigned char *>(row) + off, bytes, &S.full[st]);
-    S.issued = c + 1;
-}
-
-// Thread 0: set up the ring barriers and start the first NS chunks of the row.
-__device__ __forceinline__ void ring_start(Ctx &S, unsigned char *ring, const void *row, int V, int esize) {
-    for (int s = 0; s < NS; s++) {
-        mbar_init(&S.full[s], 1);
-        mbar_init(&S.empty[s], NWARP);
-    }
-    mbar_fence_init();
-    S.issued = 0;
-    S.ring_fail = 0;
-    const uint32_t RB = (uint32_t)V * esize;
-    const int nc = ring_chunks(V, esize);
-    for (int c = 0; c < NS && c < nc; c++) ring_issue(S, ring, row, RB, c);
-}
-
-// Thread 0: wait (bounded) for the latest chunk of every stage, so that no copy into shared
-// memory is still in flight when the CTA moves on or exits.
-__device__ __forceinline__ void ring_drain(Ctx &S) {
-    for (int c = max(0, S.issued - NS); c < S.issued; c++) mbar_wait(&S.full[c % NS], (uint32_t)(c / NS) & 1u);
-}
-
+// Values of segment j of a ring stage (16-byte aligned rows: 8 elements per lane).
 template <typename E>
 __device__ __forceinline__ void ring_values(const unsigned char *buf, int j, float v[8]);
 template <>
@@ -297,66 +419,8 @@ __device__ __forceinline__ void ring_values<float>(const unsigned char *buf, int
     unpack8(r, v);
 }
 
-// Pass 1 over the ring: per-segment max (and weight sums), same results as pass_stats.
-// Thread 0 refills a stage once all warps released it.  Returns false if a bounded wait
-// expired (the caller fails the row).
-template <typename E>
-__device__ bool pass_stats_ring(Ctx &S, unsigned char *ring, const E *row, int V, int nseg, float *segmax,
-                                float *segsum, bool need_sum, float s) {
-    const int warp = warp_id(), lane = lane_id();
-    const uint32_t RB = (uint32_t)V * sizeof(E);
-    const int nc = ring_chunks(V, (int)sizeof(E));
-    constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
-    int c = 0;
-    for (; c < nc; c++) {
-        const int st = c % NS;
-        const uint32_t par = (uint32_t)(c / NS) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&S.full[st], par))) break;
-        const unsigned char *buf = ring + st * SB;
-        for (int j = warp; j < SPC; j += NWARP) {
-            const int seg = c * SPC + j;
-            if (seg >= nseg) break;
-            float v[8];
-            ring_values<E>(buf, j, v);
-            const int base = seg * SEG + lane * 8;
-            if (base + 8 > V) {
-#pragma unroll
-                for (int t = 0; t < 8; t++)
-                    if (base + t >= V) v[t] = -INFINITY;
-            }
-            patch_seg(S, seg * SEG, v);
-            const float mx = warp_max(max8(v));
-            float sum = 0.f;
-            if (need_sum && mx > -INFINITY) {
-                const float ms = __fmul_rn(mx, s);
-#pragma unroll
-                for (int t = 0; t < 8; t++) sum += ex2(fmaf(v[t], s, -ms));
-                sum = warp_sum(sum);
-            }
-            if (lane == 0) {
-                segmax[seg] = mx;
-                segsum[seg] = sum;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[st]);
-        if (threadIdx.x == 0 && c + NS < nc) {
-            if (mbar_wait(&S.empty[st], par)) ring_issue(S, ring, row, RB, c + NS);
-            else S.ring_fail = 1;
-        }
-    }
-    if (c < nc) atomicOr(&S.ring_fail, 1);
-    __syncthreads();
-    if (S.ring_fail) {
-        if (threadIdx.x == 0) ring_drain(S);
-        __syncthreads();
-        return false;
-    }
-    return true;
-}
-
 // ------------------------------------------------------------------------------------------
-// selection helpers (radix select with 11/11/10-bit digits, MSB first)
+// selection helpers (radix select, MSB first)
 // ------------------------------------------------------------------------------------------
 
 __device__ __forceinline__ void digit_round(int round, int &shift, int &width, uint32_t &mask) {
@@ -365,11 +429,10 @@ __device__ __forceinline__ void digit_round(int round, int &shift, int &width, u
     mask = round == 0 ? 0u : (round == 1 ? 0xFFE00000u : 0xFFFFFC00u);
 }
 
-// Warp 0 scans a count histogram from the highest bin down and finds the bin d holding the
+// One warp scans a count histogram from the highest bin down and finds the bin d holding the
 // need-th largest element (cum_above(d) < need <= cum_above(d) + cnt[d]).  Writes S.sel_digit
-// and S.sel_below (= cum_above(d)).  need >= 1.
-__device__ __forceinline__ void find_count_bin(Ctx &S, const uint32_t *cnt, int nbins, long long need) {
-    if (warp_id() != 0) return;
+// and S.sel_below (= cum_above(d)).  need >= 1; nbins a multiple of 32.
+__device__ __forceinline__ void find_count_bin(RowCtx &S, const uint32_t *cnt, int nbins, long long need) {
     const int lane = lane_id();
     const int per = nbins / 32;
     const int top = nbins - lane * per;   // this lane covers bins [top - per, top)
@@ -400,108 +463,53 @@ __device__ __forceinline__ void find_count_bin(Ctx &S, const uint32_t *cnt, int 
     }
 }
 
-// Warp 0 finds, in a 256-bin count histogram scanned from the top, the bin holding the
-// need-th largest element; 8 bins per lane.  Writes S.sel_digit and S.sel_below.
-__device__ __forceinline__ void find_count_bin256(Ctx &S, const uint32_t *cnt, long long need) {
-    if (warp_id() != 0) return;
-    const int lane = lane_id();
-    const int top = 256 - lane * 8;
-    uint32_t c8[8];
-    long long tot = 0;
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-        c8[j] = cnt[top - 1 - j];
-        tot += c8[j];
-    }
-    long long incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    long long excl = incl - tot;
-    unsigned msk = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-    int owner = msk ? __ffs(msk) - 1 : 31;
-    if (lane == owner) {
-        long long c = excl;
-        int dsel = top - 8;
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            if (c + (long long)c8[j] >= need) {
-                dsel = top - 1 - j;
-                break;
-            }
-            c += c8[j];
-        }
-        S.sel_digit = dsel;
-        S.sel_below = c;
-    }
-}
-
 // A lower bound on the need-th largest of n float keys in shared memory: the top 16 bits of
 // that key (two 8-bit radix rounds) with the low 16 bits cleared.  At least `need` keys are
-// >= the bound, and every key above it shares the bound's 16-bit prefix or exceeds it.
-__device__ uint32_t select_bound16(Ctx &S, const float *vals, int n, int need, uint32_t *cnt) {
+// >= the bound.
+// hist1, when given, already holds the first round's histogram of the top byte.
+template <class G>
+__device__ uint32_t select_bound16(const G &g, RowCtx &S, const float *vals, int n, int need, uint32_t *cnt,
+                                   const uint32_t *hist1 = nullptr) {
     uint32_t prefix = 0;
     long long nd = need;
     for (int round = 0; round < 2; round++) {
         const int shift = 24 - 8 * round;
         const uint32_t mask = round == 0 ? 0u : 0xFF000000u;
-        for (int d = threadIdx.x; d < 256; d += NT) cnt[d] = 0;
-        __syncthreads();
-        for (int j = threadIdx.x; j < n; j += NT) {
-            uint32_t key = fkey(vals[j]);
-            if ((key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & 255u], 1u);
+        const uint32_t *h = cnt;
+        if (round == 0 && hist1) {
+            h = hist1;
+        } else {
+            for (int d = g.t; d < 256; d += G::kThreads) cnt[d] = 0;
+            g.sync();
+            for (int j = g.t; j < n; j += G::kThreads) {
+                uint32_t key = fkey(vals[j]);
+                if ((key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & 255u], 1u);
+            }
+            g.sync();
         }
-        __syncthreads();
-        find_count_bin256(S, cnt, nd);
-        __syncthreads();
+        if (g.warp() == 0) find_count_bin(S, h, 256, nd);
+        g.sync();
         prefix |= (uint32_t)S.sel_digit << shift;
         nd -= S.sel_below;
-        __syncthreads();
+        g.sync();
     }
     return prefix;
 }
 
-// The need-th largest (1-based) of n float keys fkey(vals[j]) held in shared memory.
-__device__ uint32_t select_kth_smem(Ctx &S, const float *vals, int n, int need, uint32_t *cnt) {
+// The need-th largest key among the row's tokens (full passes over the row from global).
+template <typename E, bool VEC, class G>
+__device__ uint32_t select_kth_row(const G &g, RowCtx &S, const E *row, int V, int nseg, int need, uint32_t *cnt) {
     uint32_t prefix = 0;
     long long nd = need;
+    const int warp = g.warp(), lane = g.lane();
     for (int round = 0; round < 3; round++) {
         int shift, width;
         uint32_t mask;
         digit_round(round, shift, width, mask);
         const int nb = 1 << width;
-        for (int d = threadIdx.x; d < nb; d += NT) cnt[d] = 0;
-        __syncthreads();
-        for (int j = threadIdx.x; j < n; j += NT) {
-            uint32_t key = fkey(vals[j]);
-            if ((key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & (nb - 1)], 1u);
-        }
-        __syncthreads();
-        find_count_bin(S, cnt, nb, nd);
-        __syncthreads();
-        prefix |= (uint32_t)S.sel_digit << shift;
-        nd -= S.sel_below;
-        __syncthreads();
-    }
-    return prefix;
-}
-
-// The need-th largest key among the row's tokens (full passes over the row, re-read from L2).
-template <typename E, bool VEC>
-__device__ uint32_t select_kth_row(Ctx &S, const E *row, int V, int nseg, int need, uint32_t *cnt) {
-    uint32_t prefix = 0;
-    long long nd = need;
-    const int warp = warp_id(), lane = lane_id();
-    for (int round = 0; round < 3; round++) {
-        int shift, width;
-        uint32_t mask;
-        digit_round(round, shift, width, mask);
-        const int nb = 1 << width;
-        for (int d = threadIdx.x; d < nb; d += NT) cnt[d] = 0;
-        __syncthreads();
-        for (int seg = warp; seg < nseg; seg += NWARP) {
+        for (int d = g.t; d < nb; d += G::kThreads) cnt[d] = 0;
+        g.sync();
+        for (int seg = warp; seg < nseg; seg += G::kWarps) {
             float v[8];
             seg_values<E, VEC>(S, row, V, seg, v);
 #pragma unroll
@@ -511,21 +519,20 @@ __device__ uint32_t select_kth_row(Ctx &S, const E *row, int V, int nseg, int ne
                 if (idx < V && (key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & (nb - 1)], 1u);
             }
         }
-        __syncthreads();
-        find_count_bin(S, cnt, nb, nd);
-        __syncthreads();
+        g.sync();
+        if (warp == 0) find_count_bin(S, cnt, nb, nd);
+        g.sync();
         prefix |= (uint32_t)S.sel_digit << shift;
         nd -= S.sel_below;
-        __syncthreads();
+        g.sync();
     }
     return prefix;
 }
 
-// Warp 0 scans a fixed-point mass histogram from the top and finds the first bin d where the
-// mass above plus the bin's own mass reaches target (mass_above(d) < target <= ... + mass[d]).
-__device__ __forceinline__ void find_mass_bin(Ctx &S, const unsigned long long *mass, int nbins,
+// One warp scans a fixed-point mass histogram from the top and finds the first bin d where
+// the mass above plus the bin's own mass reaches target (above(d) < target <= ... + mass[d]).
+__device__ __forceinline__ void find_mass_bin(RowCtx &S, const unsigned long long *mass, int nbins,
                                               unsigned long long above, double target) {
-    if (warp_id() != 0) return;
     const int lane = lane_id();
     const int per = nbins / 32;
     const int top = nbins - lane * per;
@@ -559,21 +566,21 @@ __device__ __forceinline__ void find_mass_bin(Ctx &S, const unsigned long long *
 // Top-p threshold over the tokens with key >= key_lo: the lowest key level L whose mass
 // strictly above is < P * (total mass of those tokens).  Fixed-point (2^-40) weights make the
 // histogram sums exact and order-independent.
-template <typename E, bool VEC>
-__device__ uint32_t select_mass_row(Ctx &S, const E *row, int V, int nseg, uint32_t key_lo, float m, float s,
-                                    float P, unsigned long long *mass) {
+template <typename E, bool VEC, class G>
+__device__ uint32_t select_mass_row(const G &g, RowCtx &S, const E *row, int V, int nseg, uint32_t key_lo,
+                                    float m, float s, float P, unsigned long long *mass) {
     uint32_t prefix = 0;
     unsigned long long above = 0;
     double target = 0.0;
-    const int warp = warp_id(), lane = lane_id();
+    const int warp = g.warp(), lane = g.lane();
     for (int round = 0; round < 3; round++) {
         int shift, width;
         uint32_t mask;
         digit_round(round, shift, width, mask);
         const int nb = 1 << width;
-        for (int d = threadIdx.x; d < nb; d += NT) mass[d] = 0ull;
-        __syncthreads();
-        for (int seg = warp; seg < nseg; seg += NWARP) {
+        for (int d = g.t; d < nb; d += G::kThreads) mass[d] = 0ull;
+        g.sync();
+        for (int seg = warp; seg < nseg; seg += G::kWarps) {
             float v[8];
             seg_values<E, VEC>(S, row, V, seg, v);
 #pragma unroll
@@ -586,9 +593,9 @@ __device__ uint32_t select_mass_row(Ctx &S, const E *row, int V, int nseg, uint3
                 }
             }
         }
-        __syncthreads();
+        g.sync();
         if (round == 0) {
-            // total mass of the top-k set (every bin of round 0), summed by warp 0
+            // total mass of the top-k set (every bin of round 0), summed by one warp
             if (warp == 0) {
                 unsigned long long t = 0;
                 for (int d = lane; d < nb; d += 32) t += mass[d];
@@ -596,14 +603,14 @@ __device__ uint32_t select_mass_row(Ctx &S, const E *row, int V, int nseg, uint3
                 for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
                 if (lane == 0) S.sel_target = (double)P * (double)t;
             }
-            __syncthreads();
+            g.sync();
             target = S.sel_target;
         }
-        find_mass_bin(S, mass, nb, above, target);
-        __syncthreads();
+        if (warp == 0) find_mass_bin(S, mass, nb, above, target);
+        g.sync();
         prefix |= (uint32_t)S.sel_digit << shift;
         above = S.sel_mass;
-        __syncthreads();
+        g.sync();
     }
     return prefix;
 }
@@ -615,23 +622,24 @@ __device__ uint32_t select_mass_row(Ctx &S, const E *row, int V, int nseg, uint3
 // Index j of the draw from weights w[0..n) in shared memory with uniform u: the first j whose
 // running sum exceeds u * W (W = total); the last positive-weight j if rounding leaves none;
 // -1 when no weight is positive.  `pre` (n floats) receives the prefix sums.
-__device__ int draw_small(const float *w, float *pre, int n, float u, Ctx &S) {
-    for (int j = threadIdx.x; j < n; j += NT) pre[j] = w[j];
-    __syncthreads();
+template <class G>
+__device__ int draw_small(const G &g, const float *w, float *pre, int n, float u, RowCtx &S) {
+    for (int j = g.t; j < n; j += G::kThreads) pre[j] = w[j];
+    g.sync();
     if (n <= 0) return -1;
-    block_scan_incl(pre, n, S.redf);
+    g_scan_incl(g, pre, n, S.redf);
     float W = pre[n - 1];
     if (!(W > 0.f)) return -1;
     float target = __fmul_rn(u, W);
     int best = 0x7fffffff;
-    for (int j = threadIdx.x; j < n; j += NT)
+    for (int j = g.t; j < n; j += G::kThreads)
         if (pre[j] > target) best = min(best, j);
-    best = block_min_i(best, S.redi);
+    best = g_min_i(g, best, S.redi);
     if (best == 0x7fffffff) {
         int last = -1;
-        for (int j = threadIdx.x; j < n; j += NT)
+        for (int j = g.t; j < n; j += G::kThreads)
             if (w[j] > 0.f) last = max(last, j);
-        best = block_max_i(last, S.redi);
+        best = g_max_i(g, last, S.redi);
     }
     return best;
 }
@@ -661,32 +669,32 @@ struct WResid {      // max(0, p_v - q_v)
 };
 
 // Draw from a whole row with per-segment weight sums segw[0..nseg) (overwritten by their
-// prefix sums).  The crossing segment is re-read by warp 0 and scanned lane by lane.
-// Returns the token, or -1 when no weight is positive.
-template <typename E, bool VEC, bool QVEC, typename WF>
-__device__ int draw_by_segments(Ctx &S, const E *row, const float *qrow, int V, int nseg, float *segw,
-                                float u, const WF &wf) {
-    block_scan_incl(segw, nseg, S.redf);
+// prefix sums).  The crossing segment is re-read by the group's first warp and scanned lane
+// by lane.  Returns the token, or -1 when no weight is positive.
+template <typename E, bool VEC, bool QVEC, typename WF, class G>
+__device__ int draw_by_segments(const G &g, RowCtx &S, const E *row, const float *qrow, int V, int nseg,
+                                float *segw, float u, const WF &wf) {
+    g_scan_incl(g, segw, nseg, S.redf);
     const float W = segw[nseg - 1];
     if (!(W > 0.f)) return -1;
     const float target = __fmul_rn(u, W);
     int best = 0x7fffffff;
-    for (int j = threadIdx.x; j < nseg; j += NT)
+    for (int j = g.t; j < nseg; j += G::kThreads)
         if (segw[j] > target) best = min(best, j);
-    best = block_min_i(best, S.redi);
+    best = g_min_i(g, best, S.redi);
     bool fallback = false;
     if (best == 0x7fffffff) {
         int last = -1;
-        for (int j = threadIdx.x; j < nseg; j += NT) {
+        for (int j = g.t; j < nseg; j += G::kThreads) {
             float prev = j ? segw[j - 1] : 0.f;
             if (segw[j] > prev) last = max(last, j);
         }
-        best = block_max_i(last, S.redi);
+        best = g_max_i(g, last, S.redi);
         fallback = true;
         if (best < 0) return -1;
     }
-    if (warp_id() == 0) {
-        const int lane = lane_id();
+    if (g.warp() == 0) {
+        const int lane = g.lane();
         const int seg = best;
         float v[8], qv[8];
         seg_values<E, VEC>(S, row, V, seg, v);
@@ -725,16 +733,16 @@ __device__ int draw_by_segments(Ctx &S, const E *row, const float *qrow, int V, 
         lastpos = warp_max_i(lastpos);
         if (lane == 0) S.tok = pick != 0x7fffffff ? pick : lastpos;
     }
-    __syncthreads();
+    g.sync();
     return S.tok;
 }
 
-// Per-segment sums of a weight functor over the whole row (one pass; q row optional).
-template <typename E, bool VEC, bool QVEC, typename WF, typename WF2>
-__device__ __forceinline__ void seg_sums(Ctx &S, const E *row, const float *qrow, int V, int nseg, float *out1,
-                                         const WF &wf1, float *out2, const WF2 &wf2) {
-    const int warp = warp_id(), lane = lane_id();
-    for (int seg = warp; seg < nseg; seg += NWARP) {
+// Per-segment sums of weight functors over the whole row (one pass; q row optional).
+template <typename E, bool VEC, bool QVEC, typename WF, typename WF2, class G>
+__device__ __forceinline__ void seg_sums(const G &g, const RowCtx &S, const E *row, const float *qrow, int V,
+                                         int nseg, float *out1, const WF &wf1, float *out2, const WF2 &wf2) {
+    const int warp = g.warp(), lane = g.lane();
+    for (int seg = warp; seg < nseg; seg += G::kWarps) {
         float v[8], qv[8];
         seg_values<E, VEC>(S, row, V, seg, v);
         if (qrow) {
@@ -759,7 +767,7 @@ __device__ __forceinline__ void seg_sums(Ctx &S, const E *row, const float *qrow
             if (out2) out2[seg] = c;
         }
     }
-    __syncthreads();
+    g.sync();
 }
 
 }  // namespace sv

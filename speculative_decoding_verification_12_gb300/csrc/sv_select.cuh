@@ -1,0 +1,647 @@
+// sv_select.cuh -- what happens to a row once its per-segment statistics exist: the kept set
+// (top-k / top-p), the draws, p(x_i) and q(x_i) of the row's draft, and -- once every row of a
+// request is done -- the request's first-rejection scan and final token.
+//
+// "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust":
+//  - "The Memory Bandwidth Wall and Speculative Math": accept x_i with probability
+//    min(1, p(x_i)/q(x_i)); at the first rejection draw from max(0, p - q) normalised.
+//  - "The Verification Algorithm": stop at the first rejection; with every draft accepted the
+//    extra token comes from row K.
+// "Adding Speculative Decoding", table "The existing base": greedy accepts while the draft is
+// the argmax; the token at the first mismatch is that row's argmax.
+//
+// Everything here is templated on the thread group G that runs it.
+#pragma once
+
+#include "sv_row.cuh"
+
+namespace sv {
+
+// Shared-memory scratch of the group that selects rows and finalises requests.
+struct Scratch {
+    float *segX, *segY;           // per-segment scratch (segment lists, residual sums)
+    unsigned long long *cand;     // CAP candidate keys (order key << 32) | ~token
+    float *aux, *aux2;            // CAP floats each
+    unsigned long long *sorted;   // WCAP keys (aliases aux/aux2)
+    uint32_t *hcnt;               // radix histogram (aliases aux)
+    unsigned long long *hmass;    // fixed-point mass histogram (aliases cand)
+};
+
+// Carves a Scratch out of `p`: segX/segY (nsegp floats each) then 32 KB of candidate area.
+__device__ __forceinline__ Scratch carve_scratch(unsigned char *p, int nsegp) {
+    Scratch c;
+    c.segX = reinterpret_cast<float *>(p);
+    c.segY = c.segX + nsegp;
+    unsigned char *area = reinterpret_cast<unsigned char *>(c.segY + nsegp);
+    c.cand = reinterpret_cast<unsigned long long *>(area);
+    c.aux = reinterpret_cast<float *>(area + size_t(CAP) * 8);
+    c.aux2 = c.aux + CAP;
+    c.sorted = reinterpret_cast<unsigned long long *>(c.aux);
+    c.hmass = reinterpret_cast<unsigned long long *>(area);
+    c.hcnt = reinterpret_cast<uint32_t *>(area + size_t(HB) * 8);
+    return c;
+}
+__host__ __device__ inline size_t scratch_bytes(int nsegp) { return size_t(2) * nsegp * 4 + size_t(CAP) * 16; }
+__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
+
+#ifdef SV_TIMING
+#define SV_MARK(A, r, j)                                                           \
+    do {                                                                           \
+        if (threadIdx.x % 32 == 0) (A).timing[(size_t)(r) * NTIME + (j)] = global_ns(); \
+    } while (0)
+#else
+#define SV_MARK(A, r, j) \
+    do {                 \
+    } while (0)
+#endif
+
+// Appends this lane's tokens of segment seg whose key reaches tkey to the candidate buffer
+// (warp-aggregated; entries beyond CAP are counted but not stored).
+__device__ __forceinline__ void append_candidates(RowCtx &S, unsigned long long *cand, int seg, const float v[8],
+                                                  uint32_t tkey, int V) {
+    const int lane = lane_id();
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        int idx = seg * SEG + lane * 8 + j;
+        c += (idx < V && fkey(v[j]) >= tkey) ? 1 : 0;
+    }
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if (lane == 0 && total) base = atomicAdd(&S.ncand, total);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    int pos = base + incl - c;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        int idx = seg * SEG + lane * 8 + j;
+        uint32_t key = fkey(v[j]);
+        if (idx < V && key >= tkey) {
+            if (pos < CAP) cand[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)idx);
+            pos++;
+        }
+    }
+}
+
+// One warp: top-k cut, top-p cut and kept mass over n <= WCAP candidates sorted by value
+// (descending), 8 per lane.  Writes S.n2 (kept count), S.zk (kept mass), S.cutkey.
+__device__ __forceinline__ void warp_cut(RowCtx &S, const unsigned long long *srt, int n, int K, float m, float s,
+                                         bool topp, float P) {
+    const int lane = lane_id(), base = lane * 8;
+    const int kk = min(K, n);
+    const uint32_t kkey = (uint32_t)(srt[kk - 1] >> 32);
+    uint32_t key[8];
+    int c1 = 0;
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const int idx = base + t;
+        key[t] = idx < n ? (uint32_t)(srt[idx] >> 32) : 0u;
+        c1 += (idx < n && key[t] >= kkey) ? 1 : 0;
+    }
+    const int n1 = warp_sum_i(c1);
+    float pre[8], loc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        loc += (base + t < n1) ? weight(key2f(key[t]), m, s) : 0.f;
+        pre[t] = loc;
+    }
+    float Z1;
+    const float ex = warp_excl_scan(loc, Z1);
+#pragma unroll
+    for (int t = 0; t < 8; t++) pre[t] += ex;
+    int n2 = n1;
+    if (topp) {
+        // a value level is cut when the mass strictly above it reaches P * Z1
+        const float PZ = __fmul_rn(P, Z1);
+        int cut = 0x7fffffff;
+        uint32_t prevkey = base > 0 ? (uint32_t)(srt[base - 1] >> 32) : 0u;
+        float prevpre = ex;
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const int idx = base + t;
+            if (idx > 0 && idx < n1 && key[t] != prevkey && prevpre >= PZ) cut = min(cut, idx);
+            prevkey = key[t];
+            prevpre = pre[t];
+        }
+        cut = warp_min_i(cut);
+        if (cut != 0x7fffffff) n2 = cut;
+    }
+    float zsel = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; t++)
+        if (base + t == n2 - 1) zsel = pre[t];
+    const float Z = __shfl_sync(0xffffffffu, zsel, (n2 - 1) >> 3);
+    if (lane == 0) {
+        S.n2 = n2;
+        S.zk = Z;
+        S.cutkey = (uint32_t)(srt[n2 - 1] >> 32);
+    }
+}
+
+// One warp: the residual draw of a LIST row should its draft be rejected -- r = max(0, p - q)
+// over the kept list (p is zero elsewhere, so r is too), q gathered from the draft row; an
+// empty residual falls back to p.  ltok/lw: the list in token order (n <= WCAP).
+__device__ __forceinline__ int warp_list_residual(const int *ltok, const float *lw, int n, float invZ,
+                                                  const float *qrow, float u) {
+    const int lane = lane_id();
+    float pw[8], rw[8];
+    int tk[8];
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const int idx = lane * 8 + t;
+        tk[t] = idx < n ? ltok[idx] : -1;
+        pw[t] = idx < n ? __fmul_rn(lw[idx], invZ) : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const float q = tk[t] >= 0 ? __ldg(qrow + tk[t]) : 0.f;
+        rw[t] = tk[t] >= 0 ? fmaxf(__fsub_rn(pw[t], q), 0.f) : 0.f;
+    }
+    int j = warp_draw8(rw, n, u);
+    if (j < 0) j = warp_draw8(pw, n, u);
+    return j >= 0 ? ltok[j] : -1;
+}
+
+// Kept set of a sampled row from the top-k candidates.  Returns false on candidate overflow.
+template <typename E, bool VEC, class G>
+__device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const Scratch &X, const E *row,
+                                     const SegStats &o, RowStat &st, bool want_bonus) {
+    const int warp = g.warp(), lane = g.lane();
+    const int V = A.V, nseg = A.nseg, K = S.K, row_idx = S.r;
+    const float m = S.m, s = S.s;
+    const float *segA = o.mx;
+    // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
+    SV_MARK(A, row_idx, 16);
+    uint32_t tkey = 0;
+    if (nseg >= K) tkey = select_bound16(g, S, segA, nseg, K, X.hcnt, o.hist);
+    SV_MARK(A, row_idx, 17);
+    // Segments whose max reaches the bound.  When a segment's second value is below it, its
+    // max is its only candidate: the lane holding it is known, so one 16-byte load finds the
+    // token.  Segments with two or more candidates are re-read whole.
+    int *segl = reinterpret_cast<int *>(X.segX);
+    int *single = reinterpret_cast<int *>(X.segY);
+    if (g.t == 0) {
+        S.nsel = 0;
+        S.ncand = 0;
+        S.n2 = 0;
+    }
+    g.sync();
+    for (int j = g.t; j < nseg; j += G::kThreads) {
+        if (fkey(segA[j]) < tkey) continue;
+        if (fkey(o.b[j]) < tkey) single[atomicAdd(&S.n2, 1)] = j;
+        else segl[atomicAdd(&S.nsel, 1)] = j;
+    }
+    g.sync();
+    const int nsingle = S.n2;
+    for (int jj = g.t; jj < nsingle; jj += G::kThreads) {
+        const int j = single[jj];
+        const int tok = find_in_lane<E, VEC>(S, row, V, j, o.lane[j], segA[j]);
+        if (tok >= 0) {
+            const int pos = atomicAdd(&S.ncand, 1);
+            if (pos < CAP) X.cand[pos] = ((unsigned long long)fkey(segA[j]) << 32) | (uint32_t)(~(uint32_t)tok);
+        } else {
+            segl[atomicAdd(&S.nsel, 1)] = j;
+        }
+    }
+    g.sync();
+    const int nsel = S.nsel;
+    SV_MARK(A, row_idx, 18);
+    constexpr int U = sizeof(E) == 2 ? 8 : 4;
+    for (int j0 = warp; j0 < nsel; j0 += G::kWarps * U) {
+        Raw8<E> raw[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int j = j0 + u * G::kWarps;
+            if (j < nsel) raw[u] = load_raw8<VEC>(row, segl[j] * SEG + lane * 8, V);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int j = j0 + u * G::kWarps;
+            if (j < nsel) {
+                const int seg = segl[j];
+                float v[8];
+                unpack8(raw[u], v);
+                patch_seg(S, seg * SEG, v);
+                append_candidates(S, X.cand, seg, v, tkey, V);
+            }
+        }
+    }
+    g.sync();
+    const int n = S.ncand;
+    SV_MARK(A, row_idx, 19);
+    if (n > CAP || n < 1) return false;
+
+    if (n <= WCAP) {
+        // rank sort by (value desc, token asc): keys are distinct, so ranks are a permutation
+        unsigned long long *srt = X.sorted;
+        for (int j = g.t; j < n; j += G::kThreads) {
+            const unsigned long long c = X.cand[j];
+            int rk = 0;
+            for (int i = 0; i < n; i++) rk += X.cand[i] > c ? 1 : 0;
+            srt[rk] = c;
+        }
+        g.sync();
+        SV_MARK(A, row_idx, 20);
+        if (warp == 0) warp_cut(S, srt, n, K, m, s, S.topp_on, S.P);
+        g.sync();
+        SV_MARK(A, row_idx, 21);
+        const int n2 = S.n2;
+        const float Z = S.zk;
+        st.Z = Z;
+        st.invZ = __frcp_rn(Z);
+        st.taukey = S.cutkey;
+        st.tau = key2f(S.cutkey);
+        st.kind = KIND_LIST;
+        st.nlist = n2;
+        // the kept set in token order (rank by token id), stored for the residual draw
+        int *ltok = reinterpret_cast<int *>(X.cand);
+        float *lw = reinterpret_cast<float *>(X.cand) + WCAP;
+        for (int j = g.t; j < n2; j += G::kThreads) {
+            const uint32_t tj = ~(uint32_t)srt[j];
+            int rk = 0;
+            for (int i = 0; i < n2; i++) rk += (~(uint32_t)srt[i]) < tj ? 1 : 0;
+            ltok[rk] = (int)tj;
+            lw[rk] = weight(key2f((uint32_t)(srt[j] >> 32)), m, s);
+        }
+        g.sync();
+        int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
+        for (int j = g.t; j < n2; j += G::kThreads) L[j] = make_int2(ltok[j], __float_as_int(lw[j]));
+        SV_MARK(A, row_idx, 22);
+        // warp 0: the extra-token draw (last row); warp 1 (or 0): the residual draw should the
+        // row's draft be rejected, with q gathered on the kept list
+        const bool want_resid = S.i < S.k;
+        const int wres = G::kWarps > 1 ? 1 : 0;
+        if (want_bonus && warp == 0) {
+            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            float w8[8];
+#pragma unroll
+            for (int t = 0; t < 8; t++) w8[t] = (lane * 8 + t < n2) ? lw[lane * 8 + t] : 0.f;
+            const int j = warp_draw8(w8, n2, u);
+            if (lane == 0) S.tok = j >= 0 ? ltok[j] : -1;
+        }
+        if (want_resid && warp == wres) {
+            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
+            const int t = warp_list_residual(ltok, lw, n2, st.invZ, qrow, u);
+            if (lane == 0) S.a = t;
+        }
+        g.sync();
+        if (want_bonus) st.bonus = S.tok;
+        if (want_resid) st.resid = S.a;
+        SV_MARK(A, row_idx, 23);
+        return true;
+    }
+
+    // larger candidate sets: group-wide bitonic sort and scans
+    const int np = pow2_at_least(n);
+    for (int j = n + g.t; j < np; j += G::kThreads) X.cand[j] = 0ull;
+    g.sync();
+    g_sort_desc(g, X.cand, np);
+    const int kk = min(K, n);
+    const uint32_t kkey = (uint32_t)(X.cand[kk - 1] >> 32);
+    int c1 = 0;
+    for (int j = g.t; j < n; j += G::kThreads) c1 += ((uint32_t)(X.cand[j] >> 32) >= kkey) ? 1 : 0;
+    const int n1 = g_sum_i(g, c1, S.redi);
+    for (int j = g.t; j < n1; j += G::kThreads) X.aux[j] = weight(key2f((uint32_t)(X.cand[j] >> 32)), m, s);
+    g.sync();
+    for (int j = g.t; j < n1; j += G::kThreads) X.aux2[j] = X.aux[j];
+    g.sync();
+    g_scan_incl(g, X.aux2, n1, S.redf);
+    int n2 = n1;
+    if (S.topp_on) {
+        const float PZ = __fmul_rn(S.P, X.aux2[n1 - 1]);
+        int cut = 0x7fffffff;
+        for (int j = g.t; j < n1; j += G::kThreads) {
+            if (j > 0 && (uint32_t)(X.cand[j] >> 32) != (uint32_t)(X.cand[j - 1] >> 32) && X.aux2[j - 1] >= PZ)
+                cut = min(cut, j);
+        }
+        cut = g_min_i(g, cut, S.redi);
+        if (cut != 0x7fffffff) n2 = cut;
+    }
+    const float Z = X.aux2[n2 - 1];
+    const uint32_t taukey = (uint32_t)(X.cand[n2 - 1] >> 32);
+    st.Z = Z;
+    st.invZ = __frcp_rn(Z);
+    st.taukey = taukey;
+    st.tau = key2f(taukey);
+    st.kind = n2 <= LCAP ? KIND_LIST : KIND_THRESH;
+    st.nlist = n2 <= LCAP ? n2 : 0;
+    g.sync();
+    if (n2 <= LCAP || want_bonus) {
+        const int np2 = pow2_at_least(n2);
+        for (int j = g.t; j < np2; j += G::kThreads) {
+            unsigned long long c = X.cand[j];
+            X.cand[j] = j < n2 ? ((c << 32) | (c >> 32)) : 0ull;
+        }
+        g.sync();
+        g_sort_desc(g, X.cand, np2);
+        for (int j = g.t; j < n2; j += G::kThreads) X.aux[j] = weight(key2f((uint32_t)X.cand[j]), m, s);
+        g.sync();
+        if (n2 <= LCAP) {
+            int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
+            for (int j = g.t; j < n2; j += G::kThreads)
+                L[j] = make_int2((int32_t)(~(uint32_t)(X.cand[j] >> 32)), __float_as_int(X.aux[j]));
+        }
+        if (want_bonus) {
+            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            int j = draw_small(g, X.aux, X.aux2, n2, u, S);
+            st.bonus = j >= 0 ? (int32_t)(~(uint32_t)(X.cand[j] >> 32)) : -1;
+        }
+        if (n2 <= LCAP && S.i < S.k) {
+            // the residual draw should the row's draft be rejected (as in the small-set path)
+            int *ltok = reinterpret_cast<int *>(X.aux2) + CAP / 2;
+            for (int j = g.t; j < n2; j += G::kThreads) ltok[j] = (int)(~(uint32_t)(X.cand[j] >> 32));
+            g.sync();
+            if (warp == 0) {
+                const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+                const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
+                const int t = warp_list_residual(ltok, X.aux, n2, st.invZ, qrow, u);
+                if (lane == 0) S.a = t;
+            }
+            g.sync();
+            st.resid = S.a;
+        }
+    }
+    g.sync();
+    return true;
+}
+
+// Kept set by radix select over the whole row (any top-k / top-p).
+template <typename E, bool VEC, class G>
+__device__ void kept_by_select(const G &g, const Args &A, RowCtx &S, const Scratch &X, const E *row, RowStat &st,
+                               bool want_bonus) {
+    const int V = A.V, nseg = A.nseg;
+    const float m = S.m, s = S.s;
+    uint32_t key_lo = 0;
+    if (S.topk_on) key_lo = select_kth_row<E, VEC>(g, S, row, V, nseg, S.K, X.hcnt);
+    if (S.topp_on) key_lo = select_mass_row<E, VEC>(g, S, row, V, nseg, key_lo, m, s, S.P, X.hmass);
+    WKept wk{m, s, key_lo};
+    seg_sums<E, VEC, false>(g, S, row, nullptr, V, nseg, X.segY, wk, nullptr, wk);
+    float part = 0.f;
+    for (int j = g.t; j < nseg; j += G::kThreads) part += X.segY[j];
+    const float Z = g_sum(g, part, S.redf);
+    st.Z = Z;
+    st.invZ = __frcp_rn(Z);
+    st.taukey = key_lo;
+    st.tau = key_lo ? key2f(key_lo) : -INFINITY;
+    st.kind = KIND_THRESH;
+    st.nlist = 0;
+    if (want_bonus) {
+        const float u = __ldg(A.uni + (size_t)S.r * 2 + 1);
+        st.bonus = draw_by_segments<E, VEC, false>(g, S, row, nullptr, V, nseg, X.segY, u, wk);
+    }
+}
+
+// The row's statistics, kept set, draws and draft gathers from its per-segment maxima (segA)
+// and weight sums (segB, for rows with no filter); writes the row's RowStat, kept list and
+// (p, q) of its draft.  segA/segB are consumed.
+template <typename E, bool VEC, class G>
+__device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &X, const SegStats &o) {
+    float *segA = o.mx, *segB = o.b;
+    const int V = A.V, nseg = A.nseg, row_idx = S.r;
+    const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)row_idx * V;
+    RowStat st;
+    st.m = 0.f; st.s = 0.f; st.tau = -INFINITY; st.Z = 1.f; st.invZ = 1.f; st.taukey = 0;
+    st.argmax = -1; st.bonus = -1; st.kind = KIND_SKIP; st.nlist = 0; st.resid = -1; st.pad1 = 0;
+    const bool sampled = !S.greedy;
+    const bool want_bonus = sampled && S.i == S.k;
+    const float s = S.s;
+    float mx = -INFINITY;
+    for (int j = g.t; j < nseg; j += G::kThreads) mx = fmaxf(mx, segA[j]);
+    const float m = g_max(g, mx, S.redf);
+    if (g.t == 0) S.m = m;
+    g.sync();
+    st.m = m;
+    st.s = s;
+
+    if (!sampled) {
+        // greedy: lowest id of the maximum -- the first segment holding it, the lowest lane of
+        // that segment holding it (recorded while streaming), then the first slot of the lane
+        int first = 0x7fffffff;
+        for (int j = g.t; j < nseg; j += G::kThreads)
+            if (segA[j] == m) first = min(first, j);
+        first = g_min_i(g, first, S.redi);
+        if (g.t == 0) {
+            int tok = first != 0x7fffffff ? find_in_lane<E, VEC>(S, row, V, first, o.lane[first], m) : -1;
+            S.tok = tok >= 0 ? tok : 0;
+        }
+        g.sync();
+        st.argmax = S.tok;
+        st.kind = KIND_GREEDY;
+    } else if (S.need_sum) {
+        // no filter: Z from the segment sums rescaled to the row max (fixed order)
+        float part = 0.f;
+        for (int j = g.t; j < nseg; j += G::kThreads) {
+            float w = segA[j] > -INFINITY ? __fmul_rn(segB[j], weight(segA[j], m, s)) : 0.f;
+            segB[j] = w;
+            part += w;
+        }
+        const float Z = g_sum(g, part, S.redf);
+        st.Z = Z;
+        st.invZ = __frcp_rn(Z);
+        st.kind = KIND_FULL;
+        if (want_bonus) {
+            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            WKept wk{m, s, 0u};
+            st.bonus = draw_by_segments<E, VEC, false>(g, S, row, nullptr, V, nseg, segB, u, wk);
+        }
+    } else {
+        bool done = false;
+        if (S.mode == MODE_TOP2) done = kept_from_candidates<E, VEC>(g, A, S, X, row, o, st, want_bonus);
+        if (!done) kept_by_select<E, VEC>(g, A, S, X, row, st, want_bonus);
+    }
+    SV_MARK(A, row_idx, 3);
+
+    // the draft of this row: p(x_i) and q(x_i) (prefetched while the row streamed)
+    if (g.t == 0 && S.i < S.k) {
+        const int x = S.xtok;
+        float p = 0.f, q = 0.f;
+        if (!sampled) {
+            p = NAN;
+            q = NAN;
+        } else if (x >= 0 && x < V) {
+            const float z = S.zx;
+            p = fkey(z) >= st.taukey ? __fmul_rn(weight(z, m, s), st.invZ) : 0.f;
+            q = S.qx;
+        }
+        const size_t d = (size_t)(S.d0 + S.i);
+        A.pq[d * 2] = p;
+        A.pq[d * 2 + 1] = q;
+        if (A.out_pq) {
+            A.out_pq[d * 2] = p;
+            A.out_pq[d * 2 + 1] = q;
+        }
+    }
+    if (g.t == 0) A.stats[row_idx] = st;
+}
+
+// A RowStat written by another CTA, read through L2.
+__device__ __forceinline__ RowStat load_stat(const RowStat *p) {
+    const int4 *q = reinterpret_cast<const int4 *>(p);
+    const int4 a = __ldcg(q), b = __ldcg(q + 1), c = __ldcg(q + 2);
+    RowStat st;
+    st.m = __int_as_float(a.x);
+    st.s = __int_as_float(a.y);
+    st.tau = __int_as_float(a.z);
+    st.Z = __int_as_float(a.w);
+    st.invZ = __int_as_float(b.x);
+    st.taukey = (uint32_t)b.y;
+    st.argmax = b.z;
+    st.bonus = b.w;
+    st.kind = c.x;
+    st.nlist = c.y;
+    st.resid = c.z;
+    st.pad1 = c.w;
+    return st;
+}
+
+// Accept test of one draft: accept with probability min(1, p/q), i.e. iff u < min(1, p/q);
+// q == 0 < p accepts and p == 0 rejects.
+__device__ __forceinline__ bool accept_test(float p, float q, float u) {
+    if (!(p > 0.f)) return false;
+    if (q == 0.f) return true;
+    const float ratio = __fdiv_rn(p, q);
+    return u < (ratio < 1.f ? ratio : 1.f);
+}
+
+// Request phase, run by the group that completed the request's last row: validate, find the
+// first rejection (one lane per draft, ballot), pick the final token, write the outputs.
+template <typename E, bool VEC, bool QVEC, class G>
+__device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
+    const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
+    if (g.warp() == 0) {
+        const int lane = g.lane();
+        int status = S.status;
+        int a = -1, tok = -1, need = 0;
+        if (status == 0) {
+            const bool greedy = S.greedy;
+            bool badtok = false, baduni = false, badrow = false;
+            a = k;
+            for (int i0 = 0; i0 <= k; i0 += 32) {
+                const int i = i0 + lane;
+                bool rej = false;
+                if (i <= k && __ldcg(&A.stats[r0 + i].kind) == KIND_FAIL) badrow = true;
+                if (i < k) {
+                    const int x = __ldg(A.tokens + d0 + i);
+                    if (x < 0 || x >= V) badtok = true;
+                    if (greedy) {
+                        rej = x != __ldcg(&A.stats[r0 + i].argmax);
+                    } else {
+                        const float p = __ldcg(A.pq + (size_t)(d0 + i) * 2);
+                        const float q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
+                        rej = !accept_test(p, q, __ldg(A.uni + (size_t)(r0 + i) * 2));
+                    }
+                }
+                if (!greedy && i <= k) {
+                    const float u0 = __ldg(A.uni + (size_t)(r0 + i) * 2), u1 = __ldg(A.uni + (size_t)(r0 + i) * 2 + 1);
+                    if (!(u0 >= 0.f && u0 < 1.f) || !(u1 >= 0.f && u1 < 1.f)) baduni = true;
+                }
+                const unsigned msk = __ballot_sync(0xffffffffu, rej);
+                if (msk && a == k) a = i0 + __ffs(msk) - 1;
+            }
+            badtok = __any_sync(0xffffffffu, badtok);
+            baduni = __any_sync(0xffffffffu, baduni);
+            badrow = __any_sync(0xffffffffu, badrow);
+            if (badtok) status = 2;
+            else if (baduni) status = 5;
+            else if (badrow) status = 7;
+            if (status == 0) {
+                if (greedy) {
+                    tok = __ldcg(&A.stats[r0 + a].argmax);
+                } else if (a == k) {
+                    tok = __ldcg(&A.stats[r0 + k].bonus);
+                } else if (__ldcg(&A.stats[r0 + a].kind) == KIND_LIST) {
+                    tok = __ldcg(&A.stats[r0 + a].resid);   // drawn speculatively with the row
+                } else {
+                    need = 1;
+                }
+            } else {
+                a = -1;
+            }
+        }
+        if (lane == 0) {
+            if (status) record_error(A, status, b);
+            S.a = a;
+            S.tok = tok;
+            S.need_resid = need;
+        }
+    }
+    g.sync();
+    if (S.need_resid) {
+        // residual max(0, p - q) over a whole row (rows that keep too many tokens for a list)
+        const int a = S.a;
+        const RowStat st = load_stat(A.stats + r0 + a);
+        const float *qrow = A.q + (size_t)(d0 + a) * V;
+        const float u = __ldg(A.uni + (size_t)(r0 + a) * 2 + 1);
+        if (g.warp() == 0) build_penalties(A, S, a);
+        g.sync();
+        const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)(r0 + a) * V;
+        WResid wr{st.m, st.s, st.invZ, st.taukey};
+        WProb wp{st.m, st.s, st.invZ, st.taukey};
+        seg_sums<E, VEC, QVEC>(g, S, row, qrow, V, A.nseg, X.segX, wr, X.segY, wp);
+        int tok = draw_by_segments<E, VEC, QVEC>(g, S, row, qrow, V, A.nseg, X.segX, u, wr);
+        if (tok < 0) tok = draw_by_segments<E, VEC, QVEC>(g, S, row, nullptr, V, A.nseg, X.segY, u, wp);
+        if (g.t == 0) S.tok = tok;
+        g.sync();
+    }
+    // outputs: accepted drafts, the final token, -1 padding
+    const int a = S.a, kw = A.k_max + 1;
+    for (int j = g.t; j < kw; j += G::kThreads) {
+        int v = -1;
+        if (a >= 0) v = j < a ? __ldg(A.tokens + d0 + j) : (j == a ? S.tok : -1);
+        A.out_tok[(size_t)b * kw + j] = v;
+    }
+    if (g.t == 0) {
+        A.acc[b] = a;
+        A.counters[b] = 0;
+    }
+}
+
+// Writes -1 outputs for request b (no rows, or inconsistent row_offsets).
+template <class G>
+__device__ __forceinline__ void fail_request(const G &g, const Args &A, int b) {
+    const int kw = A.k_max + 1;
+    for (int j = g.t; j < kw; j += G::kThreads) A.out_tok[(size_t)b * kw + j] = -1;
+    if (g.t == 0) {
+        A.acc[b] = -1;
+        record_error(A, 1, b);
+    }
+}
+
+// Requests that own no rows (row_offsets[j] == row_offsets[j+1]) get -1 outputs from the first
+// row of the nearest non-empty request before them (leading ones from the request of row 0).
+template <class G>
+__device__ __forceinline__ void fail_empty_requests(const G &g, const Args &A, const RowCtx &S) {
+    if (!A.row_off || S.i != 0 || S.b < 0) return;
+    if (S.r == 0)
+        for (int j = S.b - 1; j >= 0; j--) fail_request(g, A, j);
+    for (int j = S.b + 1; j < A.B && __ldg(A.row_off + j) == __ldg(A.row_off + j + 1); j++) fail_request(g, A, j);
+}
+
+// After a row: count it towards its request; the group that brings the count to the
+// request's row count finalises it.  Every thread of the group must call this.
+template <typename E, bool VEC, bool QVEC, class G>
+__device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
+    g.sync();
+    if (g.t == 0) {
+        __threadfence();
+        const int old = atomicAdd(A.counters + S.b, 1);
+        S.last = (old == S.nrows - 1);
+    }
+    g.sync();
+    if (S.last) {
+        __threadfence();
+        finalize<E, VEC, QVEC>(g, A, S, X);
+#ifdef SV_TIMING
+        if (g.t == 0) A.timing[(size_t)S.r * NTIME + 7] = 1;
+#endif
+    }
+    g.sync();
+}
+
+}  // namespace sv

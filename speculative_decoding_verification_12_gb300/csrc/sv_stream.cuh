@@ -1,0 +1,185 @@
+// sv_stream.cuh -- the streaming pass of the persistent kernel: per-segment statistics of a
+// row computed from its chunks in the shared-memory ring, specialised per statistics mode so
+// that a clean segment costs a handful of instructions per lane.
+//
+// A segment is "clean" when it lies wholly inside the row and holds no penalised token; clean
+// bf16 segments are reduced on packed bf16 pairs.  The rest (the row's ragged last segment,
+// segments holding a penalised token, and every fp32 segment) take the float path.
+#pragma once
+
+#include "sv_row.cuh"
+
+namespace sv {
+
+// Warp result of one segment from each lane's top value m1 (and second value m2): lane 0
+// writes the max, the lowest lane holding it, and in MODE_TOP2 the segment's second value.
+template <int MODE>
+__device__ __forceinline__ void seg_emit(int seg, float m1, float m2, const SegStats &o) {
+    const float mx = redux_max(m1);
+    if constexpr (MODE == MODE_ARG || MODE == MODE_TOP2) {
+        const int at = __ffs(__ballot_sync(0xffffffffu, m1 == mx)) - 1;
+        float sec = 0.f;
+        if constexpr (MODE == MODE_TOP2) sec = redux_max(lane_id() == at ? m2 : m1);
+        if (lane_id() == 0) {
+            o.mx[seg] = mx;
+            o.lane[seg] = at;
+            if constexpr (MODE == MODE_TOP2) o.b[seg] = sec;
+        }
+    } else {
+        if (lane_id() == 0) o.mx[seg] = mx;
+    }
+}
+
+// Statistics of a segment from this lane's 8 values (already masked and penalised).
+template <int MODE>
+__device__ __forceinline__ void seg_from_values(const float v[8], int seg, float s, const SegStats &o) {
+    if constexpr (MODE == MODE_SUM) {
+        const float mx = redux_max(max8(v));
+        float sum = 0.f;
+        if (mx > -INFINITY) {
+            const float ms = __fmul_rn(mx, s);
+#pragma unroll
+            for (int t = 0; t < 8; t++) sum += ex2(fmaf(v[t], s, -ms));
+            sum = warp_sum(sum);
+        }
+        if (lane_id() == 0) {
+            o.mx[seg] = mx;
+            o.b[seg] = sum;
+        }
+    } else if constexpr (MODE == MODE_TOP2) {
+        float m1 = v[0], m2 = -INFINITY;
+#pragma unroll
+        for (int t = 1; t < 8; t++) {
+            m2 = fmaxf(m2, fminf(m1, v[t]));
+            m1 = fmaxf(m1, v[t]);
+        }
+        seg_emit<MODE>(seg, m1, m2, o);
+    } else {
+        seg_emit<MODE>(seg, max8(v), 0.f, o);
+    }
+}
+
+// Clean segment: bf16 pairs reduced packed (top two of the lane's 8 in MODE_TOP2).
+template <typename E, int MODE>
+__device__ __forceinline__ void seg_clean(const Raw8<E> &raw, int seg, float s, const SegStats &o) {
+    if constexpr (sizeof(E) == 2 && MODE != MODE_SUM) {
+        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw.a);
+        const __nv_bfloat162 a = __hmax2(p[0], p[1]), c = __hmax2(p[2], p[3]);
+        const __nv_bfloat162 M = __hmax2(a, c);
+        if constexpr (MODE == MODE_TOP2) {
+            const __nv_bfloat162 b = __hmin2(p[0], p[1]), d = __hmin2(p[2], p[3]);
+            const __nv_bfloat162 S2 = __hmax2(__hmin2(a, c), __hmax2(b, d));
+            // fold the two halves: top = max of the maxima, second = max(min of the maxima,
+            // the halves' seconds)
+            const __nv_bfloat162 Ms = __lowhigh2highlow(M), Ss = __lowhigh2highlow(S2);
+            const __nv_bfloat162 T1 = __hmax2(M, Ms);
+            const __nv_bfloat162 T2 = __hmax2(__hmin2(M, Ms), __hmax2(S2, Ss));
+            seg_emit<MODE>(seg, __low2float(T1), __low2float(T2), o);
+        } else {
+            seg_emit<MODE>(seg, fmaxf(__low2float(M), __high2float(M)), 0.f, o);
+        }
+    } else {
+        float v[8];
+        unpack8(raw, v);
+        seg_from_values<MODE>(v, seg, s, o);
+    }
+}
+
+// Segment that is ragged (ends past V) or holds a penalised token.
+template <typename E, int MODE>
+__device__ __noinline__ void seg_dirty(const Raw8<E> raw, int seg, int V, const RowCtx &R, float s,
+                                       const SegStats o) {
+    float v[8];
+    unpack8(raw, v);
+    const int base = seg * SEG + lane_id() * 8;
+#pragma unroll
+    for (int t = 0; t < 8; t++)
+        if (base + t >= V) v[t] = -INFINITY;
+    patch_seg(R, seg * SEG, v);
+    seg_from_values<MODE>(v, seg, s, o);
+}
+
+// Ring position shared by the producer and the consumers: stage index and phase parity.
+struct RingPos {
+    int st;
+    uint32_t ph;
+    __device__ __forceinline__ void next(int pns) {
+        if (++st == pns) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// One streamer warp's share of a row: waits for each chunk, copies its segments to registers,
+// releases the stage, then reduces them.  Returns false when a wait timed out.
+template <typename E, int MODE, bool PEN>
+__device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned long long *empty,
+                                           const unsigned char *ring, int pns, RingPos &rp, int nchunks, int nseg,
+                                           int V, int sw, const RowCtx &R, const SegStats &o, const uint32_t *dmask,
+                                           unsigned long long *tslot) {
+    constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
+    constexpr int PER = (SPC + PSTREAM - 1) / PSTREAM;
+    constexpr bool EVEN = SPC % PSTREAM == 0;
+    const int nfull = V / SEG;                          // segments wholly inside the row
+    const float s = R.s;
+    (void)tslot;
+    for (int c = 0; c < nchunks; c++) {
+#ifdef SV_TIMING
+        const unsigned long long tw = global_ns();
+#endif
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[rp.st], rp.ph))) return false;
+#ifdef SV_TIMING
+        if (lane_id() == 0 && sw == 0) {
+            if (c == 0) tslot[8] = global_ns();
+            else tslot[10] += global_ns() - tw;
+        }
+#endif
+        const unsigned char *buf = ring + rp.st * SB;
+        Raw8<E> raw[PER];
+#pragma unroll
+        for (int u = 0; u < PER; u++) {
+            const int jj = sw + u * PSTREAM;
+            if (EVEN || jj < SPC) raw[u] = ring_raw<E>(buf, jj);
+        }
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&empty[rp.st]);
+        rp.next(pns);
+#pragma unroll
+        for (int u = 0; u < PER; u++) {
+            const int jj = sw + u * PSTREAM;
+            const int seg = c * SPC + jj;
+            if ((!EVEN && jj >= SPC) || seg >= nseg) continue;
+            bool clean = seg < nfull;
+            if constexpr (PEN) clean = clean && !((dmask[seg >> 5] >> (seg & 31)) & 1u);
+            if (clean) seg_clean<E, MODE>(raw[u], seg, s, o);
+            else seg_dirty<E, MODE>(raw[u], seg, V, R, s, o);
+        }
+    }
+    return true;
+}
+
+// Dispatch on the row's statistics mode and on whether it has penalised tokens.
+template <typename E>
+__device__ __forceinline__ bool stream_row_any(unsigned long long *full, unsigned long long *empty,
+                                               const unsigned char *ring, int pns, RingPos &rp, int nchunks,
+                                               int nseg, int V, int sw, const RowCtx &R, const SegStats &o,
+                                               const uint32_t *dmask, unsigned long long *tslot) {
+    const int mode = R.mode;
+    if (R.npen > 0) {
+        switch (mode) {
+            case MODE_ARG: return stream_row<E, MODE_ARG, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+            case MODE_TOP2: return stream_row<E, MODE_TOP2, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+            case MODE_SUM: return stream_row<E, MODE_SUM, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+            default: return stream_row<E, MODE_MAX, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+        }
+    }
+    switch (mode) {
+        case MODE_ARG: return stream_row<E, MODE_ARG, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+        case MODE_TOP2: return stream_row<E, MODE_TOP2, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+        case MODE_SUM: return stream_row<E, MODE_SUM, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+        default: return stream_row<E, MODE_MAX, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+    }
+}
+
+}  // namespace sv

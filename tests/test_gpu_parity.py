@@ -210,3 +210,19 @@ def test_ragged_b512_v151936_sampled(sv, oracle_lib):
 def test_stream_b1024_k7_v128256_sampled(sv, oracle_lib):
     s, g, w = _sampled(oracle_lib, "stream", 12)
     assert s["requests"] >= 10
+
+
+def test_max_vocabulary_row_kernel(sv, oracle_lib):
+    """V = 2^21 (the largest supported): the persistent kernel's shared memory no longer fits,
+    so the one-CTA-per-row kernel runs on aligned rows."""
+    w = W.random_batch(27, B=3, k_max=2, V=1 << 21, dtype="bf16", greedy_frac=0.3, penalties=True)
+    w.top_k[:] = [0, 40, 3000]
+    w.top_p[:] = [1.0, 0.9, 0.5]
+    full_compare(oracle_lib, w)
+
+
+def test_many_rows_few_ctas(sv, oracle_lib):
+    """More rows than resident CTAs with mixed greedy / sampled / ragged requests: rows are
+    claimed dynamically and requests finalised by whichever CTA completes them."""
+    w = W.random_batch(28, B=300, k_max=8, V=4096, dtype="bf16", varlen=True, greedy_frac=0.3)
+    full_compare(oracle_lib, w)
