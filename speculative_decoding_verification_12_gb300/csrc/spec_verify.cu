@@ -1,17 +1,17 @@
 // spec_verify.cu -- batched speculative-decoding verification for GB300 (sm_103a): the
-// C-ABI entry points and the two verify kernels.
+// C-ABI entry points and the verify kernels.
 //
-// Persistent kernel (16-byte aligned rows; the fast path).  A grid of two CTAs per SM claims
-// target rows from a counter in the workspace.  Inside a CTA the warps specialise:
-//   warp 0     issues cp.async.bulk copies of row after row into a 6 x 8 KB shared-memory
-//              ring (completion on mbarriers with transaction counts);
-//   warp 1     claims the next rows and prepares them: request lookup, sampling
-//              parameters, penalties of the earlier drafts, and the row's draft gathers
-//              (x_i, z(x_i), q(x_i)), up to NRB rows ahead;
-//   warps 2-9  reduce each streamed 256-token segment to its max (and weight sum);
-//   warps 10-13 turn a finished row's segment statistics into its kept set, draws and
-//              draft probabilities while the next row streams, and finalise a request when
-//              its last row is done.
+// Fast path (16-byte aligned rows): two kernels per call.
+//   stream kernel  SCTA persistent CTAs per SM claim work units (whole rows, then parts of the
+//                  last wave of rows) from a counter in the workspace.  Warp 0 issues
+//                  cp.async.bulk copies of each unit into a shared-memory ring (completion on
+//                  mbarriers with transaction counts); warp 1 prepares the units (request
+//                  lookup, sampling parameters, penalties of the earlier drafts, the row's draft
+//                  gathers); the streamer warps reduce each 256-token segment to the statistics
+//                  the row's filters need and write them to the workspace.
+//   select kernel  one CTA per row, launched as a programmatic dependent of the stream kernel:
+//                  the row's kept set, draws and draft probabilities; the last row of a request
+//                  finalises it.
 // Every mbarrier wait is bounded in time; on expiry the row fails with SV_DEV_TIMEOUT.
 //
 // Row kernel (any alignment).  One CTA per row streams it with plain 128-bit or scalar loads
@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
         // the last thread prefetches the row's draft gathers while the row streams
         int x = -1;
         E zraw = E(0);
-        float qx = 0.f;
+        float qx = 0.f, u1 = 0.f;
+        if (g.t == RT - 1 && !S.greedy) u1 = __ldg(A.uni + (size_t)r * 2 + 1);
         if (g.t == RT - 1 && S.i < S.k) {
             x = __ldg(A.tokens + S.d0 + S.i);
             if (x >= 0 && x < A.V) {
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
             S.xtok = x;
             S.zx = elem_z_raw(S, zraw, x);
             S.qx = qx;
+            S.u1 = u1;
         }
         g.sync();
         SV_MARK(A, r, 2);
@@ -103,54 +105,80 @@ __global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
 // persistent kernel: 16-byte aligned rows
 // ------------------------------------------------------------------------------------------
 
-struct PShared {
+// ------------------------------------------------------------------------------------------
+// Two-kernel path (16-byte aligned rows).  Streaming and selection have opposite needs: the
+// stream is bound by HBM bandwidth and wants every issue slot for its reductions; a row's
+// selection is a short chain of dependent steps that wants many rows in flight.  So:
+//   stream kernel  persistent CTAs stream every row once through a bulk-copy ring and write
+//                  per-segment statistics (or, for greedy rows, a (max, position) key) to the
+//                  workspace; the last wave of rows is split into parts so that the kernel
+//                  does not end on a few CTAs streaming whole rows;
+//   select kernel  one CTA per row turns the statistics into the row's kept set, draws and
+//                  draft probabilities, and the request's last row finalises it.  It is
+//                  launched as a programmatic dependent of the stream kernel: each CTA looks up
+//                  its row, penalties and draft gathers while the stream finishes, then waits
+//                  for the stream's results.
+// ------------------------------------------------------------------------------------------
+
+struct SShared {
     unsigned long long full[PNS_MAX];   // ring stage holds its chunk (transaction count)
     unsigned long long empty[PNS_MAX];  // every streamer warp released the stage
-    unsigned long long rb_desc[NRB];  // row buffer prepared by the scheduler
-    unsigned long long rb_stats[NRB]; // row buffer's segment statistics complete
-    unsigned long long rb_free[NRB];  // selector done with the row buffer
+    unsigned long long rb_desc[NRB];    // unit buffer prepared by the scheduler
+    unsigned long long rb_done[NRB];    // every streamer warp finished the unit
     int fail;
     RowCtx rc[NRB];
 };
 
-// Per row buffer of the persistent kernel: segment max, second value / weight sum, lane of the
-// max, and a bitmask of the segments holding a penalised token; rounded to 128 bytes so that
-// every buffer after it (and the 8-byte candidate keys of the scratch) stays aligned.
-__host__ __device__ inline size_t pstats_bytes(int np) { return ((size_t(3) * np + np / 32) * 4 + 127) & ~size_t(127); }
+__host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
+__host__ __device__ inline size_t mask_words(int np) { return (size_t)np / 32; }
+// Dynamic shared memory of the stream kernel: the ring, then NRB masks of penalised segments.
+__host__ __device__ inline size_t stream_smem(int nseg, int pns) {
+    return (size_t)pns * SB + up128((size_t)NRB * mask_words(nseg_pad(nseg)) * 4);
+}
+// Dynamic shared memory of the select kernel: the row's statistics, then the scratch.
+__host__ __device__ inline size_t select_smem(int nseg) {
+    const int np = nseg_pad(nseg);
+    return up128((size_t)3 * np * 4) + up128(scratch_bytes(np));
+}
 
-__device__ __forceinline__ SegStats carve_pstats(unsigned char *p, int np, uint32_t *&dmask) {
+// Segment statistics (max, second value or weight sum, lane of the max) at base.
+__device__ __forceinline__ SegStats stats_at(float *base, int np) {
     SegStats o;
-    o.mx = reinterpret_cast<float *>(p);
-    o.b = o.mx + np;
-    o.lane = reinterpret_cast<int *>(o.b + np);
+    o.mx = base;
+    o.b = base + np;
+    o.lane = reinterpret_cast<int *>(base + 2 * np);
     o.hist = nullptr;
-    dmask = reinterpret_cast<uint32_t *>(o.lane + np);
     return o;
 }
 
-__host__ __device__ inline size_t persistent_smem(int nseg, int pns) {
-    const int np = nseg_pad(nseg);
-    return size_t(pns) * SB + size_t(NRB) * pstats_bytes(np) + scratch_bytes(np);
+// Chunk range of part p of a row with nc chunks split into P parts.
+__device__ __forceinline__ void part_chunks(int nc, int P, int p, int &c0, int &c1) {
+    c0 = (int)((long long)nc * p / P);
+    c1 = (int)((long long)nc * (p + 1) / P);
 }
 
-__device__ __forceinline__ void pfail(const Args &A, PShared &P, int b) {
+__device__ __forceinline__ void sfail(const Args &A, SShared &P, int b) {
     P.fail = 1;
     record_error(A, 7, b < 0 ? 0 : b);
 }
 
-template <typename E, bool QVEC>
-__global__ void __launch_bounds__(PT, PCTA) verify_persistent_kernel(const Args A) {
+// Work unit u: row u while u < R - nsplit, then part (t mod nparts) of row R - nsplit + t / nparts
+// with t = u - (R - nsplit).
+template <typename E>
+__global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ PShared P;
+    __shared__ SShared P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int V = A.V, nseg = A.nseg, np = nseg_pad(nseg), PNS = A.pns;
+    const int V = A.V, nseg = A.nseg, np = nseg_pad(nseg), PNS = A.pns, NP = A.nparts;
     const uint32_t RB = (uint32_t)V * sizeof(E);
     const int nc = (int)((RB + SB - 1) / SB);
-    constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
     unsigned char *ring = dsm;
-    unsigned char *rbstats = dsm + size_t(PNS) * SB;   // after the ring
-    const Scratch X = carve_scratch(rbstats + size_t(NRB) * pstats_bytes(np), np);
+    uint32_t *masks = reinterpret_cast<uint32_t *>(dsm + (size_t)PNS * SB);
+    const long long whole = (long long)A.R - A.nsplit;
+    const long long units = whole + (long long)A.nsplit * NP;
 
+    // the select kernel's CTAs may be scheduled as soon as SMs free up
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int s = 0; s < PNS; s++) {
             mbar_init(&P.full[s], 1);
@@ -158,8 +186,7 @@ __global__ void __launch_bounds__(PT, PCTA) verify_persistent_kernel(const Args 
         }
         for (int s = 0; s < NRB; s++) {
             mbar_init(&P.rb_desc[s], 1);
-            mbar_init(&P.rb_stats[s], PSTREAM);
-            mbar_init(&P.rb_free[s], 1);
+            mbar_init(&P.rb_done[s], PSTREAM);
         }
         P.fail = 0;
         mbar_fence_init();
@@ -167,33 +194,27 @@ __global__ void __launch_bounds__(PT, PCTA) verify_persistent_kernel(const Args 
     __syncthreads();
 
     if (warp == 0) {
-        // ---- issuer: bulk copies of each prepared row, chunk by chunk, through the ring
+        // ---- issuer (one thread): bulk copies of each prepared unit, chunk by chunk
         if (lane != 0) return;
-        const unsigned long long pol = l2_evict_last();
+        const unsigned long long pol = l2_evict_first();
         int q = 0;
         RingPos rp{0, 0u};
         for (int j = 0;; j++) {
             const int slot = j % NRB;
             if (!mbar_wait(&P.rb_desc[slot], (uint32_t)(j / NRB) & 1u)) {
-                pfail(A, P, -1);
+                sfail(A, P, -1);
                 return;
             }
             const RowCtx &R = P.rc[slot];
             if (R.r < 0) return;
             const unsigned char *src = reinterpret_cast<const unsigned char *>(A.logits) + (size_t)R.r * RB;
-            for (int c = 0; c < R.nchunks; c++, q++) {
+            for (int c = R.c0; c < R.c1; c++, q++) {
                 const int st = rp.st;
-#ifdef SV_TIMING
-                const unsigned long long tw = global_ns();
-#endif
                 // the stage's previous fill (one lap earlier) must have been released
                 if (q >= PNS && !mbar_wait(&P.empty[st], rp.ph ^ 1u)) {
-                    pfail(A, P, R.b);
+                    sfail(A, P, R.b);
                     return;
                 }
-#ifdef SV_TIMING
-                A.timing[(size_t)R.r * NTIME + 11] += global_ns() - tw;
-#endif
                 const uint32_t off = (uint32_t)c * SB;
                 const uint32_t bytes = min((uint32_t)SB, RB - off);
                 mbar_expect_tx(&P.full[st], bytes);
@@ -202,44 +223,43 @@ __global__ void __launch_bounds__(PT, PCTA) verify_persistent_kernel(const Args 
             }
         }
     } else if (warp == 1) {
-        // ---- scheduler: claim rows and prepare their descriptors up to NRB rows ahead
+        // ---- scheduler (one warp): claim units and prepare them up to NRB ahead
         for (int j = 0;; j++) {
             const int slot = j % NRB;
             bool ok = true;
-            if (j >= NRB) ok = mbar_wait_idle(&P.rb_free[slot], (uint32_t)(j / NRB - 1) & 1u);
+            if (j >= NRB) ok = mbar_wait(&P.rb_done[slot], (uint32_t)(j / NRB - 1) & 1u);
             if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) pfail(A, P, -1);
+                if (lane == 0) sfail(A, P, -1);
                 return;
             }
             RowCtx &R = P.rc[slot];
-            int r = 0;
-            if (lane == 0) r = atomicAdd(A.hdr + 2, 1);
-            r = __shfl_sync(0xffffffffu, r, 0);
-            if (r >= A.R) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(A.hdr + 2, 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u >= units) {
                 if (lane == 0) {
                     R.r = -1;
                     mbar_arrive(&P.rb_desc[slot]);
                 }
                 return;
             }
-            SV_MARK(A, r, 0);
-#ifdef SV_TIMING
-            if (lane == 0) {
-                unsigned smid;
-                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-                A.timing[(size_t)r * NTIME + 6] = ((unsigned long long)blockIdx.x << 32) | smid;
-                A.timing[(size_t)r * NTIME + 7] = 0;
-                A.timing[(size_t)r * NTIME + 10] = 0;
-                A.timing[(size_t)r * NTIME + 11] = 0;
+            int r, part, npu;
+            if (u < whole) {
+                r = u;
+                part = 0;
+                npu = 1;
+            } else {
+                const int t = (int)(u - whole);
+                r = (int)whole + t / NP;
+                part = t - (t / NP) * NP;
+                npu = NP;
             }
-#endif
             locate_row(A, R, r);
             if (R.active) build_penalties(A, R, R.i);
             __syncwarp();
             if (R.active && R.npen > 0) {
                 // segments holding a penalised token take the streamers' slow path
-                uint32_t *dmask;
-                carve_pstats(rbstats + size_t(slot) * pstats_bytes(np), np, dmask);
+                uint32_t *dmask = masks + slot * mask_words(np);
                 for (int w = lane; w < np / 32; w += 32) dmask[w] = 0u;
                 __syncwarp();
                 for (int h = lane; h < R.npen; h += 32) {
@@ -249,74 +269,78 @@ __global__ void __launch_bounds__(PT, PCTA) verify_persistent_kernel(const Args 
             }
             __syncwarp();
             if (lane == 0) {
-                prefetch_draft<E>(A, R, reinterpret_cast<const E *>(A.logits) + (size_t)r * V);
-                R.nchunks = R.active ? nc : 0;
-                SV_MARK(A, r, 1);
+                R.part = part;
+                R.nparts = npu;
+                int c0 = 0, c1 = 0;
+                if (R.active) part_chunks(nc, npu, part, c0, c1);
+                R.c0 = c0;
+                R.c1 = c1;
                 mbar_arrive(&P.rb_desc[slot]);
+            }
+            if (part == 0) {
+                // the row's prepared context for the select kernel, with its draft gathers
+                if (lane == 0) prefetch_draft<E>(A, R, reinterpret_cast<const E *>(A.logits) + (size_t)r * V);
+                __syncwarp();
+                const int4 *src = reinterpret_cast<const int4 *>(&R);
+                int4 *dst = A.prep + (size_t)r * (PREP_BYTES / 16);
+                for (int t = lane; t < PREP_BYTES / 16; t += 32) dst[t] = src[t];
             }
             __syncwarp();
         }
-    } else if (warp < 2 + PSTREAM) {
-        // ---- streamers: per-segment statistics of each row from the ring
+    } else {
+        // ---- streamers: per-segment statistics of each unit from the ring into the workspace
         const int sw = warp - 2;
         RingPos rp{0, 0u};
         for (int j = 0;; j++) {
             const int slot = j % NRB;
             if (!__all_sync(0xffffffffu, mbar_wait(&P.rb_desc[slot], (uint32_t)(j / NRB) & 1u))) {
-                if (lane == 0) pfail(A, P, -1);
+                if (lane == 0) sfail(A, P, -1);
                 return;
             }
             const RowCtx &R = P.rc[slot];
             if (R.r < 0) return;
-            uint32_t *dmask;
-            const SegStats o = carve_pstats(rbstats + size_t(slot) * pstats_bytes(np), np, dmask);
-            unsigned long long *tslot = nullptr;
-#ifdef SV_TIMING
-            tslot = A.timing + (size_t)R.r * NTIME;
-#endif
-            if (!stream_row_any<E>(P.full, P.empty, ring, PNS, rp, R.nchunks, nseg, V, sw, R, o, dmask, tslot)) {
-                if (lane == 0) pfail(A, P, R.b);
+            const SegStats o = stats_at(A.gstats + (size_t)R.r * 3 * np, np);
+            if (!stream_row_any<E>(P.full, P.empty, ring, PNS, rp, R.c0, R.c1, nseg, V, sw, R, o,
+                                   masks + slot * mask_words(np), A.rowarg + R.r, nullptr)) {
+                if (lane == 0) sfail(A, P, R.b);
                 return;
             }
             __syncwarp();
-            if (lane == 0) {
-                if (sw == 0) SV_MARK(A, R.r, 2);
-                mbar_arrive(&P.rb_stats[slot]);
-            }
-        }
-    } else {
-        // ---- selectors: kept set, draws and gathers of each finished row; finalisation
-        const Grp<PSEL * 32, 1> g(threadIdx.x - 32 * (2 + PSTREAM));
-        for (int j = 0;; j++) {
-            const int slot = j % NRB;
-            const uint32_t par = (uint32_t)(j / NRB) & 1u;
-            const bool ok = mbar_wait_idle(&P.rb_desc[slot], par);
-            RowCtx &R = P.rc[slot];
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) pfail(A, P, -1);
-            }
-            g.sync();
-            if (P.fail || R.r < 0) return;
-            const bool ok2 = mbar_wait_idle(&P.rb_stats[slot], par);
-            if (!__all_sync(0xffffffffu, ok2)) {
-                if (lane == 0) pfail(A, P, R.b);
-            }
-            g.sync();
-            if (P.fail) return;
-            SV_MARK(A, R.r, 9);
-            if (R.b >= 0) {
-                fail_empty_requests(g, A, R);
-                uint32_t *dmask;
-                const SegStats o = carve_pstats(rbstats + size_t(slot) * pstats_bytes(np), np, dmask);
-                if (R.active) select_row<E, true>(g, A, R, X, o);
-                SV_MARK(A, R.r, 4);
-                arrive_and_finalize<E, true, QVEC>(g, A, R, X);
-                SV_MARK(A, R.r, 5);
-            }
-            g.sync();
-            if (g.t == 0) mbar_arrive(&P.rb_free[slot]);
+            if (lane == 0) mbar_arrive(&P.rb_done[slot]);
         }
     }
+}
+
+// One CTA per row: the row's kept set, draws and draft probabilities from the statistics the
+// stream kernel wrote; the request's last row finalises the request.
+template <typename E, bool QVEC>
+__global__ void __launch_bounds__(SELT, 4) select_kernel(const Args A) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ RowCtx S;
+    const Grp<SELT, 0> g(threadIdx.x);
+    const int r = blockIdx.x;
+    const int np = nseg_pad(A.nseg);
+    float *sb = reinterpret_cast<float *>(dsm);
+    const Scratch X = carve_scratch(dsm + up128((size_t)3 * np * 4), np);
+    SV_MARK(A, r, 0);
+    // the stream kernel's results (and every earlier write on the stream) are visible past here
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    SV_MARK(A, r, 1);
+    // the row's prepared context and segment statistics, in one round of loads
+    {
+        const int4 *src = A.prep + (size_t)r * (PREP_BYTES / 16);
+        if (g.t < PREP_BYTES / 16) reinterpret_cast<int4 *>(&S)[g.t] = __ldcg(src + g.t);
+        const float4 *gs = reinterpret_cast<const float4 *>(A.gstats + (size_t)r * 3 * np);
+        for (int t = g.t; t < 3 * np / 4; t += SELT) reinterpret_cast<float4 *>(sb)[t] = __ldcg(gs + t);
+    }
+    g.sync();
+    SV_MARK(A, r, 2);
+    if (S.b < 0) return;   // a row outside every request: nothing to count
+    fail_empty_requests(g, A, S);
+    if (S.active) select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
+    SV_MARK(A, r, 4);
+    arrive_and_finalize<E, true, QVEC>(g, A, S, X);
+    SV_MARK(A, r, 5);
 }
 
 __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *nd, int B, int32_t *hdr) {
@@ -357,39 +381,51 @@ static cudaError_t launch_rows(const Args &A, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Launches the persistent kernel with (SMs x resident CTAs) CTAs; returns cudaErrorNotSupported
-// (nothing launched) when it cannot be resident for this vocabulary.
+// Launches the stream kernel (SCTA CTAs per SM) and the select kernel as its programmatic
+// dependent; returns cudaErrorNotSupported (nothing launched) when the kernels cannot be
+// resident for this vocabulary.
 template <typename E, bool QVEC>
-static cudaError_t launch_persistent(const Args &A, cudaStream_t stream) {
-    static size_t enabled = 0;
+static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
+    static size_t enabled1 = 0, enabled2 = 0;
     static int sms[64] = {0};
-    static int occ_for_nseg[64] = {0};
-    static int occ_val[64] = {0};
-    // the deepest ring (3..PNS_MAX stages) that still lets two CTAs share an SM
-    Args B = A;
-    B.pns = PNS_MAX;
-    while (B.pns > 3 && PCTA * (persistent_smem(A.nseg, B.pns) + sizeof(PShared) + 1024) > 228 * 1024) B.pns--;
-    const size_t smem = persistent_smem(A.nseg, B.pns);
-    if (smem > 227 * 1024) return cudaErrorNotSupported;
-    auto kern = verify_persistent_kernel<E, QVEC>;
-    cudaError_t e = ensure_smem(kern, smem, enabled);
-    if (e != cudaSuccess) return e;
     int dev = 0;
+    cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
     if (!sms[dev] && (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    if (occ_for_nseg[dev] != A.nseg) {
-        int occ = 0;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, PT, smem)) != cudaSuccess) return e;
-        occ_val[dev] = occ;
-        occ_for_nseg[dev] = A.nseg;
-    }
-    const int occ = occ_val[dev];
-    if (occ < 1) return cudaErrorNotSupported;
-    const int grid = (int)((long long)sms[dev] * occ < (long long)A.R ? sms[dev] * occ : A.R);
-    kern<<<grid, PT, smem, stream>>>(B);
-    return cudaGetLastError();
+    Args B = A;
+    const long long ctas = (long long)sms[dev] * SCTA;
+    // the last wave of rows (one per CTA) is split into parts of at least 2 chunks
+    const long long nc = ((long long)A.V * sizeof(E) + SB - 1) / SB;
+    B.nparts = (int)(nc / 2 < SPLIT_PARTS ? nc / 2 : SPLIT_PARTS);
+    if (B.nparts < 2 || A.R < 2) B.nparts = 1;
+    B.nsplit = B.nparts > 1 ? (int)(ctas < A.R ? ctas : A.R) : 0;
+    // shared memory of one stream CTA when SCTA share an SM (228 KB, 1 KB reserved per CTA)
+    const size_t budget = (SCTA == 1 ? (size_t)232448 : (size_t)233472 / SCTA - 1024) - sizeof(SShared);
+    B.pns = PNS_MAX;
+    while (B.pns > 3 && stream_smem(A.nseg, B.pns) > budget) B.pns--;
+    const size_t smem1 = stream_smem(A.nseg, B.pns), smem2 = select_smem(A.nseg);
+    if (smem1 > budget || smem2 > (size_t)232448 - sizeof(RowCtx)) return cudaErrorNotSupported;
+    auto k1 = stream_kernel<E>;
+    auto k2 = select_kernel<E, QVEC>;
+    if ((e = ensure_smem(k1, smem1, enabled1)) != cudaSuccess) return e;
+    if ((e = ensure_smem(k2, smem2, enabled2)) != cudaSuccess) return e;
+    const long long units = (long long)A.R - B.nsplit + (long long)B.nsplit * B.nparts;
+    const int grid = (int)(ctas < units ? ctas : units);
+    k1<<<grid, ST, smem1, stream>>>(B);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)A.R);
+    cfg.blockDim = dim3(SELT);
+    cfg.dynamicSmemBytes = smem2;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k2, B);
 }
 
 }  // namespace sv
@@ -398,7 +434,7 @@ using namespace sv;
 
 extern "C" size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V) {
     if (B < 1 || total_rows < B || V < 1) return 0;
-    return ws_layout(B, total_rows).total;
+    return ws_layout(B, total_rows, V).total;
 }
 
 extern "C" const char *sv_status_string(sv_status s) {
@@ -426,7 +462,7 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
     if (!target_logits || !num_drafts || !uniforms || !out_tokens || !accept_len || !workspace) return SV_ERR_INVALID_ARG;
     if (D > 0 && (!draft_probs || !draft_tokens)) return SV_ERR_INVALID_ARG;
     if (!params.temperature || !params.top_k || !params.top_p || !params.greedy) return SV_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(B, total_rows);
+    const WsLayout L = ws_layout(B, total_rows, V);
     if (((uintptr_t)workspace & 255) != 0 || workspace_bytes < L.total) return SV_ERR_WORKSPACE;
 
     char *ws = static_cast<char *>(workspace);
@@ -448,27 +484,32 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
     A.out_pq = out_pq;
     A.hdr = reinterpret_cast<int32_t *>(ws);
     A.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+    A.rowarg = reinterpret_cast<unsigned long long *>(ws + L.rowarg);
+    A.prep = reinterpret_cast<int4 *>(ws + L.prep);
+    A.gstats = reinterpret_cast<float *>(ws + L.gstats);
     A.stats = reinterpret_cast<RowStat *>(ws + L.stats);
     A.pq = reinterpret_cast<float *>(ws + L.pq);
-    A.lists = reinterpret_cast<int32_t *>(ws + L.lists);
     A.timing = reinterpret_cast<unsigned long long *>(ws + L.timing);
     A.B = B;
     A.k_max = k_max;
     A.V = V;
     A.R = total_rows;
-    A.nseg = (V + SEG - 1) / SEG;
+    A.nseg = nseg_of(V);
     A.pns = 0;
+    A.nparts = 1;
+    A.nsplit = 0;
     const size_t esz = logits_dtype == SV_BF16 ? 2 : 4;
     const bool vec = ((uintptr_t)target_logits % 16 == 0) && ((size_t)V * esz) % 16 == 0;
     const bool qvec = (!draft_probs || (uintptr_t)draft_probs % 16 == 0) && ((size_t)V * 4) % 16 == 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // clear the error word, the row claim counter and the per-request arrival counters
-    if (cudaMemsetAsync(ws, 0, L.counters + (size_t)B * 4, st) != cudaSuccess) return SV_ERR_CUDA;
+    // clear the error word, the work claim counter, the per-request arrival counters, the
+    // per-row part counters and the greedy rows' argmax keys
+    if (cudaMemsetAsync(ws, 0, L.rowarg + (size_t)total_rows * 8, st) != cudaSuccess) return SV_ERR_CUDA;
     cudaError_t e = cudaErrorNotSupported;
     if (vec) {
-        if (logits_dtype == SV_BF16) e = qvec ? launch_persistent<uint16_t, true>(A, st) : launch_persistent<uint16_t, false>(A, st);
-        else e = qvec ? launch_persistent<float, true>(A, st) : launch_persistent<float, false>(A, st);
+        if (logits_dtype == SV_BF16) e = qvec ? launch_two_kernels<uint16_t, true>(A, st) : launch_two_kernels<uint16_t, false>(A, st);
+        else e = qvec ? launch_two_kernels<float, true>(A, st) : launch_two_kernels<float, false>(A, st);
     }
     if (e == cudaErrorNotSupported) {
         cudaGetLastError();   // clear a sticky "not supported" from the probe, if any

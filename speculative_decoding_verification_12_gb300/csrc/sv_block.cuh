@@ -87,6 +87,21 @@ struct Grp {
     }
 };
 
+// A group of NTH threads (whole warps) synchronised on a named barrier chosen at run time.
+template <int NTH>
+struct GrpR {
+    static constexpr int kThreads = NTH;
+    static constexpr int kWarps = NTH / 32;
+    int t;     // thread index within the group
+    int bar;   // named barrier id (1..15)
+    __device__ __forceinline__ GrpR(int t_, int bar_) : t(t_), bar(bar_) {}
+    __device__ __forceinline__ int warp() const { return t >> 5; }
+    __device__ __forceinline__ int lane() const { return t & 31; }
+    __device__ __forceinline__ void sync() const {
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(NTH) : "memory");
+    }
+};
+
 template <class G>
 __device__ __forceinline__ float g_max(const G &g, float v, float *red) {
     v = warp_max(v);
@@ -318,11 +333,11 @@ __device__ __forceinline__ bool mbar_wait_idle(unsigned long long *bar, uint32_t
     return true;
 }
 
-// L2 policy that keeps lines resident in preference to others (rows re-read shortly after
-// they stream stay in L2).
-__device__ __forceinline__ unsigned long long l2_evict_last() {
+// L2 policy that evicts lines first: rows streamed once should not displace the small
+// per-segment statistics the next kernel reads back.
+__device__ __forceinline__ unsigned long long l2_evict_first() {
     unsigned long long pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 // One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16) that

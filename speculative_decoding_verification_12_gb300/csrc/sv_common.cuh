@@ -8,10 +8,13 @@
 namespace sv {
 
 constexpr int SEG = 256;              // elements per segment: one warp step of 32 lanes x 8
-constexpr int CAP = 1536;             // candidate buffer (top-k candidates, kept lists) per CTA
+#ifndef SV_CAP
+#define SV_CAP 1536
+#endif
+constexpr int CAP = SV_CAP;           // candidate buffer (top-k candidates, kept lists) per group
 constexpr int KCAP = 512;             // top-k up to this goes through the candidate buffer
 constexpr int WCAP = 256;             // candidate sets up to this are cut and drawn by one warp
-constexpr int LCAP = 256;             // kept-list entries stored per row for the residual draw
+constexpr int LCAP = 256;             // kept sets up to this are drawn from as lists (KIND_LIST)
 constexpr int HB = 2048;              // radix histogram bins (11-bit digits)
 #ifndef SV_SB
 #define SV_SB 12288
@@ -26,23 +29,31 @@ constexpr double FIXED_ONE = 1099511627776.0;   // 2^40: fixed-point scale of to
 // Row kernel (one CTA per row; any alignment): 256 threads, 8 warps.
 constexpr int RT = 256;
 
-// Persistent kernel (16-byte aligned rows): warp 0 issues bulk copies, warp 1 schedules rows,
-// PSTREAM warps reduce the streamed chunks, PSEL warps select the kept set and finalise.
+// Stream kernel (16-byte aligned rows), SCTA CTAs per SM: warp 0 issues bulk copies, warp 1
+// schedules work units, PSTREAM warps reduce the streamed chunks.  Select kernel: SELT threads
+// per row.
+#ifndef SV_SCTA
+#define SV_SCTA 3
+#endif
 #ifndef SV_PSTREAM
 #define SV_PSTREAM 8
 #endif
-#ifndef SV_PCTA
-#define SV_PCTA 2
+#ifndef SV_SPLIT_PARTS
+#define SV_SPLIT_PARTS 4              // parts the last wave of rows is split into (1: no split)
 #endif
+constexpr int SCTA = SV_SCTA;
 constexpr int PSTREAM = SV_PSTREAM;
-constexpr int PSEL = 4;
-constexpr int PCTA = SV_PCTA;         // resident CTAs per SM the kernel is built for
-constexpr int PT = 32 * (2 + PSTREAM + PSEL);
+constexpr int SPLIT_PARTS = SV_SPLIT_PARTS;
+constexpr int ST = 32 * (2 + PSTREAM);
+constexpr int SELT = 128;
 #ifndef SV_PNS_MAX
-#define SV_PNS_MAX 8
+#define SV_PNS_MAX 16
 #endif
 constexpr int PNS_MAX = SV_PNS_MAX;   // ring stages at most (the launch picks what fits)
-constexpr int NRB = 3;                // row buffers (rows between scheduler and selector)
+#ifndef SV_NRB
+#define SV_NRB 3
+#endif
+constexpr int NRB = SV_NRB;           // unit buffers between the scheduler and the streamers
 
 // What the streaming pass records per 256-token segment of a row (besides its max).
 enum : int32_t {
@@ -81,31 +92,42 @@ struct __align__(16) RowStat {
 };
 
 struct WsLayout {
-    size_t counters, stats, pq, lists, timing, total;
+    size_t counters, rowarg, stats, pq, prep, gstats, timing, total;
 };
 
-// Phase timestamps (globaltimer ns) per row, recorded only in builds with SV_TIMING.
+// Phase timestamps (globaltimer ns) per work unit, recorded only in builds with SV_TIMING.
 constexpr int NTIME = 24;
+constexpr int PMAX = 8;               // persistent kernel: most parts a row is split into
 
 __host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ inline int nseg_of(int V) { return (V + SEG - 1) / SEG; }
+__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
 
-// Workspace: [header 256 B: error word, first bad request, row claim counter]
-// [per-request arrival counters][RowStat per row][(p, q) per draft]
-// [kept lists: LCAP x (token, weight) per row][timing, SV_TIMING builds only].
-__host__ __device__ inline WsLayout ws_layout(int B, int R) {
+// Workspace: [header 256 B: error word, first bad request, work claim counter]
+// [per-request arrival counters][per-row argmax keys of greedy rows]
+// [RowStat per row][(p, q) per draft][prepared row context, 640 B per row]
+// [segment statistics: 3 words per padded segment
+// per row][timing, SV_TIMING builds only].  The header, the counters and the argmax keys are
+// cleared by every call.
+__host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     WsLayout L;
+    const size_t np = (size_t)nseg_pad(nseg_of(V));
     size_t o = 256;
     L.counters = o;
-    o = up256(o + size_t(B) * 4);
+    o = (o + size_t(B) * 4 + 7) & ~size_t(7);
+    L.rowarg = o;
+    o = up256(o + size_t(R) * 8);
     L.stats = o;
     o = up256(o + size_t(R) * sizeof(RowStat));
     L.pq = o;
     o = up256(o + size_t(R > B ? R - B : 0) * 8);
-    L.lists = o;
-    o = up256(o + size_t(R) * LCAP * 8);
+    L.prep = o;
+    o = up256(o + size_t(R) * 640);
+    L.gstats = o;
+    o = up256(o + size_t(R) * np * 12);
     L.timing = o;
 #ifdef SV_TIMING
-    o = up256(o + size_t(R) * NTIME * 8);
+    o = up256(o + size_t(R) * PMAX * NTIME * 8);
 #endif
     L.total = o;
     return L;
@@ -127,14 +149,18 @@ struct Args {
     int32_t *out_tok;
     int32_t *acc;
     float *out_pq;            // may be NULL
-    int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] row claim counter
+    int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] work claim counter
     int32_t *counters;
+    unsigned long long *rowarg;   // persistent kernel: greedy rows' (max key, ~lowest position)
+    float *gstats;            // per-row segment statistics [R][3][npad] (stream -> select kernel)
+    int4 *prep;               // per-row prepared context, 640 B each (stream -> select kernel)
     RowStat *stats;
     float *pq;
-    int32_t *lists;
     unsigned long long *timing;   // SV_TIMING builds only
     int B, k_max, V, R, nseg;
     int pns;                  // persistent kernel: ring stages
+    int nparts;               // persistent kernel: parts each split row is cut into (1: none)
+    int nsplit;               // persistent kernel: the last nsplit rows are split
 };
 
 }  // namespace sv

@@ -13,22 +13,33 @@
 // reproducible run to run.
 #pragma once
 
+#include <stddef.h>
+
 #include "sv_block.cuh"
 
 namespace sv {
 
-// One row and its request, plus the scratch the row's selection uses.
-struct RowCtx {
-    // the row
+// One row and its request, plus the scratch the row's selection uses.  The first PREP_BYTES
+// (everything about the row that does not depend on its logits' statistics) are laid out so
+// that they can be copied verbatim between kernels.
+struct __align__(16) RowCtx {
+    // ---- the row (prepared once; PREP_BYTES)
     int r, b, i, k, r0, d0, nrows, status, active, greedy, K;
     float T, P, pres, freq, s;
-    int topk_on, topp_on, need_sum, mode, nchunks;
+    int topk_on, topp_on, need_sum, mode;
     int npen;
-    int pid[MAXK];
-    float ppen[MAXK];
-    int draft_raw[MAXK];
     int xtok;       // the row's draft token (-1 if none), its penalised target value and q value
     float zx, qx;
+    float u1;       // slot-1 uniform of the row (sampled rows: extra-token or residual draw)
+    int tix;        // index of the row's (or unit's) timing record
+    int pad0[6];
+    int pid[MAXK];
+    float ppen[MAXK];
+    // ---- stream kernel: the work unit
+    int c0, c1;     // chunks [c0, c1) of the row form this work unit
+    int part;       // part index and number of parts of the unit's row (1: streamed whole)
+    int nparts;
+    int draft_raw[MAXK];
     // selection scratch
     float m;
     float redf[16];
@@ -40,8 +51,11 @@ struct RowCtx {
     long long sel_below;
     unsigned long long sel_mass;
     double sel_target;
-    int last, a, tok, need_resid;
+    int last, a, tok, need_resid, plast;
 };
+
+constexpr int PREP_BYTES = 32 * 4 + 2 * MAXK * 4;
+static_assert(offsetof(RowCtx, pid) == 128 && offsetof(RowCtx, c0) == PREP_BYTES, "RowCtx prepared prefix");
 
 // Records a device-data error: the first code wins; the lowest request index is kept.
 __device__ __forceinline__ void record_error(const Args &A, int code, int b) {
@@ -124,6 +138,8 @@ __device__ __forceinline__ void locate_row(const Args &A, RowCtx &S, int r) {
     }
     if (lane == 0) {
         S.r = r;
+        S.tix = r;
+        S.part = 0;
         S.r0 = r0;
         S.nrows = nrows;
         S.i = r - r0;
@@ -254,6 +270,7 @@ __device__ __forceinline__ void prefetch_draft(const Args &A, RowCtx &S, const E
     S.xtok = x;
     S.zx = zx;
     S.qx = qx;
+    S.u1 = (S.active && !S.greedy) ? __ldg(A.uni + (size_t)S.r * 2 + 1) : 0.f;
 }
 
 // Loads and penalises the 8 values of this lane in segment seg (global memory).
@@ -482,7 +499,7 @@ __device__ uint32_t select_bound16(const G &g, RowCtx &S, const float *vals, int
             for (int d = g.t; d < 256; d += G::kThreads) cnt[d] = 0;
             g.sync();
             for (int j = g.t; j < n; j += G::kThreads) {
-                uint32_t key = fkey(vals[j]);
+                const uint32_t key = fkey(vals[j]);
                 if ((key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & 255u], 1u);
             }
             g.sync();

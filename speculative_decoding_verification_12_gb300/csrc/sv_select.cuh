@@ -42,7 +42,6 @@ __device__ __forceinline__ Scratch carve_scratch(unsigned char *p, int nsegp) {
     return c;
 }
 __host__ __device__ inline size_t scratch_bytes(int nsegp) { return size_t(2) * nsegp * 4 + size_t(CAP) * 16; }
-__host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
 
 #ifdef SV_TIMING
 #define SV_MARK(A, r, j)                                                           \
@@ -167,22 +166,55 @@ __device__ __forceinline__ int warp_list_residual(const int *ltok, const float *
     return j >= 0 ? ltok[j] : -1;
 }
 
+// Appends j to list[] for each lane where `take` holds (one atomic per warp); the whole warp
+// must call it.
+__device__ __forceinline__ void warp_append(int *list, int *count, bool take, int j) {
+    const unsigned bal = __ballot_sync(0xffffffffu, take);
+    if (!bal) return;
+    const int lane = lane_id();
+    int base = 0;
+    if (lane == 0) base = atomicAdd(count, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (take) list[base + __popc(bal & ((1u << lane) - 1u))] = j;
+}
+
+// Token id of the first of the 8 elements at `base` (raw, penalties applied) equal to target,
+// or -1.  One thread.
+template <typename E>
+__device__ __forceinline__ int first_in_raw(const RowCtx &S, const Raw8<E> &raw, int base, int V, float target) {
+    float v[8];
+    unpack8(raw, v);
+    for (int h = 0; h < S.npen; h++) {
+        const int d = S.pid[h] - base;
+#pragma unroll
+        for (int t = 0; t < 8; t++)
+            if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
+    }
+    int pos = -1;
+#pragma unroll
+    for (int t = 7; t >= 0; t--)
+        if (v[t] == target && base + t < V) pos = base + t;
+    return pos;
+}
+
 // Kept set of a sampled row from the top-k candidates.  Returns false on candidate overflow.
 template <typename E, bool VEC, class G>
 __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const Scratch &X, const E *row,
                                      const SegStats &o, RowStat &st, bool want_bonus) {
     const int warp = g.warp(), lane = g.lane();
-    const int V = A.V, nseg = A.nseg, K = S.K, row_idx = S.r;
+    const int V = A.V, nseg = A.nseg, K = S.K, row_idx = S.r, tix = S.tix;
+    (void)tix;
     const float m = S.m, s = S.s;
     const float *segA = o.mx;
     // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
-    SV_MARK(A, row_idx, 16);
+    SV_MARK(A, tix, 16);
     uint32_t tkey = 0;
     if (nseg >= K) tkey = select_bound16(g, S, segA, nseg, K, X.hcnt, o.hist);
-    SV_MARK(A, row_idx, 17);
+    SV_MARK(A, tix, 17);
     // Segments whose max reaches the bound.  When a segment's second value is below it, its
-    // max is its only candidate: the lane holding it is known, so one 16-byte load finds the
-    // token.  Segments with two or more candidates are re-read whole.
+    // max is its only candidate and the lane holding it is known: one 16-byte load finds the
+    // token.  Segments with two or more candidates are re-read whole.  Lists are compacted
+    // with warp ballots; both kinds of load go out before any is consumed.
     int *segl = reinterpret_cast<int *>(X.segX);
     int *single = reinterpret_cast<int *>(X.segY);
     if (g.t == 0) {
@@ -191,29 +223,62 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
         S.n2 = 0;
     }
     g.sync();
-    for (int j = g.t; j < nseg; j += G::kThreads) {
-        if (fkey(segA[j]) < tkey) continue;
-        if (fkey(o.b[j]) < tkey) single[atomicAdd(&S.n2, 1)] = j;
-        else segl[atomicAdd(&S.nsel, 1)] = j;
+    for (int j0 = warp * 32; j0 < nseg; j0 += G::kThreads) {
+        const int j = j0 + lane;
+        const bool cand = j < nseg && fkey(segA[j]) >= tkey;
+        const bool one = cand && fkey(o.b[j]) < tkey;
+        warp_append(single, &S.n2, one, j);
+        warp_append(segl, &S.nsel, cand && !one, j);
     }
     g.sync();
-    const int nsingle = S.n2;
-    for (int jj = g.t; jj < nsingle; jj += G::kThreads) {
-        const int j = single[jj];
-        const int tok = find_in_lane<E, VEC>(S, row, V, j, o.lane[j], segA[j]);
-        if (tok >= 0) {
-            const int pos = atomicAdd(&S.ncand, 1);
-            if (pos < CAP) X.cand[pos] = ((unsigned long long)fkey(segA[j]) << 32) | (uint32_t)(~(uint32_t)tok);
-        } else {
-            segl[atomicAdd(&S.nsel, 1)] = j;
+    const int nsingle = S.n2, nmulti = S.nsel;
+    SV_MARK(A, tix, 18);
+    constexpr int U = sizeof(E) == 2 ? 2 : 1;
+    // first round: one single per thread and U multi segments per warp in flight together
+    Raw8<E> sraw;
+    int sj = -1;
+    if (g.t < nsingle) {
+        sj = single[g.t];
+        sraw = load_raw8<VEC>(row, sj * SEG + o.lane[sj] * 8, V);
+    }
+    Raw8<E> raw[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+        const int j = warp + u * G::kWarps;
+        if (j < nmulti) raw[u] = load_raw8<VEC>(row, segl[j] * SEG + lane * 8, V);
+    }
+    for (int jj0 = 0; jj0 < nsingle; jj0 += G::kThreads) {
+        if (jj0 > 0) {
+            sj = jj0 + g.t < nsingle ? single[jj0 + g.t] : -1;
+            if (sj >= 0) sraw = load_raw8<VEC>(row, sj * SEG + o.lane[sj] * 8, V);
+        }
+        int tok = -1;
+        if (sj >= 0) tok = first_in_raw(S, sraw, sj * SEG + o.lane[sj] * 8, V, segA[sj]);
+        // a single whose value was not found (cannot happen with consistent statistics) is
+        // appended to the multi list, after the segments already in flight
+        warp_append(segl, &S.nsel, sj >= 0 && tok < 0, sj);
+        const bool ok = sj >= 0 && tok >= 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        int base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&S.ncand, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+        if (ok && base < CAP) X.cand[base] = ((unsigned long long)fkey(segA[sj]) << 32) | (uint32_t)(~(uint32_t)tok);
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+        const int j = warp + u * G::kWarps;
+        if (j < nmulti) {
+            const int seg = segl[j];
+            float v[8];
+            unpack8(raw[u], v);
+            patch_seg(S, seg * SEG, v);
+            append_candidates(S, X.cand, seg, v, tkey, V);
         }
     }
     g.sync();
+    // further rounds: multi segments beyond the first U per warp (and any fallbacks)
     const int nsel = S.nsel;
-    SV_MARK(A, row_idx, 18);
-    constexpr int U = sizeof(E) == 2 ? 8 : 4;
-    for (int j0 = warp; j0 < nsel; j0 += G::kWarps * U) {
-        Raw8<E> raw[U];
+    for (int j0 = warp + U * G::kWarps; j0 < nsel; j0 += G::kWarps * U) {
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const int j = j0 + u * G::kWarps;
@@ -231,9 +296,18 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             }
         }
     }
+    // fallbacks appended after the first round's multi segments but inside it
+    if (nsel > nmulti && nmulti < U * G::kWarps) {
+        for (int j0 = nmulti + warp; j0 < min(nsel, U * G::kWarps); j0 += G::kWarps) {
+            const int seg = segl[j0];
+            float v[8];
+            seg_values<E, VEC>(S, row, V, seg, v);
+            append_candidates(S, X.cand, seg, v, tkey, V);
+        }
+    }
     g.sync();
     const int n = S.ncand;
-    SV_MARK(A, row_idx, 19);
+    SV_MARK(A, tix, 19);
     if (n > CAP || n < 1) return false;
 
     if (n <= WCAP) {
@@ -246,10 +320,10 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             srt[rk] = c;
         }
         g.sync();
-        SV_MARK(A, row_idx, 20);
+        SV_MARK(A, tix, 20);
         if (warp == 0) warp_cut(S, srt, n, K, m, s, S.topp_on, S.P);
         g.sync();
-        SV_MARK(A, row_idx, 21);
+        SV_MARK(A, tix, 21);
         const int n2 = S.n2;
         const float Z = S.zk;
         st.Z = Z;
@@ -269,15 +343,13 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             lw[rk] = weight(key2f((uint32_t)(srt[j] >> 32)), m, s);
         }
         g.sync();
-        int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
-        for (int j = g.t; j < n2; j += G::kThreads) L[j] = make_int2(ltok[j], __float_as_int(lw[j]));
-        SV_MARK(A, row_idx, 22);
+        SV_MARK(A, tix, 22);
         // warp 0: the extra-token draw (last row); warp 1 (or 0): the residual draw should the
         // row's draft be rejected, with q gathered on the kept list
         const bool want_resid = S.i < S.k;
         const int wres = G::kWarps > 1 ? 1 : 0;
         if (want_bonus && warp == 0) {
-            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            const float u = S.u1;
             float w8[8];
 #pragma unroll
             for (int t = 0; t < 8; t++) w8[t] = (lane * 8 + t < n2) ? lw[lane * 8 + t] : 0.f;
@@ -285,7 +357,7 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             if (lane == 0) S.tok = j >= 0 ? ltok[j] : -1;
         }
         if (want_resid && warp == wres) {
-            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            const float u = S.u1;
             const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
             const int t = warp_list_residual(ltok, lw, n2, st.invZ, qrow, u);
             if (lane == 0) S.a = t;
@@ -293,7 +365,7 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
         g.sync();
         if (want_bonus) st.bonus = S.tok;
         if (want_resid) st.resid = S.a;
-        SV_MARK(A, row_idx, 23);
+        SV_MARK(A, tix, 23);
         return true;
     }
 
@@ -342,13 +414,8 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
         g_sort_desc(g, X.cand, np2);
         for (int j = g.t; j < n2; j += G::kThreads) X.aux[j] = weight(key2f((uint32_t)X.cand[j]), m, s);
         g.sync();
-        if (n2 <= LCAP) {
-            int2 *L = reinterpret_cast<int2 *>(A.lists + (size_t)row_idx * LCAP * 2);
-            for (int j = g.t; j < n2; j += G::kThreads)
-                L[j] = make_int2((int32_t)(~(uint32_t)(X.cand[j] >> 32)), __float_as_int(X.aux[j]));
-        }
         if (want_bonus) {
-            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            const float u = S.u1;
             int j = draw_small(g, X.aux, X.aux2, n2, u, S);
             st.bonus = j >= 0 ? (int32_t)(~(uint32_t)(X.cand[j] >> 32)) : -1;
         }
@@ -358,7 +425,7 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             for (int j = g.t; j < n2; j += G::kThreads) ltok[j] = (int)(~(uint32_t)(X.cand[j] >> 32));
             g.sync();
             if (warp == 0) {
-                const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+                const float u = S.u1;
                 const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
                 const int t = warp_list_residual(ltok, X.aux, n2, st.invZ, qrow, u);
                 if (lane == 0) S.a = t;
@@ -392,7 +459,7 @@ __device__ void kept_by_select(const G &g, const Args &A, RowCtx &S, const Scrat
     st.kind = KIND_THRESH;
     st.nlist = 0;
     if (want_bonus) {
-        const float u = __ldg(A.uni + (size_t)S.r * 2 + 1);
+        const float u = S.u1;
         st.bonus = draw_by_segments<E, VEC, false>(g, S, row, nullptr, V, nseg, X.segY, u, wk);
     }
 }
@@ -401,7 +468,8 @@ __device__ void kept_by_select(const G &g, const Args &A, RowCtx &S, const Scrat
 // and weight sums (segB, for rows with no filter); writes the row's RowStat, kept list and
 // (p, q) of its draft.  segA/segB are consumed.
 template <typename E, bool VEC, class G>
-__device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &X, const SegStats &o) {
+__device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &X, const SegStats &o,
+                           const unsigned long long *argkey = nullptr) {
     float *segA = o.mx, *segB = o.b;
     const int V = A.V, nseg = A.nseg, row_idx = S.r;
     const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)row_idx * V;
@@ -411,15 +479,26 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
     const bool sampled = !S.greedy;
     const bool want_bonus = sampled && S.i == S.k;
     const float s = S.s;
-    float mx = -INFINITY;
-    for (int j = g.t; j < nseg; j += G::kThreads) mx = fmaxf(mx, segA[j]);
-    const float m = g_max(g, mx, S.redf);
+    float m;
+    if (!sampled && argkey) {
+        // greedy row whose streamers folded (max, lowest position) into one key
+        const unsigned long long key = __ldcg(argkey);
+        const uint32_t idx = ~(uint32_t)key;
+        m = key2f((uint32_t)(key >> 32));
+        st.argmax = idx < (uint32_t)V ? (int)idx : 0;   // an all -inf row: token 0
+    } else {
+        float mx = -INFINITY;
+        for (int j = g.t; j < nseg; j += G::kThreads) mx = fmaxf(mx, segA[j]);
+        m = g_max(g, mx, S.redf);
+    }
     if (g.t == 0) S.m = m;
     g.sync();
     st.m = m;
     st.s = s;
 
-    if (!sampled) {
+    if (!sampled && argkey) {
+        st.kind = KIND_GREEDY;
+    } else if (!sampled) {
         // greedy: lowest id of the maximum -- the first segment holding it, the lowest lane of
         // that segment holding it (recorded while streaming), then the first slot of the lane
         int first = 0x7fffffff;
@@ -446,7 +525,7 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
         st.invZ = __frcp_rn(Z);
         st.kind = KIND_FULL;
         if (want_bonus) {
-            const float u = __ldg(A.uni + (size_t)row_idx * 2 + 1);
+            const float u = S.u1;
             WKept wk{m, s, 0u};
             st.bonus = draw_by_segments<E, VEC, false>(g, S, row, nullptr, V, nseg, segB, u, wk);
         }
@@ -455,7 +534,7 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
         if (S.mode == MODE_TOP2) done = kept_from_candidates<E, VEC>(g, A, S, X, row, o, st, want_bonus);
         if (!done) kept_by_select<E, VEC>(g, A, S, X, row, st, want_bonus);
     }
-    SV_MARK(A, row_idx, 3);
+    SV_MARK(A, S.tix, 3);
 
     // the draft of this row: p(x_i) and q(x_i) (prefetched while the row streamed)
     if (g.t == 0 && S.i < S.k) {
@@ -638,7 +717,7 @@ __device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, R
         __threadfence();
         finalize<E, VEC, QVEC>(g, A, S, X);
 #ifdef SV_TIMING
-        if (g.t == 0) A.timing[(size_t)S.r * NTIME + 7] = 1;
+        if (g.t == 0) A.timing[(size_t)S.tix * NTIME + 7] = 1;
 #endif
     }
     g.sync();

@@ -59,6 +59,81 @@ __device__ __forceinline__ void seg_from_values(const float v[8], int seg, float
     }
 }
 
+// Greedy rows: each lane keeps the largest value it has seen and where: a strictly larger value
+// is the only reason to move, since its segments arrive in token order.  For clean segments the
+// lane keeps the segment's raw elements (register selects, no branch) and finds the position
+// within them once, at the end of the unit.
+template <typename E>
+struct ArgRun {
+    float best;
+    int seg;        // segment of best (clean), or -1
+    int idx;        // token of best when it came from a dirty segment
+    Raw8<E> raw;    // the lane's elements of segment seg
+};
+
+// Offset (0..7) of the first of the lane's 8 values equal to m (IEEE equality: -0 == +0).
+template <typename E>
+__device__ __forceinline__ int first_equal8(const Raw8<E> &raw, float m) {
+    float v[8];
+    unpack8(raw, v);
+    int t = 7;
+#pragma unroll
+    for (int j = 6; j >= 0; j--)
+        if (v[j] == m) t = j;
+    return t;
+}
+
+template <typename E>
+__device__ __forceinline__ void arg_clean(const Raw8<E> &raw, int seg, ArgRun<E> &a) {
+    float m1;
+    if constexpr (sizeof(E) == 2) {
+        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw.a);
+        const __nv_bfloat162 M = __hmax2(__hmax2(p[0], p[1]), __hmax2(p[2], p[3]));
+        m1 = fmaxf(__low2float(M), __high2float(M));
+    } else {
+        float v[8];
+        unpack8(raw, v);
+        m1 = max8(v);
+    }
+    const bool up = m1 > a.best;
+    a.best = up ? m1 : a.best;
+    a.seg = up ? seg : a.seg;
+    a.raw.a = up ? raw.a : a.raw.a;
+    if constexpr (sizeof(E) == 4) a.raw.b = up ? raw.b : a.raw.b;
+}
+
+template <typename E>
+__device__ __forceinline__ void arg_dirty(const Raw8<E> &raw, int seg, int V, const RowCtx &R, ArgRun<E> &a) {
+    float v[8];
+    unpack8(raw, v);
+    const int base = seg * SEG + lane_id() * 8;
+#pragma unroll
+    for (int t = 0; t < 8; t++)
+        if (base + t >= V) v[t] = -INFINITY;
+    patch_seg(R, seg * SEG, v);
+    const float m1 = max8(v);
+    if (m1 > a.best) {
+        int t = 7;
+#pragma unroll
+        for (int j = 6; j >= 0; j--)
+            if (v[j] == m1) t = j;
+        a.best = m1;
+        a.seg = -1;
+        a.idx = base + t;
+    }
+}
+
+// Folds a warp's running argmax into the row's 64-bit key (order key of the max, then the
+// complement of the lowest position holding it): one atomicMax per warp and unit.
+template <typename E>
+__device__ __forceinline__ void arg_flush(const ArgRun<E> &a, unsigned long long *slot) {
+    const int idx = a.seg >= 0 ? a.seg * SEG + lane_id() * 8 + first_equal8<E>(a.raw, a.best) : a.idx;
+    const uint32_t k = fkey(a.best);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, k);
+    const uint32_t imin = __reduce_min_sync(0xffffffffu, k == kmax ? (uint32_t)idx : 0xffffffffu);
+    if (lane_id() == 0) atomicMax(slot, ((unsigned long long)kmax << 32) | (unsigned long long)(~imin));
+}
+
 // Clean segment: bf16 pairs reduced packed (top two of the lane's 8 in MODE_TOP2).
 template <typename E, int MODE>
 __device__ __forceinline__ void seg_clean(const Raw8<E> &raw, int seg, float s, const SegStats &o) {
@@ -115,23 +190,27 @@ struct RingPos {
 // releases the stage, then reduces them.  Returns false when a wait timed out.
 template <typename E, int MODE, bool PEN>
 __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned long long *empty,
-                                           const unsigned char *ring, int pns, RingPos &rp, int nchunks, int nseg,
+                                           const unsigned char *ring, int pns, RingPos &rp, int c0, int c1, int nseg,
                                            int V, int sw, const RowCtx &R, const SegStats &o, const uint32_t *dmask,
-                                           unsigned long long *tslot) {
+                                           unsigned long long *argslot, unsigned long long *tslot) {
     constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
     constexpr int PER = (SPC + PSTREAM - 1) / PSTREAM;
     constexpr bool EVEN = SPC % PSTREAM == 0;
     const int nfull = V / SEG;                          // segments wholly inside the row
     const float s = R.s;
     (void)tslot;
-    for (int c = 0; c < nchunks; c++) {
+    ArgRun<E> arg;
+    arg.best = -INFINITY;
+    arg.seg = -1;
+    arg.idx = 0x7fffffff;
+    for (int c = c0; c < c1; c++) {
 #ifdef SV_TIMING
         const unsigned long long tw = global_ns();
 #endif
         if (!__all_sync(0xffffffffu, mbar_wait(&full[rp.st], rp.ph))) return false;
 #ifdef SV_TIMING
-        if (lane_id() == 0 && sw == 0) {
-            if (c == 0) tslot[8] = global_ns();
+        if (tslot && lane_id() == 0 && sw == 0) {
+            if (c == c0) tslot[8] = global_ns();
             else tslot[10] += global_ns() - tw;
         }
 #endif
@@ -152,33 +231,40 @@ __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned lo
             if ((!EVEN && jj >= SPC) || seg >= nseg) continue;
             bool clean = seg < nfull;
             if constexpr (PEN) clean = clean && !((dmask[seg >> 5] >> (seg & 31)) & 1u);
-            if (clean) seg_clean<E, MODE>(raw[u], seg, s, o);
-            else seg_dirty<E, MODE>(raw[u], seg, V, R, s, o);
+            if constexpr (MODE == MODE_ARG) {
+                if (clean) arg_clean<E>(raw[u], seg, arg);
+                else arg_dirty<E>(raw[u], seg, V, R, arg);
+            } else {
+                if (clean) seg_clean<E, MODE>(raw[u], seg, s, o);
+                else seg_dirty<E, MODE>(raw[u], seg, V, R, s, o);
+            }
         }
     }
+    if constexpr (MODE == MODE_ARG) arg_flush(arg, argslot);
     return true;
 }
 
 // Dispatch on the row's statistics mode and on whether it has penalised tokens.
 template <typename E>
 __device__ __forceinline__ bool stream_row_any(unsigned long long *full, unsigned long long *empty,
-                                               const unsigned char *ring, int pns, RingPos &rp, int nchunks,
+                                               const unsigned char *ring, int pns, RingPos &rp, int c0, int c1,
                                                int nseg, int V, int sw, const RowCtx &R, const SegStats &o,
-                                               const uint32_t *dmask, unsigned long long *tslot) {
+                                               const uint32_t *dmask, unsigned long long *argslot,
+                                               unsigned long long *tslot) {
     const int mode = R.mode;
     if (R.npen > 0) {
         switch (mode) {
-            case MODE_ARG: return stream_row<E, MODE_ARG, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
-            case MODE_TOP2: return stream_row<E, MODE_TOP2, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
-            case MODE_SUM: return stream_row<E, MODE_SUM, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
-            default: return stream_row<E, MODE_MAX, true>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+            case MODE_ARG: return stream_row<E, MODE_ARG, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+            case MODE_TOP2: return stream_row<E, MODE_TOP2, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+            case MODE_SUM: return stream_row<E, MODE_SUM, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+            default: return stream_row<E, MODE_MAX, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
         }
     }
     switch (mode) {
-        case MODE_ARG: return stream_row<E, MODE_ARG, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
-        case MODE_TOP2: return stream_row<E, MODE_TOP2, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
-        case MODE_SUM: return stream_row<E, MODE_SUM, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
-        default: return stream_row<E, MODE_MAX, false>(full, empty, ring, pns, rp, nchunks, nseg, V, sw, R, o, dmask, tslot);
+        case MODE_ARG: return stream_row<E, MODE_ARG, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+        case MODE_TOP2: return stream_row<E, MODE_TOP2, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+        case MODE_SUM: return stream_row<E, MODE_SUM, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+        default: return stream_row<E, MODE_MAX, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
     }
 }
 

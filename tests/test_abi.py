@@ -46,8 +46,10 @@ def test_workspace_size(libsv):
     a = libsv.sv_workspace_bytes(256, 1280, 128256)
     b = libsv.sv_workspace_bytes(512, 2560, 151936)
     assert 0 < a < b and a % 256 == 0
-    # per row: statistics + a kept list; per request: a counter
-    assert a < 1280 * 4096 + 256 * 64 + 65536
+    # per row: statistics, a kept list and 12 bytes per (padded) 256-token segment; per
+    # request: a counter
+    nsegp = ((128256 + 255) // 256 + 31) // 32 * 32
+    assert a < 1280 * (4096 + 12 * nsegp) + 256 * 64 + 65536
 
 
 def test_host_checks_reject_bad_calls(libsv):
