@@ -26,6 +26,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "verify rows/s and achieved HBM GB/s (% of GB300 roofline) vs CPU oracle"
+
+# DRAM bytes (read + write) of one whole spec_verify call, both kernels, from the ncu capture
+# summarised in profiles/stream_select_zipf_b160_ncu_full.md (160 requests, scaled by rows to
+# the full batch).  Valid only for the kernels as captured; None elsewhere.
+TRAFFIC_PER_CALL = {"b256_k4_v128256_bf16_zipf": 353.9e6}
 DEFAULT_WORKLOAD = "b256_k4_v128256_bf16_zipf"
 
 
@@ -202,7 +207,7 @@ def run_ours(args):
     sv.lib()
 
     sp = W.spec(args.workload)
-    w = W.make(args.workload)           # every rank verifies its own full batch (weak scaling)
+    w = W.make(args.workload, requests=None if args.requests is None else list(range(args.requests)))
     db = DeviceBatch.from_host(w, dev, want_pq=False)
     stream = torch.cuda.Stream(dev)
     copies = [(db.target_logits, db.draft_probs)]
@@ -295,7 +300,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": sp.name, "B": sp.B, "k": sp.k_max, "V": sp.V, "logits": sp.dtype,
+            "config": {"workload": sp.name, "B": w.B, "k": sp.k_max, "V": sp.V, "logits": sp.dtype,
                        "top_k": 50, "top_p": 0.9, "greedy_share": 0.25, "parallelism": f"replicas x{world}",
                        "l2": f"{args.copies} rotating device copies of the inputs "
                              f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + db.draft_probs.numel() * 4) / 1e9:.2f} GB > L2)"},
@@ -305,10 +310,16 @@ def run_ours(args):
                        "tokens_per_step": float(acc.mean() + 1)},
             "bytes_per_step": nb,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": args.traffic, "peak_source": peak_kind,
-                         "kernel": "sv::verify_kernel<bf16>"},
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": args.traffic if args.traffic is not None else
+                         (TRAFFIC_PER_CALL.get(sp.name) if args.requests is None else None),
+                         "traffic_unit": "bytes per call (ncu dram read+write)",
+                         "kernel": "one spec_verify call: stream_kernel<bf16> + select_kernel (PDL-chained)",
+                         "timed": "CUDA events around whole calls on the launching stream"},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps,
+            # each spec_verify call launches the stream kernel and the select kernel (the
+            # clearing of the workspace header is a cudaMemsetAsync, not counted)
+            "gpu_launches": 2 * args.steps,
             "clocks": clk,
         }
         if not args.no_cpu_baseline and world == 1:
@@ -327,6 +338,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--requests", type=int, default=None,
+                    help="verify only the first N requests of the workload (small cases for ncu captures)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per launch of the verify kernel, if captured")
     ap.add_argument("--no-cpu-baseline", action="store_true")
