@@ -148,6 +148,35 @@ sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const fl
 sv_status spec_rollback(int32_t *kv_seq_len, const int32_t *accept_len, const int32_t *num_drafts,
                         int32_t B, void *workspace, void *stream);
 
+/*
+ * spec_verify_static -- spec_verify with a workspace that the library owns.
+ *
+ * Not part of the method: the sources verify drafts with whatever memory the serving process
+ * provides; this entry point exists for callers that cannot provide device memory for a
+ * workspace -- a host program with no device allocator of its own, or code that must not
+ * allocate on the verification path.  It allocates nothing: the workspace is a device array of
+ * SV_STATIC_WORKSPACE_BYTES (32 MiB) compiled into the library, present once per device.
+ *
+ *   Arguments, layout and results are those of spec_verify, without workspace and
+ *   workspace_bytes.
+ *   The first call on a device looks up the array's address (cudaGetSymbolAddress) with that
+ *   device current; make that first call before any stream capture begins.
+ *   A batch whose sv_workspace_bytes(B, total_rows, V) exceeds SV_STATIC_WORKSPACE_BYTES is
+ *   rejected with SV_ERR_WORKSPACE before anything is enqueued.
+ *   Every call on a device shares the one array: calls must be ordered (one stream, or events
+ *   between streams).  Two calls that overlap in time race on it and their results are
+ *   undefined.
+ *   Device-data errors still turn the affected request's outputs into -1; the sticky error word
+ *   itself stays inside the library's array.
+ */
+#define SV_STATIC_WORKSPACE_BYTES (32u << 20)
+
+sv_status spec_verify_static(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                             const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
+                             int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                             const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
+                             void *stream);
+
 /* Reads the sticky device-data error word of a workspace (synchronises the device; meant for
  * tests and debugging).  *code receives an SV_DEV_* value, *first_bad_request the lowest
  * request index that set it (-1 if none).  Returns SV_OK when no error was recorded,

@@ -543,3 +543,37 @@ extern "C" sv_status sv_read_device_error(const void *workspace, int32_t *code, 
     if (first_bad_request) *first_bad_request = h[1] ? INT_MAX - h[1] : -1;
     return h[0] ? SV_ERR_DEVICE_DATA : SV_OK;
 }
+
+// ------------------------------------------------------------------------------------------
+// spec_verify_static: spec_verify on a workspace the library owns (a file-scope device array),
+// for callers that cannot hand the library device memory.  Nothing is allocated: the array is
+// part of the loaded module.  Every call shares it, so calls must not overlap in time.
+// ------------------------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char sv_static_workspace[SV_STATIC_WORKSPACE_BYTES];
+
+extern "C" sv_status spec_verify_static(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                                        const int32_t *draft_tokens, const int32_t *num_drafts,
+                                        const int32_t *row_offsets, int32_t B, int32_t k_max, int32_t V,
+                                        int32_t total_rows, sv_params params, const float *uniforms,
+                                        int32_t *out_tokens, int32_t *accept_len, float *out_pq, void *stream) {
+    // the array's address on each device, looked up once with that device current
+    static void *base[64] = {nullptr};
+    if (B < 1 || k_max < 0 || V < 1 || total_rows < B) return SV_ERR_INVALID_ARG;
+    const size_t need = sv_workspace_bytes(B, total_rows, V);
+    if (need == 0) return SV_ERR_INVALID_ARG;
+    if (need > (size_t)SV_STATIC_WORKSPACE_BYTES) return SV_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
+    if (!base[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, sv_static_workspace) != cudaSuccess || !p) return SV_ERR_CUDA;
+        base[dev] = p;
+    }
+    // spec_verify clears what must start at zero (error word, claim and arrival counters,
+    // greedy argmax keys) on `stream` before its kernels run
+    return spec_verify(target_logits, logits_dtype, draft_probs, draft_tokens, num_drafts, row_offsets, B, k_max, V,
+                       total_rows, params, uniforms, out_tokens, accept_len, out_pq, base[dev],
+                       (size_t)SV_STATIC_WORKSPACE_BYTES, stream);
+}
