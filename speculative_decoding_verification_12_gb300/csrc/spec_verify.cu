@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
 // One CTA per row: the row's kept set, draws and draft probabilities from the statistics the
 // stream kernel wrote; the request's last row finalises the request.
 template <typename E, bool QVEC>
-__global__ void __launch_bounds__(SELT, 4) select_kernel(const Args A) {
+__global__ void __launch_bounds__(SELT, 9) select_kernel(const Args A) {
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ RowCtx S;
     const Grp<SELT, 0> g(threadIdx.x);

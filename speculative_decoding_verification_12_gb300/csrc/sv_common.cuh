@@ -9,13 +9,14 @@ namespace sv {
 
 constexpr int SEG = 256;              // elements per segment: one warp step of 32 lanes x 8
 #ifndef SV_CAP
-#define SV_CAP 1536
+#define SV_CAP 512
 #endif
 constexpr int CAP = SV_CAP;           // candidate buffer (top-k candidates, kept lists) per group
-constexpr int KCAP = 512;             // top-k up to this goes through the candidate buffer
+constexpr int KCAP = 256;             // top-k up to this goes through the candidate buffer
 constexpr int WCAP = 256;             // candidate sets up to this are cut and drawn by one warp
 constexpr int LCAP = 256;             // kept sets up to this are drawn from as lists (KIND_LIST)
-constexpr int HB = 2048;              // radix histogram bins (11-bit digits)
+constexpr int HB = 256;               // radix histogram bins (8-bit digits, 4 rounds)
+constexpr int NRADIX = 4;             // radix rounds over a 32-bit key
 #ifndef SV_SB
 #define SV_SB 12288
 #endif

@@ -441,9 +441,9 @@ __device__ __forceinline__ void ring_values<float>(const unsigned char *buf, int
 // ------------------------------------------------------------------------------------------
 
 __device__ __forceinline__ void digit_round(int round, int &shift, int &width, uint32_t &mask) {
-    shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
-    width = round == 2 ? 10 : 11;
-    mask = round == 0 ? 0u : (round == 1 ? 0xFFE00000u : 0xFFFFFC00u);
+    shift = 24 - 8 * round;
+    width = 8;
+    mask = round == 0 ? 0u : (0xFFFFFFFFu << (32 - 8 * round));
 }
 
 // One warp scans a count histogram from the highest bin down and finds the bin d holding the
@@ -519,7 +519,7 @@ __device__ uint32_t select_kth_row(const G &g, RowCtx &S, const E *row, int V, i
     uint32_t prefix = 0;
     long long nd = need;
     const int warp = g.warp(), lane = g.lane();
-    for (int round = 0; round < 3; round++) {
+    for (int round = 0; round < NRADIX; round++) {
         int shift, width;
         uint32_t mask;
         digit_round(round, shift, width, mask);
@@ -590,7 +590,7 @@ __device__ uint32_t select_mass_row(const G &g, RowCtx &S, const E *row, int V, 
     unsigned long long above = 0;
     double target = 0.0;
     const int warp = g.warp(), lane = g.lane();
-    for (int round = 0; round < 3; round++) {
+    for (int round = 0; round < NRADIX; round++) {
         int shift, width;
         uint32_t mask;
         digit_round(round, shift, width, mask);

@@ -178,23 +178,45 @@ __device__ __forceinline__ void warp_append(int *list, int *count, bool take, in
     if (take) list[base + __popc(bal & ((1u << lane) - 1u))] = j;
 }
 
-// Token id of the first of the 8 elements at `base` (raw, penalties applied) equal to target,
-// or -1.  One thread.
+// Appends the elements at `base` (8 raw values of one lane, penalties applied) whose key
+// reaches tkey to the candidate buffer, one thread per lane-run and one atomic per warp; base
+// < 0 contributes nothing.  Returns this thread's count.  The whole warp must call it.
 template <typename E>
-__device__ __forceinline__ int first_in_raw(const RowCtx &S, const Raw8<E> &raw, int base, int V, float target) {
+__device__ __forceinline__ int lane_candidates(RowCtx &S, unsigned long long *cand, const Raw8<E> &raw, int base,
+                                               int V, uint32_t tkey) {
+    const int lane = lane_id();
     float v[8];
     unpack8(raw, v);
-    for (int h = 0; h < S.npen; h++) {
-        const int d = S.pid[h] - base;
+    if (base >= 0) {
+        for (int h = 0; h < S.npen; h++) {
+            const int d = S.pid[h] - base;
 #pragma unroll
-        for (int t = 0; t < 8; t++)
-            if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
+            for (int t = 0; t < 8; t++)
+                if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
+        }
     }
-    int pos = -1;
+    int c = 0;
 #pragma unroll
-    for (int t = 7; t >= 0; t--)
-        if (v[t] == target && base + t < V) pos = base + t;
-    return pos;
+    for (int t = 0; t < 8; t++) c += (base >= 0 && base + t < V && fkey(v[t]) >= tkey) ? 1 : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = 0;
+    if (lane == 0 && total) pos = atomicAdd(&S.ncand, total);
+    pos = __shfl_sync(0xffffffffu, pos, 0) + incl - c;
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const uint32_t key = fkey(v[t]);
+        if (base >= 0 && base + t < V && key >= tkey) {
+            if (pos < CAP) cand[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)(base + t));
+            pos++;
+        }
+    }
+    return c;
 }
 
 // Kept set of a sampled row from the top-k candidates.  Returns false on candidate overflow.
@@ -252,17 +274,14 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             sj = jj0 + g.t < nsingle ? single[jj0 + g.t] : -1;
             if (sj >= 0) sraw = load_raw8<VEC>(row, sj * SEG + o.lane[sj] * 8, V);
         }
-        int tok = -1;
-        if (sj >= 0) tok = first_in_raw(S, sraw, sj * SEG + o.lane[sj] * 8, V, segA[sj]);
-        // a single whose value was not found (cannot happen with consistent statistics) is
+        // every element of lane `at` that reaches the bound is a candidate (the segment's max
+        // among them); the rest of the segment lies below the bound
+        int found = 0;
+        if (sj >= 0) found = lane_candidates(S, X.cand, sraw, sj * SEG + o.lane[sj] * 8, V, tkey);
+        else lane_candidates(S, X.cand, sraw, -1, V, tkey);
+        // a single with no element at the bound (cannot happen with consistent statistics) is
         // appended to the multi list, after the segments already in flight
-        warp_append(segl, &S.nsel, sj >= 0 && tok < 0, sj);
-        const bool ok = sj >= 0 && tok >= 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, ok);
-        int base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&S.ncand, __popc(bal));
-        base = __shfl_sync(0xffffffffu, base, 0) + __popc(bal & ((1u << lane) - 1u));
-        if (ok && base < CAP) X.cand[base] = ((unsigned long long)fkey(segA[sj]) << 32) | (uint32_t)(~(uint32_t)tok);
+        warp_append(segl, &S.nsel, sj >= 0 && found == 0, sj);
     }
 #pragma unroll
     for (int u = 0; u < U; u++) {

@@ -11,15 +11,16 @@
 
 namespace sv {
 
-// Warp result of one segment from each lane's top value m1 (and second value m2): lane 0
-// writes the max, the lowest lane holding it, and in MODE_TOP2 the segment's second value.
+// Warp result of one segment from each lane's top value m1: lane 0 writes the max, the lowest
+// lane holding it and, in MODE_TOP2, the largest value held by any other lane (every element
+// outside lane `at` is at most that value).
 template <int MODE>
-__device__ __forceinline__ void seg_emit(int seg, float m1, float m2, const SegStats &o) {
+__device__ __forceinline__ void seg_emit(int seg, float m1, const SegStats &o) {
     const float mx = redux_max(m1);
     if constexpr (MODE == MODE_ARG || MODE == MODE_TOP2) {
         const int at = __ffs(__ballot_sync(0xffffffffu, m1 == mx)) - 1;
         float sec = 0.f;
-        if constexpr (MODE == MODE_TOP2) sec = redux_max(lane_id() == at ? m2 : m1);
+        if constexpr (MODE == MODE_TOP2) sec = redux_max(lane_id() == at ? -INFINITY : m1);
         if (lane_id() == 0) {
             o.mx[seg] = mx;
             o.lane[seg] = at;
@@ -46,16 +47,8 @@ __device__ __forceinline__ void seg_from_values(const float v[8], int seg, float
             o.mx[seg] = mx;
             o.b[seg] = sum;
         }
-    } else if constexpr (MODE == MODE_TOP2) {
-        float m1 = v[0], m2 = -INFINITY;
-#pragma unroll
-        for (int t = 1; t < 8; t++) {
-            m2 = fmaxf(m2, fminf(m1, v[t]));
-            m1 = fmaxf(m1, v[t]);
-        }
-        seg_emit<MODE>(seg, m1, m2, o);
     } else {
-        seg_emit<MODE>(seg, max8(v), 0.f, o);
+        seg_emit<MODE>(seg, max8(v), o);
     }
 }
 
@@ -134,25 +127,13 @@ __device__ __forceinline__ void arg_flush(const ArgRun<E> &a, unsigned long long
     if (lane_id() == 0) atomicMax(slot, ((unsigned long long)kmax << 32) | (unsigned long long)(~imin));
 }
 
-// Clean segment: bf16 pairs reduced packed (top two of the lane's 8 in MODE_TOP2).
+// Clean segment: bf16 pairs reduced packed.
 template <typename E, int MODE>
 __device__ __forceinline__ void seg_clean(const Raw8<E> &raw, int seg, float s, const SegStats &o) {
     if constexpr (sizeof(E) == 2 && MODE != MODE_SUM) {
         const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw.a);
-        const __nv_bfloat162 a = __hmax2(p[0], p[1]), c = __hmax2(p[2], p[3]);
-        const __nv_bfloat162 M = __hmax2(a, c);
-        if constexpr (MODE == MODE_TOP2) {
-            const __nv_bfloat162 b = __hmin2(p[0], p[1]), d = __hmin2(p[2], p[3]);
-            const __nv_bfloat162 S2 = __hmax2(__hmin2(a, c), __hmax2(b, d));
-            // fold the two halves: top = max of the maxima, second = max(min of the maxima,
-            // the halves' seconds)
-            const __nv_bfloat162 Ms = __lowhigh2highlow(M), Ss = __lowhigh2highlow(S2);
-            const __nv_bfloat162 T1 = __hmax2(M, Ms);
-            const __nv_bfloat162 T2 = __hmax2(__hmin2(M, Ms), __hmax2(S2, Ss));
-            seg_emit<MODE>(seg, __low2float(T1), __low2float(T2), o);
-        } else {
-            seg_emit<MODE>(seg, fmaxf(__low2float(M), __high2float(M)), 0.f, o);
-        }
+        const __nv_bfloat162 M = __hmax2(__hmax2(p[0], p[1]), __hmax2(p[2], p[3]));
+        seg_emit<MODE>(seg, fmaxf(__low2float(M), __high2float(M)), o);
     } else {
         float v[8];
         unpack8(raw, v);
