@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
 // One CTA per row: the row's kept set, draws and draft probabilities from the statistics the
 // stream kernel wrote; the request's last row finalises the request.
 template <typename E, bool QVEC>
-__global__ void __launch_bounds__(SELT, 9) select_kernel(const Args A) {
+__global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_kernel(const Args A) {
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ RowCtx S;
     const Grp<SELT, 0> g(threadIdx.x);
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(SELT, 9) select_kernel(const Args A) {
     // the row's prepared context and segment statistics, in one round of loads
     {
         const int4 *src = A.prep + (size_t)r * (PREP_BYTES / 16);
-        if (g.t < PREP_BYTES / 16) reinterpret_cast<int4 *>(&S)[g.t] = __ldcg(src + g.t);
+        for (int t = g.t; t < PREP_BYTES / 16; t += SELT) reinterpret_cast<int4 *>(&S)[t] = __ldcg(src + t);
         const float4 *gs = reinterpret_cast<const float4 *>(A.gstats + (size_t)r * 3 * np);
         for (int t = g.t; t < 3 * np / 4; t += SELT) reinterpret_cast<float4 *>(sb)[t] = __ldcg(gs + t);
     }

@@ -46,7 +46,10 @@ constexpr int SCTA = SV_SCTA;
 constexpr int PSTREAM = SV_PSTREAM;
 constexpr int SPLIT_PARTS = SV_SPLIT_PARTS;
 constexpr int ST = 32 * (2 + PSTREAM);
-constexpr int SELT = 128;
+#ifndef SV_SELT
+#define SV_SELT 128
+#endif
+constexpr int SELT = SV_SELT;         // threads per select CTA (one row each)
 #ifndef SV_PNS_MAX
 #define SV_PNS_MAX 16
 #endif

@@ -144,9 +144,10 @@ __device__ __forceinline__ void warp_cut(RowCtx &S, const unsigned long long *sr
 
 // One warp: the residual draw of a LIST row should its draft be rejected -- r = max(0, p - q)
 // over the kept list (p is zero elsewhere, so r is too), q gathered from the draft row; an
-// empty residual falls back to p.  ltok/lw: the list in token order (n <= WCAP).
+// empty residual falls back to p.  ltok/lw: the list in token order (n <= WCAP); lq, when
+// given, holds q at those tokens (else q is gathered from qrow).
 __device__ __forceinline__ int warp_list_residual(const int *ltok, const float *lw, int n, float invZ,
-                                                  const float *qrow, float u) {
+                                                  const float *qrow, float u, const float *lq = nullptr) {
     const int lane = lane_id();
     float pw[8], rw[8];
     int tk[8];
@@ -158,7 +159,7 @@ __device__ __forceinline__ int warp_list_residual(const int *ltok, const float *
     }
 #pragma unroll
     for (int t = 0; t < 8; t++) {
-        const float q = tk[t] >= 0 ? __ldg(qrow + tk[t]) : 0.f;
+        const float q = tk[t] >= 0 ? (lq ? lq[lane * 8 + t] : __ldg(qrow + tk[t])) : 0.f;
         rw[t] = tk[t] >= 0 ? fmaxf(__fsub_rn(pw[t], q), 0.f) : 0.f;
     }
     int j = warp_draw8(rw, n, u);
@@ -330,13 +331,20 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
     if (n > CAP || n < 1) return false;
 
     if (n <= WCAP) {
-        // rank sort by (value desc, token asc): keys are distinct, so ranks are a permutation
+        // rank sort by (value desc, token asc): keys are distinct, so ranks are a permutation.
+        // q of each candidate (the residual needs it on the kept list) is gathered meanwhile.
         unsigned long long *srt = X.sorted;
+        const bool want_resid = S.i < S.k;
+        const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
+        float *qs = X.aux2;           // q at sorted positions
+        float *lq = X.aux2 + WCAP;    // q in token order
         for (int j = g.t; j < n; j += G::kThreads) {
             const unsigned long long c = X.cand[j];
+            const float qv = want_resid ? __ldg(qrow + (int)(~(uint32_t)c)) : 0.f;
             int rk = 0;
             for (int i = 0; i < n; i++) rk += X.cand[i] > c ? 1 : 0;
             srt[rk] = c;
+            qs[rk] = qv;
         }
         g.sync();
         SV_MARK(A, tix, 20);
@@ -360,12 +368,12 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             for (int i = 0; i < n2; i++) rk += (~(uint32_t)srt[i]) < tj ? 1 : 0;
             ltok[rk] = (int)tj;
             lw[rk] = weight(key2f((uint32_t)(srt[j] >> 32)), m, s);
+            lq[rk] = qs[j];
         }
         g.sync();
         SV_MARK(A, tix, 22);
         // warp 0: the extra-token draw (last row); warp 1 (or 0): the residual draw should the
         // row's draft be rejected, with q gathered on the kept list
-        const bool want_resid = S.i < S.k;
         const int wres = G::kWarps > 1 ? 1 : 0;
         if (want_bonus && warp == 0) {
             const float u = S.u1;
@@ -376,9 +384,7 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             if (lane == 0) S.tok = j >= 0 ? ltok[j] : -1;
         }
         if (want_resid && warp == wres) {
-            const float u = S.u1;
-            const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
-            const int t = warp_list_residual(ltok, lw, n2, st.invZ, qrow, u);
+            const int t = warp_list_residual(ltok, lw, n2, st.invZ, qrow, S.u1, lq);
             if (lane == 0) S.a = t;
         }
         g.sync();
@@ -612,23 +618,35 @@ __device__ __forceinline__ bool accept_test(float p, float q, float u) {
 template <typename E, bool VEC, bool QVEC, class G>
 __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
     const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
+    int *xs = reinterpret_cast<int *>(X.cand);   // the request's draft tokens, for the outputs
     if (g.warp() == 0) {
+        // one round of loads: every row's statistics, draft, (p, q) and uniforms at once; the
+        // final token is then taken from the lane that holds the stopping row
         const int lane = g.lane();
         int status = S.status;
         int a = -1, tok = -1, need = 0;
         if (status == 0) {
             const bool greedy = S.greedy;
-            bool badtok = false, baduni = false, badrow = false;
+            bool badtok = false, baduni = false, badrow = false, found = false;
             a = k;
             for (int i0 = 0; i0 <= k; i0 += 32) {
                 const int i = i0 + lane;
                 bool rej = false;
-                if (i <= k && __ldcg(&A.stats[r0 + i].kind) == KIND_FAIL) badrow = true;
+                int kind = KIND_SKIP, argm = -1, bonus = -1, resid = -1;
+                if (i <= k) {
+                    const RowStat *st = A.stats + r0 + i;
+                    kind = __ldcg(&st->kind);
+                    argm = __ldcg(&st->argmax);
+                    bonus = __ldcg(&st->bonus);
+                    resid = __ldcg(&st->resid);
+                    if (kind == KIND_FAIL) badrow = true;
+                }
                 if (i < k) {
                     const int x = __ldg(A.tokens + d0 + i);
+                    xs[i] = x;
                     if (x < 0 || x >= V) badtok = true;
                     if (greedy) {
-                        rej = x != __ldcg(&A.stats[r0 + i].argmax);
+                        rej = x != argm;
                     } else {
                         const float p = __ldcg(A.pq + (size_t)(d0 + i) * 2);
                         const float q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
@@ -640,7 +658,22 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
                     if (!(u0 >= 0.f && u0 < 1.f) || !(u1 >= 0.f && u1 < 1.f)) baduni = true;
                 }
                 const unsigned msk = __ballot_sync(0xffffffffu, rej);
-                if (msk && a == k) a = i0 + __ffs(msk) - 1;
+                // the stopping row: the first rejection, else row k (in the last chunk)
+                int stop = -1;
+                if (!found && msk) stop = __ffs(msk) - 1;
+                else if (!found && i0 + 32 > k) stop = k - i0;
+                if (stop >= 0) {
+                    found = true;
+                    a = i0 + stop;
+                    const int kind_a = __shfl_sync(0xffffffffu, kind, stop);
+                    const int argm_a = __shfl_sync(0xffffffffu, argm, stop);
+                    const int bonus_a = __shfl_sync(0xffffffffu, bonus, stop);
+                    const int resid_a = __shfl_sync(0xffffffffu, resid, stop);
+                    if (greedy) tok = argm_a;
+                    else if (a == k) tok = bonus_a;
+                    else if (kind_a == KIND_LIST) tok = resid_a;   // drawn speculatively with the row
+                    else need = 1;
+                }
             }
             badtok = __any_sync(0xffffffffu, badtok);
             baduni = __any_sync(0xffffffffu, baduni);
@@ -648,18 +681,10 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
             if (badtok) status = 2;
             else if (baduni) status = 5;
             else if (badrow) status = 7;
-            if (status == 0) {
-                if (greedy) {
-                    tok = __ldcg(&A.stats[r0 + a].argmax);
-                } else if (a == k) {
-                    tok = __ldcg(&A.stats[r0 + k].bonus);
-                } else if (__ldcg(&A.stats[r0 + a].kind) == KIND_LIST) {
-                    tok = __ldcg(&A.stats[r0 + a].resid);   // drawn speculatively with the row
-                } else {
-                    need = 1;
-                }
-            } else {
+            if (status != 0) {
                 a = -1;
+                tok = -1;
+                need = 0;
             }
         }
         if (lane == 0) {
@@ -691,7 +716,7 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
     const int a = S.a, kw = A.k_max + 1;
     for (int j = g.t; j < kw; j += G::kThreads) {
         int v = -1;
-        if (a >= 0) v = j < a ? __ldg(A.tokens + d0 + j) : (j == a ? S.tok : -1);
+        if (a >= 0) v = j < a ? xs[j] : (j == a ? S.tok : -1);
         A.out_tok[(size_t)b * kw + j] = v;
     }
     if (g.t == 0) {
@@ -727,13 +752,14 @@ template <typename E, bool VEC, bool QVEC, class G>
 __device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
     g.sync();
     if (g.t == 0) {
-        __threadfence();
-        const int old = atomicAdd(A.counters + S.b, 1);
+        // release this row's results, acquire the other rows' (the group's writes are ordered
+        // before by the barrier above)
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(A.counters + S.b) : "memory");
         S.last = (old == S.nrows - 1);
     }
     g.sync();
     if (S.last) {
-        __threadfence();
         finalize<E, VEC, QVEC>(g, A, S, X);
 #ifdef SV_TIMING
         if (g.t == 0) A.timing[(size_t)S.tix * NTIME + 7] = 1;
