@@ -243,6 +243,13 @@ __global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
                 }
                 return;
             }
+#ifdef SV_TIMING
+            if (lane == 0) {
+                A.timing[(size_t)u * NTIME + 0] = global_ns();
+                A.timing[(size_t)u * NTIME + 6] = (unsigned long long)blockIdx.x;
+                A.timing[(size_t)u * NTIME + 10] = 0;
+            }
+#endif
             int r, part, npu;
             if (u < whole) {
                 r = u;
@@ -271,6 +278,10 @@ __global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
             if (lane == 0) {
                 R.part = part;
                 R.nparts = npu;
+                R.tix = u;
+#ifdef SV_TIMING
+                A.timing[(size_t)u * NTIME + 12] = (unsigned long long)r;
+#endif
                 int c0 = 0, c1 = 0;
                 if (R.active) part_chunks(nc, npu, part, c0, c1);
                 R.c0 = c0;
@@ -300,12 +311,19 @@ __global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
             const RowCtx &R = P.rc[slot];
             if (R.r < 0) return;
             const SegStats o = stats_at(A.gstats + (size_t)R.r * 3 * np, np);
+            unsigned long long *tslot = nullptr;
+#ifdef SV_TIMING
+            tslot = A.timing + (size_t)R.tix * NTIME;
+#endif
             if (!stream_row_any<E>(P.full, P.empty, ring, PNS, rp, R.c0, R.c1, nseg, V, sw, R, o,
-                                   masks + slot * mask_words(np), A.rowarg + R.r, nullptr)) {
+                                   masks + slot * mask_words(np), A.rowarg + R.r, tslot)) {
                 if (lane == 0) sfail(A, P, R.b);
                 return;
             }
             __syncwarp();
+#ifdef SV_TIMING
+            if (lane == 0 && sw == 0) A.timing[(size_t)R.tix * NTIME + 2] = global_ns();
+#endif
             if (lane == 0) mbar_arrive(&P.rb_done[slot]);
         }
     }
@@ -322,10 +340,10 @@ __global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_ke
     const int np = nseg_pad(A.nseg);
     float *sb = reinterpret_cast<float *>(dsm);
     const Scratch X = carve_scratch(dsm + up128((size_t)3 * np * 4), np);
-    SV_MARK(A, r, 0);
+    SV_MARK(A, 4 * A.R + r, 0);
     // the stream kernel's results (and every earlier write on the stream) are visible past here
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    SV_MARK(A, r, 1);
+    SV_MARK(A, 4 * A.R + r, 1);
     // the row's prepared context and segment statistics, in one round of loads
     {
         const int4 *src = A.prep + (size_t)r * (PREP_BYTES / 16);
@@ -334,13 +352,17 @@ __global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_ke
         for (int t = g.t; t < 3 * np / 4; t += SELT) reinterpret_cast<float4 *>(sb)[t] = __ldcg(gs + t);
     }
     g.sync();
-    SV_MARK(A, r, 2);
+#ifdef SV_TIMING
+    if (g.t == 0) S.tix = 4 * A.R + r;   // the select kernel's records follow the stream kernel's
+    g.sync();
+#endif
+    SV_MARK(A, 4 * A.R + r, 2);
     if (S.b < 0) return;   // a row outside every request: nothing to count
     fail_empty_requests(g, A, S);
     if (S.active) select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
-    SV_MARK(A, r, 4);
+    SV_MARK(A, 4 * A.R + r, 4);
     arrive_and_finalize<E, true, QVEC>(g, A, S, X);
-    SV_MARK(A, r, 5);
+    SV_MARK(A, 4 * A.R + r, 5);
 }
 
 __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *nd, int B, int32_t *hdr) {

@@ -231,8 +231,9 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
     const float *segA = o.mx;
     // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
     SV_MARK(A, tix, 16);
-    uint32_t tkey = 0;
-    if (nseg >= K) tkey = select_bound16(g, S, segA, nseg, K, X.hcnt, o.hist);
+    // (for up to 8 maxima per thread select_row computed the row max and this bound together)
+    uint32_t tkey = S.cutkey;
+    if (nseg > G::kThreads * 8) tkey = nseg >= K ? select_bound16(g, S, segA, nseg, K, X.hcnt, o.hist) : 0u;
     SV_MARK(A, tix, 17);
     // Segments whose max reaches the bound.  When a segment's second value is below it, its
     // max is its only candidate and the lane holding it is known: one 16-byte load finds the
@@ -511,6 +512,12 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
         const uint32_t idx = ~(uint32_t)key;
         m = key2f((uint32_t)(key >> 32));
         st.argmax = idx < (uint32_t)V ? (int)idx : 0;   // an all -inf row: token 0
+    } else if (sampled && !S.need_sum && S.mode == MODE_TOP2 && nseg <= G::kThreads * 8) {
+        // top-k rows: the row max and the candidates' bound in one pass over the maxima
+        const uint32_t bound = max_and_bound16(g, S, segA, nseg, S.K, X.hcnt);
+        m = S.m;
+        g.sync();
+        if (g.t == 0) S.cutkey = bound;
     } else {
         float mx = -INFINITY;
         for (int j = g.t; j < nseg; j += G::kThreads) mx = fmaxf(mx, segA[j]);
