@@ -183,6 +183,15 @@ sv_status spec_verify_static(const void *target_logits, sv_dtype logits_dtype, c
  * SV_ERR_DEVICE_DATA when one was, or SV_ERR_CUDA. */
 sv_status sv_read_device_error(const void *workspace, int32_t *code, int32_t *first_bad_request);
 
+/* Measurement aid: while set, every spec_verify call that takes the two-kernel path records
+ * the two cudaEvent_t handles on its stream immediately before and after the stream kernel
+ * (the kernel that reads every target row), so that the caller can time that kernel alone with
+ * cudaEventElapsedTime.  Recording them separates the two kernels: the select kernel then no
+ * longer overlaps the end of the stream kernel, so calls made while events are set run a
+ * little slower.  Pass NULL, NULL to stop.  Process-wide, not thread-safe; the events stay
+ * owned by the caller.  Returns SV_ERR_INVALID_ARG if only one handle is NULL. */
+sv_status sv_set_phase_events(void *stream_kernel_start, void *stream_kernel_end);
+
 /* Human-readable name of a status code. */
 const char *sv_status_string(sv_status s);
 

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
     if (warp == 0) {
         // ---- issuer (one thread): bulk copies of each prepared unit, chunk by chunk
         if (lane != 0) return;
-        const unsigned long long pol = l2_evict_first();
+        const unsigned long long pol = l2_stream_policy();
         int q = 0;
         RingPos rp{0, 0u};
         for (int j = 0;; j++) {
@@ -403,6 +403,10 @@ static cudaError_t launch_rows(const Args &A, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Events recorded around the stream kernel when set (sv_set_phase_events).  Recording them
+// separates the two kernels, so the select kernel no longer overlaps the stream's end.
+static cudaEvent_t g_phase_start = nullptr, g_phase_end = nullptr;
+
 // Launches the stream kernel (SCTA CTAs per SM) and the select kernel as its programmatic
 // dependent; returns cudaErrorNotSupported (nothing launched) when the kernels cannot be
 // resident for this vocabulary.
@@ -422,7 +426,7 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
     const long long nc = ((long long)A.V * sizeof(E) + SB - 1) / SB;
     B.nparts = (int)(nc / 2 < SPLIT_PARTS ? nc / 2 : SPLIT_PARTS);
     if (B.nparts < 2 || A.R < 2) B.nparts = 1;
-    B.nsplit = B.nparts > 1 ? (int)(ctas < A.R ? ctas : A.R) : 0;
+    B.nsplit = B.nparts > 1 ? (int)(ctas * SPLIT_WAVES < A.R ? ctas * SPLIT_WAVES : A.R) : 0;
     // shared memory of one stream CTA when SCTA share an SM (228 KB, 1 KB reserved per CTA)
     const size_t budget = (SCTA == 1 ? (size_t)232448 : (size_t)233472 / SCTA - 1024) - sizeof(SShared);
     B.pns = PNS_MAX;
@@ -435,8 +439,10 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
     if ((e = ensure_smem(k2, smem2, enabled2)) != cudaSuccess) return e;
     const long long units = (long long)A.R - B.nsplit + (long long)B.nsplit * B.nparts;
     const int grid = (int)(ctas < units ? ctas : units);
+    if (g_phase_start && (e = cudaEventRecord(g_phase_start, stream)) != cudaSuccess) return e;
     k1<<<grid, ST, smem1, stream>>>(B);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (g_phase_end && (e = cudaEventRecord(g_phase_end, stream)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)A.R);
     cfg.blockDim = dim3(SELT);
@@ -598,4 +604,11 @@ extern "C" sv_status spec_verify_static(const void *target_logits, sv_dtype logi
     return spec_verify(target_logits, logits_dtype, draft_probs, draft_tokens, num_drafts, row_offsets, B, k_max, V,
                        total_rows, params, uniforms, out_tokens, accept_len, out_pq, base[dev],
                        (size_t)SV_STATIC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" sv_status sv_set_phase_events(void *stream_kernel_start, void *stream_kernel_end) {
+    if ((stream_kernel_start == nullptr) != (stream_kernel_end == nullptr)) return SV_ERR_INVALID_ARG;
+    g_phase_start = static_cast<cudaEvent_t>(stream_kernel_start);
+    g_phase_end = static_cast<cudaEvent_t>(stream_kernel_end);
+    return SV_OK;
 }

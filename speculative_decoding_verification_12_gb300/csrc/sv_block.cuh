@@ -333,11 +333,20 @@ __device__ __forceinline__ bool mbar_wait_idle(unsigned long long *bar, uint32_t
     return true;
 }
 
-// L2 policy that evicts lines first: rows streamed once should not displace the small
-// per-segment statistics the next kernel reads back.
-__device__ __forceinline__ unsigned long long l2_evict_first() {
+#ifndef SV_L2POL
+#define SV_L2POL 0
+#endif
+// L2 policy of the streamed rows.  0: evict first (rows streamed once should not displace the
+// small per-segment statistics the next kernel reads back); 1: normal; 2: evict last.
+__device__ __forceinline__ unsigned long long l2_stream_policy() {
     unsigned long long pol;
+#if SV_L2POL == 0
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#elif SV_L2POL == 1
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#else
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+#endif
     return pol;
 }
 // One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16) that

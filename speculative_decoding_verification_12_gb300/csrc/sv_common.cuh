@@ -45,6 +45,10 @@ constexpr int RT = 256;
 constexpr int SCTA = SV_SCTA;
 constexpr int PSTREAM = SV_PSTREAM;
 constexpr int SPLIT_PARTS = SV_SPLIT_PARTS;
+#ifndef SV_SPLIT_WAVES
+#define SV_SPLIT_WAVES 2
+#endif
+constexpr int SPLIT_WAVES = SV_SPLIT_WAVES;   // waves of rows (one row per CTA each) that are split
 constexpr int ST = 32 * (2 + PSTREAM);
 #ifndef SV_SELT
 #define SV_SELT 128
