@@ -164,8 +164,12 @@ __device__ __forceinline__ void sfail(const Args &A, SShared &P, int b) {
 
 // Work unit u: row u while u < R - nsplit, then part (t mod nparts) of row R - nsplit + t / nparts
 // with t = u - (R - nsplit).
+// fp32 rows hold twice the registers per segment: two CTAs per SM instead of SCTA
 template <typename E>
-__global__ void __launch_bounds__(ST, SCTA) stream_kernel(const Args A) {
+__host__ __device__ constexpr int stream_ctas() { return sizeof(E) == 2 ? SCTA : (SCTA < 2 ? SCTA : 2); }
+
+template <typename E>
+__global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args A) {
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ SShared P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -421,14 +425,14 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
     if (!sms[dev] && (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
     Args B = A;
-    const long long ctas = (long long)sms[dev] * SCTA;
+    const long long ctas = (long long)sms[dev] * stream_ctas<E>();
     // the last wave of rows (one per CTA) is split into parts of at least 2 chunks
     const long long nc = ((long long)A.V * sizeof(E) + SB - 1) / SB;
     B.nparts = (int)(nc / 2 < SPLIT_PARTS ? nc / 2 : SPLIT_PARTS);
     if (B.nparts < 2 || A.R < 2) B.nparts = 1;
     B.nsplit = B.nparts > 1 ? (int)(ctas * SPLIT_WAVES < A.R ? ctas * SPLIT_WAVES : A.R) : 0;
     // shared memory of one stream CTA when SCTA share an SM (228 KB, 1 KB reserved per CTA)
-    const size_t budget = (SCTA == 1 ? (size_t)232448 : (size_t)233472 / SCTA - 1024) - sizeof(SShared);
+    const size_t budget = (stream_ctas<E>() == 1 ? (size_t)232448 : (size_t)233472 / stream_ctas<E>() - 1024) - sizeof(SShared);
     B.pns = PNS_MAX;
     while (B.pns > 3 && stream_smem(A.nseg, B.pns) > budget) B.pns--;
     const size_t smem1 = stream_smem(A.nseg, B.pns), smem2 = select_smem(A.nseg);

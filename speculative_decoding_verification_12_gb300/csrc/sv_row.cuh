@@ -281,6 +281,42 @@ __device__ __forceinline__ void seg_values(const RowCtx &S, const E *row, int V,
     patch_seg(S, seg * SEG, v);
 }
 
+// Calls f(seg, v, qv) for every segment of a row held in global memory (v: the lane's 8
+// penalised values; qv: the draft row's 8 values when WITHQ, else zeros).  Each warp takes
+// segments warp, warp + kWarps, ... and has U of them in flight before it uses any, so a
+// full pass is not one memory latency per segment.
+template <typename E, bool VEC, bool QVEC, bool WITHQ, int U, class G, class F>
+__device__ __forceinline__ void pass_segments(const G &g, const RowCtx &S, const E *row, const float *qrow, int V,
+                                              int nseg, F &&f) {
+    const int lane = g.lane();
+    for (int s0 = g.warp(); s0 < nseg; s0 += G::kWarps * U) {
+        Raw8<E> raw[U];
+        float qv[U][8];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int seg = s0 + u * G::kWarps;
+            if (seg < nseg) {
+                raw[u] = load_raw8<VEC>(row, seg * SEG + lane * 8, V);
+                if constexpr (WITHQ) load_q8<QVEC>(qrow, seg * SEG + lane * 8, V, qv[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int seg = s0 + u * G::kWarps;
+            if (seg < nseg) {
+                float v[8];
+                unpack8(raw[u], v);
+                patch_seg(S, seg * SEG, v);
+                if constexpr (!WITHQ) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) qv[u][j] = 0.f;
+                }
+                f(seg, v, qv[u]);
+            }
+        }
+    }
+}
+
 // Per-segment statistics of a row, written by the streaming pass.
 struct SegStats {
     float *mx;        // max of the segment
@@ -383,7 +419,7 @@ __device__ __forceinline__ int find_in_lane(const RowCtx &S, const E *row, int V
 template <typename E, bool VEC, class G>
 __device__ __forceinline__ void pass_stats(const G &g, const RowCtx &S, const E *row, int V, int nseg,
                                            const SegStats &o) {
-    constexpr int U = sizeof(E) == 2 ? 4 : 2;   // segments in flight per warp
+    constexpr int U = sizeof(E) == 2 ? 2 : 1;   // segments in flight per warp
     const int warp = g.warp(), lane = g.lane();
     for (int s0 = warp; s0 < nseg; s0 += G::kWarps * U) {
         Raw8<E> raw[U];
@@ -573,16 +609,15 @@ __device__ uint32_t select_kth_row(const G &g, RowCtx &S, const E *row, int V, i
         const int nb = 1 << width;
         for (int d = g.t; d < nb; d += G::kThreads) cnt[d] = 0;
         g.sync();
-        for (int seg = warp; seg < nseg; seg += G::kWarps) {
-            float v[8];
-            seg_values<E, VEC>(S, row, V, seg, v);
+        pass_segments<E, VEC, false, false, sizeof(E) == 2 ? 2 : 1>(
+            g, S, row, nullptr, V, nseg, [&](int seg, const float *v, const float *) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                int idx = seg * SEG + lane * 8 + j;
-                uint32_t key = fkey(v[j]);
-                if (idx < V && (key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & (nb - 1)], 1u);
-            }
-        }
+                for (int j = 0; j < 8; j++) {
+                    const int idx = seg * SEG + lane * 8 + j;
+                    const uint32_t key = fkey(v[j]);
+                    if (idx < V && (key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & (nb - 1)], 1u);
+                }
+            });
         g.sync();
         if (warp == 0) find_count_bin(S, cnt, nb, nd);
         g.sync();
@@ -644,19 +679,18 @@ __device__ uint32_t select_mass_row(const G &g, RowCtx &S, const E *row, int V, 
         const int nb = 1 << width;
         for (int d = g.t; d < nb; d += G::kThreads) mass[d] = 0ull;
         g.sync();
-        for (int seg = warp; seg < nseg; seg += G::kWarps) {
-            float v[8];
-            seg_values<E, VEC>(S, row, V, seg, v);
+        pass_segments<E, VEC, false, false, sizeof(E) == 2 ? 2 : 1>(
+            g, S, row, nullptr, V, nseg, [&](int seg, const float *v, const float *) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                int idx = seg * SEG + lane * 8 + j;
-                uint32_t key = fkey(v[j]);
-                if (idx < V && key >= key_lo && (key & mask) == prefix) {
-                    unsigned long long f = __float2ull_rz(__fmul_rn(weight(v[j], m, s), (float)FIXED_ONE));
-                    if (f) atomicAdd(&mass[(key >> shift) & (nb - 1)], f);
+                for (int j = 0; j < 8; j++) {
+                    const int idx = seg * SEG + lane * 8 + j;
+                    const uint32_t key = fkey(v[j]);
+                    if (idx < V && key >= key_lo && (key & mask) == prefix) {
+                        const unsigned long long f = __float2ull_rz(__fmul_rn(weight(v[j], m, s), (float)FIXED_ONE));
+                        if (f) atomicAdd(&mass[(key >> shift) & (nb - 1)], f);
+                    }
                 }
-            }
-        }
+            });
         g.sync();
         if (round == 0) {
             // total mass of the top-k set (every bin of round 0), summed by one warp
@@ -805,20 +839,12 @@ __device__ int draw_by_segments(const G &g, RowCtx &S, const E *row, const float
 template <typename E, bool VEC, bool QVEC, typename WF, typename WF2, class G>
 __device__ __forceinline__ void seg_sums(const G &g, const RowCtx &S, const E *row, const float *qrow, int V,
                                          int nseg, float *out1, const WF &wf1, float *out2, const WF2 &wf2) {
-    const int warp = g.warp(), lane = g.lane();
-    for (int seg = warp; seg < nseg; seg += G::kWarps) {
-        float v[8], qv[8];
-        seg_values<E, VEC>(S, row, V, seg, v);
-        if (qrow) {
-            load_q8<QVEC>(qrow, seg * SEG + lane * 8, V, qv);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; j++) qv[j] = 0.f;
-        }
+    const int lane = g.lane();
+    auto body = [&](int seg, const float *v, const float *qv) {
         float a = 0.f, c = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-            int idx = seg * SEG + lane * 8 + j;
+            const int idx = seg * SEG + lane * 8 + j;
             if (idx < V) {
                 a += wf1(v[j], qv[j]);
                 if (out2) c += wf2(v[j], qv[j]);
@@ -830,7 +856,9 @@ __device__ __forceinline__ void seg_sums(const G &g, const RowCtx &S, const E *r
             out1[seg] = a;
             if (out2) out2[seg] = c;
         }
-    }
+    };
+    if (qrow) pass_segments<E, VEC, QVEC, true, sizeof(E) == 2 ? 2 : 1>(g, S, row, qrow, V, nseg, body);
+    else pass_segments<E, VEC, QVEC, false, sizeof(E) == 2 ? 2 : 1>(g, S, row, nullptr, V, nseg, body);
     g.sync();
 }
 
