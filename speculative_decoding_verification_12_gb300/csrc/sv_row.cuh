@@ -52,6 +52,7 @@ struct __align__(16) RowCtx {
     unsigned long long sel_mass;
     double sel_target;
     int last, a, tok, need_resid, plast;
+    int prepped;    // select path: the candidate segment lists are already built
 };
 
 constexpr int PREP_BYTES = 32 * 4 + 2 * MAXK * 4;
@@ -547,53 +548,6 @@ __device__ uint32_t select_bound16(const G &g, RowCtx &S, const float *vals, int
         g.sync();
     }
     return prefix;
-}
-
-// Row maximum of n segment maxima and a lower bound on the need-th largest of them, to 16
-// bits (two 8-bit radix rounds, as select_bound16), with the keys kept in registers and five
-// group barriers.  Writes S.m; returns the bound (0 when n < need).  Up to 8 values per thread.
-template <class G>
-__device__ uint32_t max_and_bound16(const G &g, RowCtx &S, const float *vals, int n, int need, uint32_t *cnt) {
-    constexpr int PT = 8;
-    static_assert(G::kThreads * PT >= 1024, "max_and_bound16 covers up to 1024 values");
-    uint32_t key[PT];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < PT; t++) {
-        const int j = g.t + t * G::kThreads;
-        const float v = j < n ? vals[j] : -INFINITY;
-        mx = fmaxf(mx, v);
-        key[t] = j < n ? fkey(v) : 0u;
-    }
-    mx = warp_max(mx);
-    uint32_t *cnt1 = cnt + 256;
-    for (int d = g.t; d < 512; d += G::kThreads) cnt[d] = 0;
-    if (g.lane() == 0) S.redf[g.warp()] = mx;
-    g.sync();
-    const bool go = n >= need;
-    if (go) {
-#pragma unroll
-        for (int t = 0; t < PT; t++)
-            if (g.t + t * G::kThreads < n) atomicAdd(&cnt[key[t] >> 24], 1u);
-    }
-    g.sync();
-    if (g.warp() == 0) {
-        float m = S.redf[0];
-        for (int w = 1; w < G::kWarps; w++) m = fmaxf(m, S.redf[w]);
-        if (go) find_count_bin(S, cnt, 256, need);
-        if (g.lane() == 0) S.m = m;
-    }
-    g.sync();
-    if (!go) return 0u;
-    const uint32_t d0 = (uint32_t)S.sel_digit;
-    const long long nd = need - S.sel_below;
-#pragma unroll
-    for (int t = 0; t < PT; t++)
-        if (g.t + t * G::kThreads < n && (key[t] >> 24) == d0) atomicAdd(&cnt1[(key[t] >> 16) & 255u], 1u);
-    g.sync();
-    if (g.warp() == 0) find_count_bin(S, cnt1, 256, nd);
-    g.sync();
-    return (d0 << 24) | ((uint32_t)S.sel_digit << 16);
 }
 
 // The need-th largest key among the row's tokens (full passes over the row from global).

@@ -179,6 +179,75 @@ __device__ __forceinline__ void warp_append(int *list, int *count, bool take, in
     if (take) list[base + __popc(bal & ((1u << lane) - 1u))] = j;
 }
 
+// Top-k rows, up to 8 segment maxima per thread: in one pass over the maxima, the row max
+// (S.m), a lower bound on the need-th largest maximum to 16 bits (two 8-bit radix rounds with
+// the keys held in registers) and the candidate segments -- those whose max reaches the bound --
+// split into single-candidate (X.segY, count S.n2) and re-read (X.segX, count S.nsel) lists.
+// Returns the bound (0 when n < need: every segment is a candidate).  Six group barriers.
+template <class G>
+__device__ uint32_t top_prepare(const G &g, RowCtx &S, const Scratch &X, const SegStats &o, int n, int need) {
+    constexpr int PT = 8;
+    static_assert(G::kThreads * PT >= 1024, "top_prepare covers up to 1024 segments");
+    const float *vals = o.mx;
+    uint32_t *cnt = X.hcnt, *cnt1 = X.hcnt + 256;
+    uint32_t key[PT];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < PT; t++) {
+        const int j = g.t + t * G::kThreads;
+        const float v = j < n ? vals[j] : -INFINITY;
+        mx = fmaxf(mx, v);
+        key[t] = j < n ? fkey(v) : 0u;
+    }
+    mx = warp_max(mx);
+    for (int d = g.t; d < 512; d += G::kThreads) cnt[d] = 0;
+    if (g.lane() == 0) S.redf[g.warp()] = mx;
+    if (g.t == 0) {
+        S.nsel = 0;
+        S.ncand = 0;
+        S.n2 = 0;
+    }
+    g.sync();
+    const bool go = n >= need;
+    if (go) {
+#pragma unroll
+        for (int t = 0; t < PT; t++)
+            if (g.t + t * G::kThreads < n) atomicAdd(&cnt[key[t] >> 24], 1u);
+    }
+    g.sync();
+    if (g.warp() == 0) {
+        float m = S.redf[0];
+        for (int w = 1; w < G::kWarps; w++) m = fmaxf(m, S.redf[w]);
+        if (go) find_count_bin(S, cnt, 256, need);
+        if (g.lane() == 0) S.m = m;
+    }
+    g.sync();
+    uint32_t tkey = 0u;
+    if (go) {
+        const uint32_t d0 = (uint32_t)S.sel_digit;
+        const long long nd = need - S.sel_below;
+#pragma unroll
+        for (int t = 0; t < PT; t++)
+            if (g.t + t * G::kThreads < n && (key[t] >> 24) == d0) atomicAdd(&cnt1[(key[t] >> 16) & 255u], 1u);
+        g.sync();
+        if (g.warp() == 0) find_count_bin(S, cnt1, 256, nd);
+        g.sync();
+        tkey = (d0 << 24) | ((uint32_t)S.sel_digit << 16);
+    }
+    int *segl = reinterpret_cast<int *>(X.segX);
+    int *single = reinterpret_cast<int *>(X.segY);
+#pragma unroll
+    for (int t = 0; t < PT; t++) {
+        const int j = g.t + t * G::kThreads;
+        const bool cand = j < n && key[t] >= tkey;
+        const bool one = cand && fkey(o.b[j]) < tkey;
+        warp_append(single, &S.n2, one, j);
+        warp_append(segl, &S.nsel, cand && !one, j);
+    }
+    g.sync();
+    return tkey;
+}
+
 // Appends the elements at `base` (8 raw values of one lane, penalties applied) whose key
 // reaches tkey to the candidate buffer, one thread per lane-run and one atomic per warp; base
 // < 0 contributes nothing.  Returns this thread's count.  The whole warp must call it.
@@ -231,9 +300,10 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
     const float *segA = o.mx;
     // lower bound on the K-th largest token: the K-th largest segment maximum, to 16 bits
     SV_MARK(A, tix, 16);
-    // (for up to 8 maxima per thread select_row computed the row max and this bound together)
+    // (for up to 8 maxima per thread select_row built the bound and the lists already)
+    const bool prepped = S.prepped;
     uint32_t tkey = S.cutkey;
-    if (nseg > G::kThreads * 8) tkey = nseg >= K ? select_bound16(g, S, segA, nseg, K, X.hcnt, o.hist) : 0u;
+    if (!prepped) tkey = nseg >= K ? select_bound16(g, S, segA, nseg, K, X.hcnt, o.hist) : 0u;
     SV_MARK(A, tix, 17);
     // Segments whose max reaches the bound.  When a segment's second value is below it, its
     // max is its only candidate and the lane holding it is known: one 16-byte load finds the
@@ -241,21 +311,29 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
     // with warp ballots; both kinds of load go out before any is consumed.
     int *segl = reinterpret_cast<int *>(X.segX);
     int *single = reinterpret_cast<int *>(X.segY);
-    if (g.t == 0) {
-        S.nsel = 0;
-        S.ncand = 0;
-        S.n2 = 0;
+    if (!prepped) {
+        if (g.t == 0) {
+            S.nsel = 0;
+            S.ncand = 0;
+            S.n2 = 0;
+        }
+        g.sync();
+        for (int j0 = warp * 32; j0 < nseg; j0 += G::kThreads) {
+            const int j = j0 + lane;
+            const bool cand = j < nseg && fkey(segA[j]) >= tkey;
+            const bool one = cand && fkey(o.b[j]) < tkey;
+            warp_append(single, &S.n2, one, j);
+            warp_append(segl, &S.nsel, cand && !one, j);
+        }
+        g.sync();
     }
-    g.sync();
-    for (int j0 = warp * 32; j0 < nseg; j0 += G::kThreads) {
-        const int j = j0 + lane;
-        const bool cand = j < nseg && fkey(segA[j]) >= tkey;
-        const bool one = cand && fkey(o.b[j]) < tkey;
-        warp_append(single, &S.n2, one, j);
-        warp_append(segl, &S.nsel, cand && !one, j);
-    }
-    g.sync();
     const int nsingle = S.n2, nmulti = S.nsel;
+#ifdef SV_TIMING
+    if (g.t == 0) {
+        A.timing[(size_t)tix * NTIME + 13] = (unsigned long long)nsingle;
+        A.timing[(size_t)tix * NTIME + 14] = (unsigned long long)nmulti;
+    }
+#endif
     SV_MARK(A, tix, 18);
     constexpr int U = sizeof(E) == 2 ? 2 : 1;
     // first round: one single per thread and U multi segments per warp in flight together
@@ -328,6 +406,9 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
     }
     g.sync();
     const int n = S.ncand;
+#ifdef SV_TIMING
+    if (g.t == 0) A.timing[(size_t)tix * NTIME + 15] = (unsigned long long)n;
+#endif
     SV_MARK(A, tix, 19);
     if (n > CAP || n < 1) return false;
 
@@ -513,12 +594,16 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
         m = key2f((uint32_t)(key >> 32));
         st.argmax = idx < (uint32_t)V ? (int)idx : 0;   // an all -inf row: token 0
     } else if (sampled && !S.need_sum && S.mode == MODE_TOP2 && nseg <= G::kThreads * 8) {
-        // top-k rows: the row max and the candidates' bound in one pass over the maxima
-        const uint32_t bound = max_and_bound16(g, S, segA, nseg, S.K, X.hcnt);
+        // top-k rows: the row max, the candidates' bound and the candidate lists in one pass
+        const uint32_t bound = top_prepare(g, S, X, o, nseg, S.K);
         m = S.m;
         g.sync();
-        if (g.t == 0) S.cutkey = bound;
+        if (g.t == 0) {
+            S.cutkey = bound;
+            S.prepped = 1;
+        }
     } else {
+        if (g.t == 0) S.prepped = 0;
         float mx = -INFINITY;
         for (int j = g.t; j < nseg; j += G::kThreads) mx = fmaxf(mx, segA[j]);
         m = g_max(g, mx, S.redf);
