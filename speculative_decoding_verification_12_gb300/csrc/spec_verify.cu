@@ -102,10 +102,6 @@ __global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
 }
 
 // ------------------------------------------------------------------------------------------
-// persistent kernel: 16-byte aligned rows
-// ------------------------------------------------------------------------------------------
-
-// ------------------------------------------------------------------------------------------
 // Two-kernel path (16-byte aligned rows).  Streaming and selection have opposite needs: the
 // stream is bound by HBM bandwidth and wants every issue slot for its reductions; a row's
 // selection is a short chain of dependent steps that wants many rows in flight.  So:

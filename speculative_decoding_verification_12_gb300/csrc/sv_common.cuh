@@ -105,7 +105,7 @@ struct WsLayout {
 
 // Phase timestamps (globaltimer ns) per work unit, recorded only in builds with SV_TIMING.
 constexpr int NTIME = 24;
-constexpr int PMAX = 8;               // persistent kernel: most parts a row is split into
+constexpr int PMAX = 8;               // stream kernel: most parts a row is split into
 
 __host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 __host__ __device__ inline int nseg_of(int V) { return (V + SEG - 1) / SEG; }
@@ -159,16 +159,16 @@ struct Args {
     float *out_pq;            // may be NULL
     int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] work claim counter
     int32_t *counters;
-    unsigned long long *rowarg;   // persistent kernel: greedy rows' (max key, ~lowest position)
+    unsigned long long *rowarg;   // greedy rows' (max key, ~lowest position), from the stream kernel
     float *gstats;            // per-row segment statistics [R][3][npad] (stream -> select kernel)
     int4 *prep;               // per-row prepared context, 640 B each (stream -> select kernel)
     RowStat *stats;
     float *pq;
     unsigned long long *timing;   // SV_TIMING builds only
     int B, k_max, V, R, nseg;
-    int pns;                  // persistent kernel: ring stages
-    int nparts;               // persistent kernel: parts each split row is cut into (1: none)
-    int nsplit;               // persistent kernel: the last nsplit rows are split
+    int pns;                  // stream kernel: ring stages
+    int nparts;               // stream kernel: parts each split row is cut into (1: none)
+    int nsplit;               // stream kernel: the last nsplit rows are split
 };
 
 }  // namespace sv

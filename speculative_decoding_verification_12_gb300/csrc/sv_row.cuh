@@ -8,8 +8,7 @@
 // z = logit - presence*[c > 0] - frequency*c counts the drafts before the row.
 //
 // Everything that works on a whole row is templated on a thread group G (sv_block.cuh), so
-// the same code serves the one-CTA-per-row kernel and the selector warps of the persistent
-// kernel.  Sums that feed a decision use a fixed association: results are bitwise
+// the same code serves the one-CTA-per-row kernel and the select kernel.  Sums that feed a decision use a fixed association: results are bitwise
 // reproducible run to run.
 #pragma once
 

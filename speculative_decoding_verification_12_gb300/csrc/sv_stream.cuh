@@ -1,4 +1,4 @@
-// sv_stream.cuh -- the streaming pass of the persistent kernel: per-segment statistics of a
+// sv_stream.cuh -- the streaming pass of the stream kernel: per-segment statistics of a
 // row computed from its chunks in the shared-memory ring, specialised per statistics mode so
 // that a clean segment costs a handful of instructions per lane.
 //
