@@ -617,20 +617,26 @@ __device__ __forceinline__ void find_mass_bin(RowCtx &S, const unsigned long lon
 
 // Top-p threshold over the tokens with key >= key_lo: the lowest key level L whose mass
 // strictly above is < P * (total mass of those tokens).  Fixed-point (2^-40) weights make the
-// histogram sums exact and order-independent.
+// histogram sums exact and order-independent.  Each bin's sum is kept as limbs of lbits bits
+// in 32-bit counters (V tokens of less than 2^lbits each cannot overflow one), because 32-bit
+// shared-memory atomics stay fast where many tokens share a bin and 64-bit ones do not; the
+// limbs are combined into the 64-bit histogram `mass` after each pass.
 template <typename E, bool VEC, class G>
 __device__ uint32_t select_mass_row(const G &g, RowCtx &S, const E *row, int V, int nseg, uint32_t key_lo,
-                                    float m, float s, float P, unsigned long long *mass) {
+                                    float m, float s, float P, unsigned long long *mass, uint32_t *limb) {
     uint32_t prefix = 0;
     unsigned long long above = 0;
     double target = 0.0;
     const int warp = g.warp(), lane = g.lane();
+    const int lbits = V > 1 ? __clz(V - 1) : 31;        // 32 - ceil(log2 V) >= 11 for V <= 2^21
+    const int nl = (41 + lbits - 1) / lbits;            // limbs covering 2^40 (at most 4)
+    const unsigned long long lmask = (1ull << lbits) - 1ull;
     for (int round = 0; round < NRADIX; round++) {
         int shift, width;
         uint32_t mask;
         digit_round(round, shift, width, mask);
         const int nb = 1 << width;
-        for (int d = g.t; d < nb; d += G::kThreads) mass[d] = 0ull;
+        for (int d = g.t; d < 4 * nb; d += G::kThreads) limb[d] = 0u;
         g.sync();
         pass_segments<E, VEC, false, false, sizeof(E) == 2 ? 2 : 1>(
             g, S, row, nullptr, V, nseg, [&](int seg, const float *v, const float *) {
@@ -640,10 +646,21 @@ __device__ uint32_t select_mass_row(const G &g, RowCtx &S, const E *row, int V, 
                     const uint32_t key = fkey(v[j]);
                     if (idx < V && key >= key_lo && (key & mask) == prefix) {
                         const unsigned long long f = __float2ull_rz(__fmul_rn(weight(v[j], m, s), (float)FIXED_ONE));
-                        if (f) atomicAdd(&mass[(key >> shift) & (nb - 1)], f);
+                        const int bin = (key >> shift) & (nb - 1);
+#pragma unroll
+                        for (int l = 0; l < 4; l++) {
+                            const uint32_t part = (uint32_t)((f >> (lbits * l)) & lmask);
+                            if (l < nl && part) atomicAdd(&limb[l * nb + bin], part);
+                        }
                     }
                 }
             });
+        g.sync();
+        for (int d = g.t; d < nb; d += G::kThreads) {
+            unsigned long long t = 0;
+            for (int l = 0; l < nl; l++) t += (unsigned long long)limb[l * nb + d] << (lbits * l);
+            mass[d] = t;
+        }
         g.sync();
         if (round == 0) {
             // total mass of the top-k set (every bin of round 0), summed by one warp

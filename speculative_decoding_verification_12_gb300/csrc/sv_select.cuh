@@ -24,7 +24,8 @@ struct Scratch {
     float *aux, *aux2;            // CAP floats each
     unsigned long long *sorted;   // WCAP keys (aliases aux/aux2)
     uint32_t *hcnt;               // radix histogram (aliases aux)
-    unsigned long long *hmass;    // fixed-point mass histogram (aliases cand)
+    unsigned long long *hmass;    // fixed-point mass histogram (aliases aux)
+    uint32_t *hlimb;              // its 32-bit limb counters, 4 x HB (aliases cand and hcnt)
 };
 
 // Carves a Scratch out of `p`: segX/segY (nsegp floats each) then 32 KB of candidate area.
@@ -37,7 +38,8 @@ __device__ __forceinline__ Scratch carve_scratch(unsigned char *p, int nsegp) {
     c.aux = reinterpret_cast<float *>(area + size_t(CAP) * 8);
     c.aux2 = c.aux + CAP;
     c.sorted = reinterpret_cast<unsigned long long *>(c.aux);
-    c.hmass = reinterpret_cast<unsigned long long *>(area);
+    c.hmass = reinterpret_cast<unsigned long long *>(area + size_t(CAP) * 8);
+    c.hlimb = reinterpret_cast<uint32_t *>(area);
     c.hcnt = reinterpret_cast<uint32_t *>(area + size_t(HB) * 8);
     return c;
 }
@@ -553,7 +555,7 @@ __device__ void kept_by_select(const G &g, const Args &A, RowCtx &S, const Scrat
     const float m = S.m, s = S.s;
     uint32_t key_lo = 0;
     if (S.topk_on) key_lo = select_kth_row<E, VEC>(g, S, row, V, nseg, S.K, X.hcnt);
-    if (S.topp_on) key_lo = select_mass_row<E, VEC>(g, S, row, V, nseg, key_lo, m, s, S.P, X.hmass);
+    if (S.topp_on) key_lo = select_mass_row<E, VEC>(g, S, row, V, nseg, key_lo, m, s, S.P, X.hmass, X.hlimb);
     WKept wk{m, s, key_lo};
     seg_sums<E, VEC, false>(g, S, row, nullptr, V, nseg, X.segY, wk, nullptr, wk);
     float part = 0.f;

@@ -78,6 +78,10 @@ def test_host_checks_reject_bad_calls(libsv):
     assert call(wsb=100) == libsv.SV_ERR_WORKSPACE
     assert l.spec_rollback(None, C.c_void_p(16), C.c_void_p(16), 4, ws, None) == libsv.SV_ERR_INVALID_ARG
     assert l.sv_status_string(libsv.SV_ERR_WORKSPACE) == b"workspace too small or misaligned"
+    # the measurement hook takes both events or neither (nothing is recorded by these calls)
+    assert l.sv_set_phase_events(C.c_void_p(16), None) == libsv.SV_ERR_INVALID_ARG
+    assert l.sv_set_phase_events(None, C.c_void_p(16)) == libsv.SV_ERR_INVALID_ARG
+    assert l.sv_set_phase_events(None, None) == libsv.SV_OK
 
 
 def test_package_has_no_cpu_fallback():

@@ -226,3 +226,32 @@ def test_many_rows_few_ctas(sv, oracle_lib):
     claimed dynamically and requests finalised by whichever CTA completes them."""
     w = W.random_batch(28, B=300, k_max=8, V=4096, dtype="bf16", varlen=True, greedy_frac=0.3)
     full_compare(oracle_lib, w)
+
+
+def test_phase_events_time_the_stream_kernel(sv):
+    """sv_set_phase_events: the library records the caller's two events around the stream
+    kernel; the interval is positive and shorter than the whole call, and results match a call
+    made without the events."""
+    from speculative_decoding_verification_12_gb300.batch import DeviceBatch
+    w = W.random_batch(11, B=32, k_max=4, V=20000, dtype="bf16", varlen=False, greedy_frac=0.3)
+    db = DeviceBatch.from_host(w, "cuda", want_pq=True)
+    db.run()
+    torch.cuda.synchronize()
+    ref = (db.out_tokens.cpu().numpy().copy(), db.accept_len.cpu().numpy().copy())
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    b.record()
+    torch.cuda.synchronize()
+    assert sv.lib().sv_set_phase_events(a.cuda_event, b.cuda_event) == sv.SV_OK
+    try:
+        c0.record()
+        db.run()
+        c1.record()
+    finally:
+        sv.lib().sv_set_phase_events(None, None)
+    torch.cuda.synchronize()
+    stream_ms, call_ms = a.elapsed_time(b), c0.elapsed_time(c1)
+    assert 0.0 < stream_ms <= call_ms
+    np.testing.assert_array_equal(db.out_tokens.cpu().numpy(), ref[0])
+    np.testing.assert_array_equal(db.accept_len.cpu().numpy(), ref[1])
