@@ -212,9 +212,10 @@ def test_stream_b1024_k7_v128256_sampled(sv, oracle_lib):
     assert s["requests"] >= 10
 
 
-def test_max_vocabulary_row_kernel(sv, oracle_lib):
-    """V = 2^21 (the largest supported): the persistent kernel's shared memory no longer fits,
-    so the one-CTA-per-row kernel runs on aligned rows."""
+def test_max_vocabulary(sv, oracle_lib):
+    """V = 2^21 (the largest supported): 8192 segments per row, beyond the select kernel's
+    one-pass bound (1024 segments), so top-k rows take the general radix bound; the select
+    kernel then holds 168 KB of statistics and scratch per row."""
     w = W.random_batch(27, B=3, k_max=2, V=1 << 21, dtype="bf16", greedy_frac=0.3, penalties=True)
     w.top_k[:] = [0, 40, 3000]
     w.top_p[:] = [1.0, 0.9, 0.5]
