@@ -148,6 +148,17 @@ def cpu_baseline(workload: str, seconds_target: float = 12.0, max_requests: int 
                       f"{cores} threads, {dt:.1f} s"}
 
 
+def workload_config(sp, w, world: int) -> dict:
+    """The `config` object of a JSON line: the workload by name and its shape and filters."""
+    def one(a):
+        u = np.unique(np.asarray(a))
+        return u.item() if u.size == 1 else "mixed"
+    return {"workload": sp.name, "B": int(w.B), "k": int(sp.k_max), "V": int(sp.V), "logits": sp.dtype,
+            "top_k": one(w.top_k), "top_p": round(float(one(w.top_p)), 4) if one(w.top_p) != "mixed" else "mixed",
+            "greedy_share": round(float(np.mean(w.greedy != 0)), 4), "ragged_k": w.row_offsets is not None,
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, budget_s: float = 150.0):
     """--impl reference: the float64 oracle on the host cores, timed per step.  A step is a
     bounded sample of the workload (a prefix of its requests) sized from a probe so that
@@ -179,8 +190,7 @@ def run_reference(args, budget_s: float = 150.0):
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": sp.name, "B": sp.B, "k": sp.k_max, "V": sp.V, "logits": sp.dtype,
-                       "step": f"first {n} of {sp.B} requests ({rows} rows) per step"},
+            "config": workload_config(sp, W.make(args.workload) if n != sp.B else w, args.gpus),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
                              "sample": f"first {n} of {sp.B} requests ({rows} rows) per step, float64 C oracle, "
@@ -318,10 +328,9 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": sp.name, "B": w.B, "k": sp.k_max, "V": sp.V, "logits": sp.dtype,
-                       "top_k": 50, "top_p": 0.9, "greedy_share": 0.25, "parallelism": f"replicas x{world}",
-                       "l2": f"{args.copies} rotating device copies of the inputs "
-                             f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + db.draft_probs.numel() * 4) / 1e9:.2f} GB > L2)"},
+            "config": dict(workload_config(sp, w, world),
+                           l2=f"{args.copies} rotating device copies of the inputs "
+                              f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + db.draft_probs.numel() * 4) / 1e9:.2f} GB > L2)"),
             "draft_tokens_per_s": drafts * world * args.steps / (ms_max / 1e3),
             "hbm_gbs": achieved,
             "accept": {"mean_accept_len": float(acc.mean()), "accept_rate": float(acc.sum() / max(drafts, 1)),
