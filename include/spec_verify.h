@@ -144,6 +144,9 @@ sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const fl
  *   workspace    the spec_verify workspace (its sticky error word records failures).
  * A request with accept_len < 0 or > k_b, k_b < 0, or a result outside [0, kv_seq_len] keeps
  * its length and records SV_DEV_BAD_LAYOUT.
+ *
+ * The same call rolls back the draft model's cache: it appended the k_b drafts and keeps the
+ * accepted ones, L - k_b + accept_len[b] (same section), which is the same update.
  */
 sv_status spec_rollback(int32_t *kv_seq_len, const int32_t *accept_len, const int32_t *num_drafts,
                         int32_t B, void *workspace, void *stream);

@@ -174,6 +174,21 @@ def test_rollback_matches_closed_form(sv, oracle_lib):
     assert sv.sv_read_device_error(ws)[0] == 1
 
 
+def test_rollback_of_draft_cache_lengths(sv, oracle_lib):
+    """spec_rollback on the draft cache's lengths (k drafts appended, accepted ones kept)."""
+    import json
+    import os
+    here = os.path.dirname(os.path.abspath(__file__))
+    cs = json.load(open(os.path.join(here, "golden", "worked_examples.json")))["rollback_draft"]["cases"]
+    L = np.array([c["current_len"] for c in cs], np.int32)
+    k = np.array([c["k"] for c in cs], np.int32)
+    a = np.array([c["accepted"] for c in cs], np.int32)
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    kv = torch.from_numpy(L).cuda()
+    sv.spec_rollback(kv, torch.from_numpy(a).cuda(), torch.from_numpy(k).cuda(), ws)
+    assert list(kv.cpu().numpy()) == [c["committed"] for c in cs]
+
+
 # ------------------------------------------------------------------------------------------
 # the measured workloads: full compare where the oracle is quick, sampled otherwise
 # ------------------------------------------------------------------------------------------

@@ -414,6 +414,18 @@ def test_rollback_closed_form(oracle_lib):
     assert nerr == 3 and (out == -1).all()
 
 
+def test_draft_rollback_is_the_same_update(oracle_lib):
+    """The draft cache appended k drafts and keeps the accepted ones: L - k + a, which is the
+    target's L - (k+1) + 1 + a written differently, so one rollback serves both caches."""
+    cs = GOLD["rollback_draft"]["cases"]
+    L = np.array([c["current_len"] for c in cs])
+    k = np.array([c["k"] for c in cs])
+    a = np.array([c["accepted"] for c in cs])
+    out, nerr = oracle_lib.rollback(L, a, k)
+    assert nerr == 0
+    assert list(out) == [c["committed"] for c in cs]
+
+
 def test_greedy_ties_go_to_lowest_id(oracle_lib):
     """Exact ties (as bf16 rows have) resolve to the lowest token id, as numpy's argmax does."""
     g = _rng(13)
