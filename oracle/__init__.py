@@ -56,6 +56,8 @@ def load(path: str):
     l.sv_oracle_verify.restype = C.c_int
     l.sv_oracle_verify.argtypes = [C.POINTER(_Batch), C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_void_p]
+    l.sv_oracle_verify_onehot.restype = C.c_int
+    l.sv_oracle_verify_onehot.argtypes = l.sv_oracle_verify.argtypes
     l.sv_oracle_row_probs.restype = C.c_int32
     l.sv_oracle_row_probs.argtypes = [C.POINTER(_Batch), C.c_int32, C.c_int32, C.c_void_p]
     l.sv_oracle_residual.restype = C.c_int32
@@ -100,13 +102,17 @@ class _Held:
                             _ptr(a["g"]), _ptr(a["u"]))
 
 
-def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1):
+def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1, onehot: bool = False):
     """Run the oracle on a workload (all requests or a subset); returns a dict of arrays.
 
     out_tokens [B, k_max+1] int32 (-1 padded), accept_len [B] int32, pq [D, 2] float64
     (p(x_i), q(x_i); NaN for greedy requests), pq_near [D] uint8 (the row's kept set sits
     on a near-tie), decisions / near_ties / error [B] int32.  Requests not in `requests`
     are left at -1 / NaN.
+
+    onehot=True runs the one-hot-draft scheme: every row is sampled with its draw uniform
+    and the drafts are accepted while they match those samples; draft_probs is not read and
+    pq's second column is 1.
     """
     h = _Held(w)
     B, D = w.B, w.total_drafts
@@ -124,8 +130,10 @@ def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1):
     else:
         ranges = [(int(b), int(b) + 1) for b in requests]
 
+    fn = l.sv_oracle_verify_onehot if onehot else l.sv_oracle_verify
+
     def run(rg):
-        rc = l.sv_oracle_verify(C.byref(h.batch), rg[0], rg[1], out.ctypes.data, acc.ctypes.data,
+        rc = fn(C.byref(h.batch), rg[0], rg[1], out.ctypes.data, acc.ctypes.data,
                                 pq.ctypes.data, near.ctypes.data, diag)
         if rc != 0:
             raise RuntimeError(f"oracle failed rc={rc}")

@@ -23,7 +23,9 @@
  *       (one-hot draft) case of the uniform-vs-ratio test.
  *  [F1] FreeToken PR #836, section "Design": every verify row samples with its own
  *       request's temperature, top-k, top-p and greedy flag; presence and frequency
- *       penalties count the drafts before a row as already generated.
+ *       penalties count the drafts before a row as already generated.  Its drafts are
+ *       argmax proposals, so it samples every verify row as a decode step would and keeps
+ *       the prefix of drafts that equals those samples (the one-hot-draft scheme).
  *  [S2] "Speculative Decoding: Draft Model Sampling, Rejection Sampling & On-Device
  *       Acceleration", Key Topic 2 and Section 2: the same accept/residual formulas.
  *
@@ -41,6 +43,8 @@
  *  - uniforms: slot 0 of row i is the accept test of draft i; slot 1 of the final row is
  *    the residual or extra-token draw.
  *  - greedy argmax breaks ties toward the lowest token id; greedy rows read neither q nor u.
+ *  - one-hot-draft scheme [F1]: row i's sample is drawn with slot 1 (the draw slot) of its
+ *    own uniforms, on every row 0..k; slot 0 is unused there.
  *
  * Near-tie bookkeeping (decisions whose float64 value lies within 1e-5 of a boundary, where
  * an fp32 implementation may legitimately decide the other way) is reported per request.
@@ -99,8 +103,10 @@ static int64_t row_start(const sv_oracle_batch *in, int32_t b) {
     return in->row_offsets ? (int64_t)in->row_offsets[b] : (int64_t)b * (in->k_max + 1);
 }
 
-/* Checks the request's layout and the inputs its path reads; returns an error code. */
-static int check_request(const sv_oracle_batch *in, int32_t b) {
+/* Checks the request's layout and the inputs its path reads; returns an error code.
+ * `slot_lo` is the first uniform slot the path reads (0 for the accept-test scheme, 1 for
+ * the one-hot scheme, which reads only the draw slot). */
+static int check_request_slots(const sv_oracle_batch *in, int32_t b, int slot_lo) {
     int32_t k = in->num_drafts[b];
     int64_t r0 = row_start(in, b);
     int64_t cap;
@@ -126,13 +132,15 @@ static int check_request(const sv_oracle_batch *in, int32_t b) {
         float P = in->top_p[b];
         if (!(P > 0.0f && P <= 1.0f)) return E_TOPP;
         for (int32_t i = 0; i <= k; i++)
-            for (int s = 0; s < 2; s++) {
+            for (int s = slot_lo; s < 2; s++) {
                 float u = in->uniforms[(r0 + i) * 2 + s];
                 if (!(u >= 0.0f && u < 1.0f)) return E_UNIFORM;
             }
     }
     return E_OK;
 }
+
+static int check_request(const sv_oracle_batch *in, int32_t b) { return check_request_slots(in, b, 0); }
 
 /* z_v for row i of request b: the logit minus the presence/frequency penalty of the drafts
  * d_0..d_{i-1} [F1].  Returns 1 when some token of the row carries a nonzero penalty. */
@@ -421,6 +429,78 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
     if (dg) dg[b] = d;
 }
 
+/* One request under the one-hot-draft scheme [F1]: the drafts are argmax proposals (q_i is
+ * one-hot at d_i), so every row i = 0..k is sampled as a decode step would sample it -- the
+ * argmax for a greedy request, else t_i = inverse CDF of the filtered p_i at the row's draw
+ * uniform u_{i,1} -- and the drafts are accepted while d_i == t_i.  The output at the first
+ * mismatch, or at row k, is that row's own sample.  No q is read; slot 0 of the uniforms is
+ * not read.  out_pq receives (p_i(d_i), 1): the one-hot draft puts mass 1 on its token. */
+static void verify_one_onehot(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, int32_t *acc,
+                              double *out_pq, uint8_t *pq_near, sv_oracle_diag *dg,
+                              double *z, double *p, double *scratch) {
+    const int32_t V = in->V;
+    const int32_t kmax1 = in->k_max + 1;
+    for (int32_t j = 0; j < kmax1; j++) out_tok[(int64_t)b * kmax1 + j] = -1;
+    sv_oracle_diag d = {0, 0, 0, 0, 0, 0, 0, 0};
+    int err = check_request_slots(in, b, 1);
+    const int64_t r0 = row_start(in, b), d0 = r0 - b;
+    const int32_t k = in->num_drafts[b];
+    if (err) {
+        acc[b] = -1;
+        if (out_pq && k >= 0 && k <= in->k_max && d0 >= 0)
+            for (int32_t i = 0; i < k && d0 + i < in->total_rows - in->B; i++) {
+                out_pq[(d0 + i) * 2] = NAN;
+                out_pq[(d0 + i) * 2 + 1] = NAN;
+            }
+        d.error = err;
+        if (dg) dg[b] = d;
+        return;
+    }
+    const int32_t *drafts = in->draft_tokens + d0;
+    int32_t a = k, token = -1;
+    int decided = 0;
+    for (int32_t i = 0; i <= k; i++) {
+        int pen = row_logits(in, b, i, z);
+        int32_t t;
+        int nt = 0, cn = 0, dec = 0;
+        row_amb amb;
+        if (in->greedy[b]) {
+            t = row_argmax(z, V, pen, &nt);
+            if (i < k) {
+                if (out_pq) { out_pq[(d0 + i) * 2] = NAN; out_pq[(d0 + i) * 2 + 1] = NAN; }
+                if (pq_near) pq_near[d0 + i] = 0;
+            }
+            if (decided) continue;
+            d.decisions++;
+            d.near_ties += nt;
+            d.near_argmax += nt;
+        } else {
+            row_probs(in, b, z, pen, p, scratch, &dec, &amb);
+            if (i < k) {
+                int32_t x = drafts[i];
+                if (out_pq) { out_pq[(d0 + i) * 2] = p[x]; out_pq[(d0 + i) * 2 + 1] = 1.0; }
+                if (pq_near) pq_near[d0 + i] = (uint8_t)in_amb(&amb, z[x] / in->temperature[b]);
+            }
+            if (decided) continue;
+            t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 1], &cn);
+            d.near_cdf += cn;
+            /* tokens whose membership of the kept set is on a near-tie could move the boundary */
+            if (!cn && amb.mass >= NEAR_TOL) { cn = 1; d.near_filter++; }
+            d.decisions += dec + 1;
+            d.near_ties += cn;
+        }
+        if (i == k || drafts[i] != t) {
+            a = i;
+            token = t;
+            decided = 1;
+        }
+    }
+    for (int32_t j = 0; j < a; j++) out_tok[(int64_t)b * kmax1 + j] = drafts[j];
+    out_tok[(int64_t)b * kmax1 + a] = token;
+    acc[b] = a;
+    if (dg) dg[b] = d;
+}
+
 /* Verifies requests [b_lo, b_hi).  Output arrays are full-batch sized; only the rows of
  * these requests are written.  Safe to call concurrently on disjoint request ranges. */
 int sv_oracle_verify(const sv_oracle_batch *in, int32_t b_lo, int32_t b_hi, int32_t *out_tokens,
@@ -432,6 +512,21 @@ int sv_oracle_verify(const sv_oracle_batch *in, int32_t b_lo, int32_t b_hi, int3
     for (int32_t b = b_lo; b < b_hi; b++)
         verify_one(in, b, out_tokens, accept_len, out_pq, pq_near, diag, buf, buf + V, buf + 2 * V,
                    buf + 3 * V);
+    free(buf);
+    return 0;
+}
+
+/* Verifies requests [b_lo, b_hi) under the one-hot-draft scheme (verify_one_onehot);
+ * draft_probs is not read and may be NULL.  Same outputs and concurrency as
+ * sv_oracle_verify. */
+int sv_oracle_verify_onehot(const sv_oracle_batch *in, int32_t b_lo, int32_t b_hi, int32_t *out_tokens,
+                            int32_t *accept_len, double *out_pq, uint8_t *pq_near, sv_oracle_diag *diag) {
+    if (!in || !out_tokens || !accept_len || in->V < 1 || b_lo < 0 || b_hi > in->B) return -1;
+    size_t V = (size_t)in->V;
+    double *buf = (double *)malloc(sizeof(double) * V * 3);
+    if (!buf) return -2;
+    for (int32_t b = b_lo; b < b_hi; b++)
+        verify_one_onehot(in, b, out_tokens, accept_len, out_pq, pq_near, diag, buf, buf + V, buf + 2 * V);
     free(buf);
     return 0;
 }

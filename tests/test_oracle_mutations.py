@@ -61,6 +61,18 @@ MUTATIONS = [
      "token = inverse_cdf(r, V, in->uniforms[(r0 + k) * 2 + 1], &cn);",
      [lambda o: pins.test_expected_tokens_closed_form(o),
       lambda o: pins.test_lossless_monte_carlo(o, 4, 1, 1.0, 0, 1.0, None, None)]),
+    ("one-hot: accepts on a mismatch", "if (i == k || drafts[i] != t) {", "if (i == k || drafts[i] == t) {",
+     [lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None)]),
+    ("one-hot: samples with the accept slot", "t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 1], &cn);",
+     "t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 0], &cn);",
+     [lambda o: pins.test_onehot_reduces_to_pinned_paths(o)]),
+    ("one-hot: emits the draft at the stopping row", "token = t;", "token = i < k ? drafts[i] : t;",
+     [lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None),
+      lambda o: pins.test_onehot_matches_when_every_sample_matches(o)]),
+    ("one-hot: scan ignores the last draft", "if (i == k || drafts[i] != t) {",
+     "if (i == k || (i + 1 < k && drafts[i] != t)) {",
+     [lambda o: pins.test_onehot_matches_when_every_sample_matches(o),
+      lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None)]),
     ("rollback keeps one row too many", "int64_t t = L - (k + 1) + 1 + a;", "int64_t t = L - (k + 1) + 2 + a;",
      [lambda o: pins.test_rollback_closed_form(o)]),
 ]

@@ -454,3 +454,138 @@ def test_inverse_cdf_never_picks_zero_weight(oracle_lib):
     w.uniforms[0, 0] = 0.0                   # accepted; the extra token is drawn with u = 0
     r = oracle_lib.verify(w)
     assert r["accept_len"][0] == 1 and list(r["out_tokens"][0]) == [3, 2]
+
+
+# ------------------------------------------------------------------------------------------
+# P9: the one-hot-draft scheme (FreeToken PR #836, Design: drafts are argmax proposals, so
+# every verify row is sampled as decode would sample it and the matching prefix is kept)
+# ------------------------------------------------------------------------------------------
+
+def _joint_closed_form(logits, drafts, T, K, P, pres, freq):
+    """Exact law of (accept_len a, final token t) for fixed drafts d_0..d_{k-1} when the
+    drafts are one-hot: a = j with t != d_j (j < k), or a = k with any t, with probability
+    prod_{i<j} p_i(d_i) * p_j(t).  p_i is the filtered target of row i with the drafts
+    before it counted by the penalties, built from the filter definitions."""
+    k, V = drafts.shape[0], logits.shape[1]
+    ps = []
+    for i in range(k + 1):
+        z = logits[i].astype(np.float64).copy()
+        c = np.bincount(drafts[:i], minlength=V).astype(np.float64)
+        z -= (pres or 0.0) * (c > 0) + (freq or 0.0) * c
+        ps.append(_brute_filter(z, T, K, P))
+    law = np.zeros((k + 1, V))
+    lead = 1.0
+    for j in range(k + 1):
+        law[j] = lead * ps[j]
+        if j < k:
+            law[j, drafts[j]] = 0.0
+            lead *= ps[j][drafts[j]]
+    return law, ps
+
+
+@pytest.mark.parametrize("V,k,T,K,P,pres,freq", [
+    (5, 2, 1.0, 0, 1.0, None, None),
+    (7, 3, 0.8, 5, 0.9, 0.5, 0.3),
+    (6, 2, 1.4, 0, 0.85, 1.0, 0.0),
+])
+def test_onehot_joint_law(oracle_lib, V, k, T, K, P, pres, freq):
+    """P9a: sampling every row and keeping the matching prefix reproduces the target's
+    sequential law exactly: the joint frequencies of (a, t) match the closed form, and no
+    zero-probability outcome (the draft itself at the stopping row) ever appears.  The
+    accept-test scheme given the same one-hot q must follow the same law (the two are equal
+    in distribution and differ only in how they use the uniforms)."""
+    n = 400_000
+    g = _rng(1000 + V * 10 + k)
+    logits = (g.standard_normal((k + 1, V)) * 1.2).astype(np.float32)
+    drafts = logits[:k].argmax(-1).astype(np.int32)            # argmax proposals
+    drafts[-1] = (drafts[-1] + 1) % V                          # and one that is not
+    law, _ = _joint_closed_form(logits, drafts, T, K, P, pres, freq)
+    q = np.zeros((k, V), np.float32)
+    q[np.arange(k), drafts] = 1.0
+    uni = g.random((n, k + 1, 2), dtype=np.float32)
+    w = W.from_rows(V, logits, q, np.broadcast_to(drafts, (n, k)), uni, temperature=T, top_k=K, top_p=P,
+                    presence=pres, frequency=freq)
+    for onehot in (True, False):
+        r = oracle_lib.verify(w, threads=8, onehot=onehot)
+        assert (r["error"] == 0).all()
+        a = r["accept_len"]
+        t = r["out_tokens"][np.arange(n), a]
+        obs = np.bincount(a * V + t, minlength=(k + 1) * V).astype(np.float64)
+        assert _chisq_p(obs, law.reshape(-1)) > 1e-4, (onehot, obs.reshape(k + 1, V), law * n)
+        assert (r["out_tokens"][:, :k][np.arange(k)[None, :] < a[:, None]] ==
+                np.broadcast_to(drafts, (n, k))[np.arange(k)[None, :] < a[:, None]]).all()
+
+
+def test_onehot_top_k_one_is_greedy(oracle_lib):
+    """P9b: with p one-hot at the argmax (top-k = 1, no ties) every row's sample is its argmax,
+    so the scheme returns the greedy result exactly, whatever the uniforms."""
+    g = _rng(31)
+    B, k, V = 300, 4, 40
+    logits = g.standard_normal((B, k + 1, V)).astype(np.float32)
+    am = logits.argmax(-1)
+    drafts = np.where(g.random((B, k)) < 0.6, am[:, :k], g.integers(0, V, (B, k))).astype(np.int32)
+    q = np.full((B, k, V), np.nan, np.float32)
+    uni = g.random((B, k + 1, 2), dtype=np.float32)
+    wg = W.from_rows(V, logits, q, drafts, uni, greedy=1, presence=0.3, frequency=0.2)
+    ws = W.from_rows(V, logits, q, drafts, uni, greedy=0, top_k=1, temperature=0.7, presence=0.3,
+                     frequency=0.2)
+    rg = oracle_lib.verify(wg)
+    rs = oracle_lib.verify(ws, onehot=True)
+    np.testing.assert_array_equal(rs["accept_len"], rg["accept_len"])
+    np.testing.assert_array_equal(rs["out_tokens"], rg["out_tokens"])
+
+
+def test_onehot_reduces_to_pinned_paths(oracle_lib):
+    """P9c: greedy requests are the same in both schemes; a request with no drafts is the
+    extra-token draw of row 0 with slot 1 in both; and the scheme reads neither q nor slot 0
+    (q all NaN and slot 0 out of range change nothing)."""
+    w = W.random_batch(17, B=60, k_max=5, V=41, varlen=True, greedy_frac=0.4)
+    ro = oracle_lib.verify(w, onehot=True)
+    rr = oracle_lib.verify(w)
+    gr = w.greedy.astype(bool)
+    np.testing.assert_array_equal(ro["accept_len"][gr], rr["accept_len"][gr])
+    np.testing.assert_array_equal(ro["out_tokens"][gr], rr["out_tokens"][gr])
+    zero = w.num_drafts == 0
+    assert zero.any()
+    np.testing.assert_array_equal(ro["out_tokens"][zero], rr["out_tokens"][zero])
+    w.draft_probs[:] = np.nan
+    w.uniforms[:, 0] = 7.0
+    r2 = oracle_lib.verify(w, onehot=True)
+    assert (r2["error"] == 0).all()
+    np.testing.assert_array_equal(r2["accept_len"], ro["accept_len"])
+    np.testing.assert_array_equal(r2["out_tokens"], ro["out_tokens"])
+    # out_pq: p(d_i) as the accept-test scheme reports it, q(d_i) = 1
+    samp = ~np.isnan(rr["pq"][:, 0])
+    np.testing.assert_array_equal(ro["pq"][samp, 0], rr["pq"][samp, 0])
+    assert (ro["pq"][samp, 1] == 1.0).all()
+    # slot 1 out of range is still an error
+    w.uniforms[w.row_start(int(np.argmin(gr))), 1] = 1.0
+    r3 = oracle_lib.verify(w, onehot=True)
+    assert r3["error"][int(np.argmin(gr))] == 5
+
+
+def test_onehot_matches_when_every_sample_matches(oracle_lib):
+    """P9d: drafts set to the samples the rows produce (found one row at a time through the
+    zero-draft reduction) are all accepted, and the output is row k's sample."""
+    g = _rng(33)
+    V, k = 23, 4
+    logits = (g.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+    u = g.random((1, k + 1, 2), dtype=np.float32)
+    drafts = np.zeros((1, k), np.int32)
+    for i in range(k):
+        # with no penalties row i does not depend on the drafts: its sample is a zero-draft draw
+        wi = W.from_rows(V, logits[i:i + 1], np.zeros((0, V), np.float32), np.zeros((1, 0), np.int32),
+                         u[:, i:i + 1], temperature=0.9, top_p=0.95)
+        drafts[0, i] = oracle_lib.verify(wi)["out_tokens"][0, 0]
+    w = W.from_rows(V, logits, np.zeros((k, V), np.float32), drafts, u, temperature=0.9, top_p=0.95)
+    r = oracle_lib.verify(w, onehot=True)
+    assert r["accept_len"][0] == k
+    assert list(r["out_tokens"][0, :k]) == list(drafts[0])
+    wk = W.from_rows(V, logits[k:], np.zeros((0, V), np.float32), np.zeros((1, 0), np.int32), u[:, k:],
+                     temperature=0.9, top_p=0.95)
+    assert r["out_tokens"][0, k] == oracle_lib.verify(wk)["out_tokens"][0, 0]
+    # change draft 2: the scan stops there and emits row 2's sample
+    drafts[0, 2] = (drafts[0, 2] + 1) % V
+    w2 = W.from_rows(V, logits, np.zeros((k, V), np.float32), drafts, u, temperature=0.9, top_p=0.95)
+    r2 = oracle_lib.verify(w2, onehot=True)
+    assert r2["accept_len"][0] == 2 and r2["out_tokens"][0, 2] == (drafts[0, 2] - 1) % V
