@@ -7,6 +7,9 @@ top-k 50, top-p 0.9, a quarter greedy).  Inputs are synthetic and seeded; three 
 of the two large inputs (0.85 GB each set) rotate between steps so no step reads inputs left
 in L2 by the one before.
 
+--scheme onehot times the one-hot-draft entry point instead (drafts = the argmax of each draft
+row's q; every row is sampled and the matching prefix kept; q is not read).
+
 Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle instead.
 """
 from __future__ import annotations
@@ -30,7 +33,7 @@ METRIC = "verify rows/s and achieved HBM GB/s (% of GB300 roofline) vs CPU oracl
 # DRAM bytes (read + write) of one stream-kernel launch on the full batch, from the ncu capture
 # summarised under profiles/ (a 160-request cut, scaled by rows).  Valid only for the kernel as
 # captured; absent (null) otherwise.
-TRAFFIC_STREAM_KERNEL = {"b256_k4_v128256_bf16_zipf": 335.6e6}
+TRAFFIC_STREAM_KERNEL = {"b256_k4_v128256_bf16_zipf": 335.1e6}
 DEFAULT_WORKLOAD = "b256_k4_v128256_bf16_zipf"
 
 
@@ -43,14 +46,15 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def algorithmic_bytes(w, accept_len) -> dict:
+def algorithmic_bytes(w, accept_len, onehot=False) -> dict:
     """Bytes the method must move for one call (see the design notes, 'Measurement').
 
     Every target row of every request (the one-pass design cannot skip rows before knowing
     where the rejection falls); one 32-byte sector of q per sampled draft (q(x_i)); at a
     rejected sampled row, q over the residual's support: the kept set of a filtered row
     (<= top-k tokens, one sector each) or the whole q row plus a re-read of the target row when
-    the row keeps every token; small per-row/per-request I/O.
+    the row keeps every token; small per-row/per-request I/O.  The one-hot scheme reads no q:
+    the target rows and the I/O only.
     """
     esz = 2 if w.dtype == "bf16" else 4
     V = w.V
@@ -58,9 +62,9 @@ def algorithmic_bytes(w, accept_len) -> dict:
     rows = int((nd + 1).sum())
     sampled = w.greedy == 0
     b_rows = rows * V * esz
-    b_q = int(nd[sampled].sum()) * 32
+    b_q = 0 if onehot else int(nd[sampled].sum()) * 32
     b_rej = 0
-    for b in np.nonzero(sampled & (accept_len < nd) & (accept_len >= 0))[0]:
+    for b in ([] if onehot else np.nonzero(sampled & (accept_len < nd) & (accept_len >= 0))[0]):
         K = int(w.top_k[b])
         if 0 < K < V:
             b_rej += 32 * K
@@ -124,7 +128,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(workload: str, seconds_target: float = 12.0, max_requests: int = 256):
+def cpu_baseline(workload: str, seconds_target: float = 12.0, max_requests: int = 256, onehot=False):
     """The float64 oracle on the host cores, on a bounded sample of the same workload: the
     first (up to) 256 requests, verified repeatedly until about 12 s of wall time."""
     import oracle
@@ -134,11 +138,13 @@ def cpu_baseline(workload: str, seconds_target: float = 12.0, max_requests: int 
     sp = W.spec(workload)
     n = min(sp.B, max_requests)
     w = W.make(workload, requests=range(n))
+    if onehot:
+        W.with_argmax_drafts(w)
     rows = int((w.num_drafts.astype(np.int64) + 1).sum())
     reps = 0
     t0 = time.perf_counter()
     while True:
-        oracle.verify(w, threads=cores)
+        oracle.verify(w, threads=cores, onehot=onehot)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= seconds_target or reps >= 1000:
@@ -148,12 +154,13 @@ def cpu_baseline(workload: str, seconds_target: float = 12.0, max_requests: int 
                       f"{cores} threads, {dt:.1f} s"}
 
 
-def workload_config(sp, w, world: int) -> dict:
+def workload_config(sp, w, world: int, onehot=False) -> dict:
     """The `config` object of a JSON line: the workload by name and its shape and filters."""
     def one(a):
         u = np.unique(np.asarray(a))
         return u.item() if u.size == 1 else "mixed"
-    return {"workload": sp.name, "B": int(w.B), "k": int(sp.k_max), "V": int(sp.V), "logits": sp.dtype,
+    extra = {"scheme": "one-hot drafts (argmax of q): every row sampled, matching prefix kept"} if onehot else {}
+    return {**extra, "workload": sp.name, "B": int(w.B), "k": int(sp.k_max), "V": int(sp.V), "logits": sp.dtype,
             "top_k": one(w.top_k), "top_p": round(float(one(w.top_p)), 4) if one(w.top_p) != "mixed" else "mixed",
             "greedy_share": round(float(np.mean(w.greedy != 0)), 4), "ragged_k": w.row_offsets is not None,
             "parallelism": f"replicas x{world}"}
@@ -172,25 +179,28 @@ def run_reference(args, budget_s: float = 150.0):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     sp = W.spec(args.workload)
     n_probe = min(sp.B, max(2 * cores, 32))
-    w = W.make(args.workload, requests=range(n_probe))
+    onehot = args.scheme == "onehot"
+    mk = lambda req: W.with_argmax_drafts(W.make(args.workload, requests=req)) if onehot else \
+        W.make(args.workload, requests=req)
+    w = mk(range(n_probe))
     t0 = time.perf_counter()
-    oracle.verify(w, threads=cores)
+    oracle.verify(w, threads=cores, onehot=onehot)
     t_req = (time.perf_counter() - t0) / n_probe
     n = int(max(1, min(sp.B, budget_s / ((args.steps + args.warmup) * max(t_req, 1e-6)))))
     if n != n_probe:
-        w = W.make(args.workload, requests=range(n))
+        w = mk(range(n))
     rows = int((w.num_drafts.astype(np.int64) + 1).sum())
     for _ in range(args.warmup):
-        oracle.verify(w, threads=cores)
+        oracle.verify(w, threads=cores, onehot=onehot)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.verify(w, threads=cores)
+        oracle.verify(w, threads=cores, onehot=onehot)
     dt = time.perf_counter() - t0
     value = rows * args.steps / dt
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(sp, W.make(args.workload) if n != sp.B else w, args.gpus),
+            "config": workload_config(sp, W.make(args.workload) if n != sp.B else w, args.gpus, onehot),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
                              "sample": f"first {n} of {sp.B} requests ({rows} rows) per step, float64 C oracle, "
@@ -217,14 +227,18 @@ def run_ours(args):
     sv.lib()
 
     sp = W.spec(args.workload)
+    onehot = args.scheme == "onehot"
     w = W.make(args.workload, requests=None if args.requests is None else list(range(args.requests)))
+    if onehot:
+        W.with_argmax_drafts(w)
     db = DeviceBatch.from_host(w, dev, want_pq=False)
     stream = torch.cuda.Stream(dev)
     copies = [(db.target_logits, db.draft_probs)]
     for _ in range(args.copies - 1):
-        copies.append((db.target_logits.clone(), db.draft_probs.clone()))
+        # the one-hot scheme reads no q: only the target logits rotate
+        copies.append((db.target_logits.clone(), db.draft_probs if onehot else db.draft_probs.clone()))
     with torch.cuda.stream(stream):
-        calls = [bound_call(db, stream, t, d) for t, d in copies]
+        calls = [bound_call(db, stream, t, d, onehot=onehot) for t, d in copies]
     torch.cuda.synchronize(dev)
 
     def barrier():
@@ -259,7 +273,7 @@ def run_ours(args):
     per_step_ms = ms_max / args.steps
     value = rows * world * args.steps / (ms_max / 1e3)
 
-    nb = algorithmic_bytes(w, acc)
+    nb = algorithmic_bytes(w, acc, onehot)
     peak, peak_kind = peaks()
     achieved = nb["total"] / (ms / args.steps / 1e3) / 1e9
 
@@ -285,10 +299,11 @@ def run_ours(args):
     host = {
         "tl": torch.from_numpy(np.ascontiguousarray(w.target_logits).view(np.int16) if w.dtype == "bf16"
                                else w.target_logits).pin_memory(),
-        "dp": torch.from_numpy(w.draft_probs).pin_memory(),
         "dt": torch.from_numpy(w.draft_tokens).pin_memory(),
         "u": torch.from_numpy(w.uniforms).pin_memory(),
     }
+    if not onehot:
+        host["dp"] = torch.from_numpy(w.draft_probs).pin_memory()
     pins_out = (torch.empty_like(db.out_tokens, device="cpu").pin_memory(),
                 torch.empty_like(db.accept_len, device="cpu").pin_memory())
     tl_dev = db.target_logits.view(torch.int16) if w.dtype == "bf16" else db.target_logits
@@ -298,7 +313,8 @@ def run_ours(args):
     def e2e_step():
         with torch.cuda.stream(stream):
             tl_dev.copy_(host["tl"], non_blocking=True)
-            db.draft_probs.copy_(host["dp"], non_blocking=True)
+            if not onehot:
+                db.draft_probs.copy_(host["dp"], non_blocking=True)
             db.draft_tokens.copy_(host["dt"], non_blocking=True)
             db.uniforms.copy_(host["u"], non_blocking=True)
             calls[0]()
@@ -328,9 +344,9 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(workload_config(sp, w, world),
+            "config": dict(workload_config(sp, w, world, onehot),
                            l2=f"{args.copies} rotating device copies of the inputs "
-                              f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + db.draft_probs.numel() * 4) / 1e9:.2f} GB > L2)"),
+                              f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + (0 if onehot else db.draft_probs.numel() * 4)) / 1e9:.2f} GB > L2)"),
             "draft_tokens_per_s": drafts * world * args.steps / (ms_max / 1e3),
             "hbm_gbs": achieved,
             "accept": {"mean_accept_len": float(acc.mean()), "accept_rate": float(acc.sum() / max(drafts, 1)),
@@ -342,11 +358,12 @@ def run_ours(args):
                          "timed": f"CUDA events recorded by the library around the stream kernel on its stream, "
                                   f"mean of {args.phase_steps} calls",
                          "traffic": args.traffic if args.traffic is not None else
-                         (TRAFFIC_STREAM_KERNEL.get(sp.name) if args.requests is None else None),
+                         (TRAFFIC_STREAM_KERNEL.get(sp.name) if args.requests is None and not onehot else None),
                          "traffic_unit": "bytes per launch (ncu dram read+write)",
                          "call": {"achieved": achieved, "frac": achieved / peak, "bytes": nb["total"],
                                   "us": per_step_ms * 1e3,
-                                  "what": "whole spec_verify call: memset + stream_kernel + select_kernel (PDL)"}},
+                                  "what": f"whole {'spec_verify_onehot' if onehot else 'spec_verify'} call: "
+                                          f"memset + stream_kernel + select_kernel (PDL)"}},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             # each spec_verify call launches the stream kernel and the select kernel (the
             # clearing of the workspace header is a cudaMemsetAsync, not counted)
@@ -354,7 +371,7 @@ def run_ours(args):
             "clocks": clk,
         }
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(args.workload)
+            line["cpu_baseline"] = cpu_baseline(args.workload, onehot=onehot)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -376,6 +393,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per launch of the verify kernel, if captured")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scheme", default="accept", choices=["accept", "onehot"],
+                    help="accept: spec_verify (accept test against q); onehot: spec_verify_onehot")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

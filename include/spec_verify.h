@@ -130,6 +130,36 @@ sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const fl
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify_onehot -- verify drafts proposed as one-hot (argmax) tokens.
+ *
+ * FreeToken PR #836, section "Design": when the draft model proposes its argmax, q_i is one-hot
+ * at x_i, and sampling every verify row exactly as a decode step would (with the request's
+ * temperature, top-k, top-p, greedy flag and the penalties of the drafts before the row), then
+ * keeping the drafts while they equal those samples, is exact rejection sampling.  It reaches
+ * the same distribution as spec_verify given one-hot q rows (accept with probability p_i(x_i);
+ * at a rejection draw from p_i without x_i), but it uses the uniforms differently and reads no
+ * q at all.
+ *
+ *   Arguments, layout and results are those of spec_verify, without draft_probs:
+ *   uniforms       device fp32 [total_rows, 2]; only slot 1 is read: slot 1 of row i is row i's
+ *                  sample (t_i = inverse CDF of p_i at u_{i,1}).  Slot 0 is not read or checked.
+ *                  Greedy requests read none (their sample is the row's argmax).
+ *   accept_len     a_b = the first i < k_b with t_i != x_i, else k_b.
+ *   out_tokens     x_0 .. x_{a-1}, then t_a (the sample of the row where the request stops),
+ *                  then -1 padding.
+ *   out_pq         optional: (p_i(x_i), 1) for every draft of a sampled request (the one-hot q
+ *                  puts mass 1 on its own token); NaN for greedy requests.
+ *   workspace      sv_workspace_bytes(B, total_rows, V) bytes, as for spec_verify; spec_rollback
+ *                  applies unchanged.
+ * Errors are those of spec_verify, except that only slot 1 of the uniforms is checked.
+ */
+sv_status spec_verify_onehot(const void *target_logits, sv_dtype logits_dtype, const int32_t *draft_tokens,
+                             const int32_t *num_drafts, const int32_t *row_offsets, int32_t B, int32_t k_max,
+                             int32_t V, int32_t total_rows, sv_params params, const float *uniforms,
+                             int32_t *out_tokens, int32_t *accept_len, float *out_pq, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
  * spec_rollback -- commit the verify step to the target KV lengths.
  *
  * From "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust",

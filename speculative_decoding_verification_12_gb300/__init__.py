@@ -47,6 +47,10 @@ def lib():
         l.spec_verify.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                   C.c_int32, C.c_int32, C.c_int32, C.c_int32, SvParams, C.c_void_p,
                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+        l.spec_verify_onehot.restype = C.c_int
+        l.spec_verify_onehot.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
+                                         C.c_int32, C.c_int32, C.c_int32, C.c_int32, SvParams, C.c_void_p,
+                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
         l.spec_verify_static.restype = C.c_int
         l.spec_verify_static.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                          C.c_int32, C.c_int32, C.c_int32, C.c_int32, SvParams, C.c_void_p,
@@ -92,16 +96,10 @@ def sv_workspace_bytes(B: int, total_rows: int, V: int) -> int:
     return int(lib().sv_workspace_bytes(B, total_rows, V))
 
 
-def spec_verify(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max: int,
-                temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy, uniforms,
-                out_tokens, accept_len, out_pq, workspace, stream=None) -> None:
-    """Verify a batch of drafts (see include/spec_verify.h for the layout and semantics).
-
-    target_logits [R, V] bf16 or fp32; draft_probs [R-B, V] fp32; draft_tokens [R-B] int32;
-    num_drafts [B] int32; row_offsets [B+1] int32 or None (uniform layout);
-    per-request params [B]; uniforms [R, 2] fp32; outputs out_tokens [B, k_max+1] int32,
-    accept_len [B] int32, out_pq [R-B, 2] fp32 or None; workspace uint8 device tensor.
-    """
+def _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max, temperature, top_k,
+                  top_p, presence_penalty, frequency_penalty, greedy, uniforms, out_tokens, accept_len, out_pq,
+                  workspace):
+    """Checks the tensors of one verify call; returns (dtype code, B, V, R, SvParams)."""
     import torch
     R, V = target_logits.shape
     B = num_drafts.numel()
@@ -130,12 +128,46 @@ def spec_verify(target_logits, draft_probs, draft_tokens, num_drafts, row_offset
     _check(workspace, "workspace")
     params = SvParams(_ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(presence_penalty),
                       _ptr(frequency_penalty), _ptr(greedy))
+    return dt, B, V, R, params
+
+
+def spec_verify(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max: int,
+                temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy, uniforms,
+                out_tokens, accept_len, out_pq, workspace, stream=None) -> None:
+    """Verify a batch of drafts (see include/spec_verify.h for the layout and semantics).
+
+    target_logits [R, V] bf16 or fp32; draft_probs [R-B, V] fp32; draft_tokens [R-B] int32;
+    num_drafts [B] int32; row_offsets [B+1] int32 or None (uniform layout);
+    per-request params [B]; uniforms [R, 2] fp32; outputs out_tokens [B, k_max+1] int32,
+    accept_len [B] int32, out_pq [R-B, 2] fp32 or None; workspace uint8 device tensor.
+    """
+    dt, B, V, R, params = _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max,
+                                        temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy,
+                                        uniforms, out_tokens, accept_len, out_pq, workspace)
     st = lib().spec_verify(_ptr(target_logits), dt, _ptr(draft_probs), _ptr(draft_tokens), _ptr(num_drafts),
                            _ptr(row_offsets), B, k_max, V, R, params, _ptr(uniforms), _ptr(out_tokens),
                            _ptr(accept_len), _ptr(out_pq), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream))
     if st != SV_OK:
         raise SvError(st, "spec_verify")
+
+
+def spec_verify_onehot(target_logits, draft_tokens, num_drafts, row_offsets, k_max: int, temperature, top_k,
+                       top_p, presence_penalty, frequency_penalty, greedy, uniforms, out_tokens, accept_len,
+                       out_pq, workspace, stream=None) -> None:
+    """Verify drafts proposed as one-hot (argmax) tokens: every row is sampled with slot 1 of
+    its uniforms and the drafts are kept while they equal the samples; no q is read (see
+    include/spec_verify.h).  Arguments as spec_verify without draft_probs; out_pq receives
+    (p(x_i), 1)."""
+    dt, B, V, R, params = _checked_args(target_logits, None, draft_tokens, num_drafts, row_offsets, k_max,
+                                        temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy,
+                                        uniforms, out_tokens, accept_len, out_pq, workspace)
+    st = lib().spec_verify_onehot(_ptr(target_logits), dt, _ptr(draft_tokens), _ptr(num_drafts),
+                                  _ptr(row_offsets), B, k_max, V, R, params, _ptr(uniforms), _ptr(out_tokens),
+                                  _ptr(accept_len), _ptr(out_pq), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != SV_OK:
+        raise SvError(st, "spec_verify_onehot")
 
 
 def spec_rollback(kv_seq_len, accept_len, num_drafts, workspace, stream=None) -> None:

@@ -11,7 +11,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import sv_workspace_bytes, spec_verify
+from . import sv_workspace_bytes, spec_verify, spec_verify_onehot
 
 
 def _t(a: Optional[np.ndarray], device, dtype=None):
@@ -70,8 +70,16 @@ class DeviceBatch:
                    greedy=_t(w.greedy, device, torch.uint8),
                    uniforms=_t(w.uniforms, device, torch.float32), want_pq=want_pq)
 
-    def run(self, stream=None, target_logits=None, draft_probs=None) -> None:
-        """Enqueue one verification (optionally on other copies of the two large inputs)."""
+    def run(self, stream=None, target_logits=None, draft_probs=None, onehot=False) -> None:
+        """Enqueue one verification (optionally on other copies of the two large inputs).
+        onehot=True runs the one-hot-draft scheme, which reads no draft_probs."""
+        if onehot:
+            spec_verify_onehot(self.target_logits if target_logits is None else target_logits,
+                               self.draft_tokens, self.num_drafts, self.row_offsets, self.k_max,
+                               self.temperature, self.top_k, self.top_p, self.presence, self.frequency,
+                               self.greedy, self.uniforms, self.out_tokens, self.accept_len, self.out_pq,
+                               self.workspace, stream)
+            return
         spec_verify(self.target_logits if target_logits is None else target_logits,
                     self.draft_probs if draft_probs is None else draft_probs,
                     self.draft_tokens, self.num_drafts, self.row_offsets, self.k_max,
@@ -86,24 +94,29 @@ class DeviceBatch:
         return out
 
 
-def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None):
-    """A zero-argument callable that enqueues spec_verify for `db` with every pointer already
-    marshalled (for tight timing loops; argument checks happen once, here)."""
-    import ctypes as C
+def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None, onehot=False):
+    """A zero-argument callable that enqueues spec_verify (spec_verify_onehot with onehot=True)
+    for `db` with every pointer already marshalled (for tight timing loops; argument checks
+    happen once, here)."""
     from . import SV_BF16, SV_F32, SV_OK, SvError, SvParams, lib
     tl = db.target_logits if target_logits is None else target_logits
     dp = db.draft_probs if draft_probs is None else draft_probs
     # one checked call validates shapes and pointers
-    spec_verify(tl, dp, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k,
-                db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens, db.accept_len,
-                db.out_pq, db.workspace, stream)
+    if onehot:
+        spec_verify_onehot(tl, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k,
+                           db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens,
+                           db.accept_len, db.out_pq, db.workspace, stream)
+    else:
+        spec_verify(tl, dp, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k,
+                    db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens, db.accept_len,
+                    db.out_pq, db.workspace, stream)
     p = lambda t: None if t is None else t.data_ptr()
     params = SvParams(p(db.temperature), p(db.top_k), p(db.top_p), p(db.presence), p(db.frequency), p(db.greedy))
-    args = (p(tl), SV_BF16 if tl.dtype == torch.bfloat16 else SV_F32, p(dp), p(db.draft_tokens),
-            p(db.num_drafts), p(db.row_offsets), db.B, db.k_max, db.V, db.R, params, p(db.uniforms),
-            p(db.out_tokens), p(db.accept_len), p(db.out_pq), p(db.workspace), db.workspace.numel(),
-            getattr(stream, "cuda_stream", stream))
-    f = lib().spec_verify
+    head = (p(tl), SV_BF16 if tl.dtype == torch.bfloat16 else SV_F32) + (() if onehot else (p(dp),))
+    args = head + (p(db.draft_tokens), p(db.num_drafts), p(db.row_offsets), db.B, db.k_max, db.V, db.R, params,
+                   p(db.uniforms), p(db.out_tokens), p(db.accept_len), p(db.out_pq), p(db.workspace),
+                   db.workspace.numel(), getattr(stream, "cuda_stream", stream))
+    f = lib().spec_verify_onehot if onehot else lib().spec_verify
 
     def call():
         st = f(*args)

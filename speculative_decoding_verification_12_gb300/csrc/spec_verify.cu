@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
             x = __ldg(A.tokens + S.d0 + S.i);
             if (x >= 0 && x < A.V) {
                 zraw = __ldg(row + x);
-                if (!S.greedy) qx = __ldg(A.q + (size_t)(S.d0 + S.i) * A.V + x);
+                if (!S.greedy) qx = A.onehot ? 1.f : __ldg(A.q + (size_t)(S.d0 + S.i) * A.V + x);
             }
         }
         pass_stats<E, VEC>(g, S, row, A.V, A.nseg, o);
@@ -477,18 +477,21 @@ extern "C" const char *sv_status_string(sv_status s) {
     return "unknown status";
 }
 
-extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
-                                 const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
-                                 int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
-                                 const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
-                                 void *workspace, size_t workspace_bytes, void *stream) {
+// Both verification schemes: onehot == false is the accept test against q; onehot == true
+// samples every row and keeps the drafts that equal the samples (draft_probs unused).
+static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                             const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
+                             int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                             const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
+                             void *workspace, size_t workspace_bytes, void *stream, bool onehot) {
+    if (onehot) draft_probs = nullptr;
     if (B < 1 || k_max < 0 || V < 1 || total_rows < B) return SV_ERR_INVALID_ARG;
     if (k_max > MAXK || V > MAXV) return SV_ERR_UNSUPPORTED;
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (!row_offsets && (long long)total_rows != (long long)B * (k_max + 1)) return SV_ERR_INVALID_ARG;
     const int D = total_rows - B;
     if (!target_logits || !num_drafts || !uniforms || !out_tokens || !accept_len || !workspace) return SV_ERR_INVALID_ARG;
-    if (D > 0 && (!draft_probs || !draft_tokens)) return SV_ERR_INVALID_ARG;
+    if (D > 0 && ((!onehot && !draft_probs) || !draft_tokens)) return SV_ERR_INVALID_ARG;
     if (!params.temperature || !params.top_k || !params.top_p || !params.greedy) return SV_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(B, total_rows, V);
     if (((uintptr_t)workspace & 255) != 0 || workspace_bytes < L.total) return SV_ERR_WORKSPACE;
@@ -526,6 +529,7 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
     A.pns = 0;
     A.nparts = 1;
     A.nsplit = 0;
+    A.onehot = onehot ? 1 : 0;
     const size_t esz = logits_dtype == SV_BF16 ? 2 : 4;
     const bool vec = ((uintptr_t)target_logits % 16 == 0) && ((size_t)V * esz) % 16 == 0;
     const bool qvec = (!draft_probs || (uintptr_t)draft_probs % 16 == 0) && ((size_t)V * 4) % 16 == 0;
@@ -550,6 +554,26 @@ extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtyp
         }
     }
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                                 const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
+                                 int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                                 const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+    return verify_call(target_logits, logits_dtype, draft_probs, draft_tokens, num_drafts, row_offsets, B, k_max, V,
+                       total_rows, params, uniforms, out_tokens, accept_len, out_pq, workspace, workspace_bytes,
+                       stream, false);
+}
+
+extern "C" sv_status spec_verify_onehot(const void *target_logits, sv_dtype logits_dtype, const int32_t *draft_tokens,
+                                        const int32_t *num_drafts, const int32_t *row_offsets, int32_t B,
+                                        int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                                        const float *uniforms, int32_t *out_tokens, int32_t *accept_len,
+                                        float *out_pq, void *workspace, size_t workspace_bytes, void *stream) {
+    return verify_call(target_logits, logits_dtype, nullptr, draft_tokens, num_drafts, row_offsets, B, k_max, V,
+                       total_rows, params, uniforms, out_tokens, accept_len, out_pq, workspace, workspace_bytes,
+                       stream, true);
 }
 
 extern "C" sv_status spec_rollback(int32_t *kv_seq_len, const int32_t *accept_len, const int32_t *num_drafts,

@@ -169,6 +169,8 @@ struct Args {
     int pns;                  // stream kernel: ring stages
     int nparts;               // stream kernel: parts each split row is cut into (1: none)
     int nsplit;               // stream kernel: the last nsplit rows are split
+    int onehot;               // 1: one-hot drafts -- every row is sampled and the drafts are
+                              // accepted while they equal the samples (q is not read)
 };
 
 }  // namespace sv

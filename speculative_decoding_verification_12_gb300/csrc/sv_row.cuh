@@ -29,7 +29,8 @@ struct __align__(16) RowCtx {
     int npen;
     int xtok;       // the row's draft token (-1 if none), its penalised target value and q value
     float zx, qx;
-    float u1;       // slot-1 uniform of the row (sampled rows: extra-token or residual draw)
+    float u1;       // slot-1 uniform of the row (sampled rows: extra-token, residual or
+                    // one-hot-scheme draw)
     int tix;        // index of the row's (or unit's) timing record
     int pad0[6];
     int pid[MAXK];
@@ -263,7 +264,7 @@ __device__ __forceinline__ void prefetch_draft(const Args &A, RowCtx &S, const E
         x = __ldg(A.tokens + S.d0 + S.i);
         if (x >= 0 && x < A.V) {
             const E raw = __ldg(row + x);
-            if (!S.greedy) qx = __ldg(A.q + (size_t)(S.d0 + S.i) * A.V + x);
+            if (!S.greedy) qx = A.onehot ? 1.f : __ldg(A.q + (size_t)(S.d0 + S.i) * A.V + x);
             zx = elem_z_raw(S, raw, x);
         }
     }

@@ -418,7 +418,7 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
         // rank sort by (value desc, token asc): keys are distinct, so ranks are a permutation.
         // q of each candidate (the residual needs it on the kept list) is gathered meanwhile.
         unsigned long long *srt = X.sorted;
-        const bool want_resid = S.i < S.k;
+        const bool want_resid = S.i < S.k && !A.onehot;
         const float *qrow = A.q + (size_t)(S.d0 + S.i) * V;
         float *qs = X.aux2;           // q at sorted positions
         float *lq = X.aux2 + WCAP;    // q in token order
@@ -528,7 +528,7 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
             int j = draw_small(g, X.aux, X.aux2, n2, u, S);
             st.bonus = j >= 0 ? (int32_t)(~(uint32_t)(X.cand[j] >> 32)) : -1;
         }
-        if (n2 <= LCAP && S.i < S.k) {
+        if (n2 <= LCAP && S.i < S.k && !A.onehot) {
             // the residual draw should the row's draft be rejected (as in the small-set path)
             int *ltok = reinterpret_cast<int *>(X.aux2) + CAP / 2;
             for (int j = g.t; j < n2; j += G::kThreads) ltok[j] = (int)(~(uint32_t)(X.cand[j] >> 32));
@@ -586,7 +586,8 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
     st.m = 0.f; st.s = 0.f; st.tau = -INFINITY; st.Z = 1.f; st.invZ = 1.f; st.taukey = 0;
     st.argmax = -1; st.bonus = -1; st.kind = KIND_SKIP; st.nlist = 0; st.resid = -1; st.pad1 = 0;
     const bool sampled = !S.greedy;
-    const bool want_bonus = sampled && S.i == S.k;
+    // the row's own sample: the extra token of row k, or under the one-hot scheme every row's
+    const bool want_bonus = sampled && (S.i == S.k || A.onehot);
     const float s = S.s;
     float m;
     if (!sampled && argkey) {
@@ -709,6 +710,8 @@ __device__ __forceinline__ bool accept_test(float p, float q, float u) {
 
 // Request phase, run by the group that completed the request's last row: validate, find the
 // first rejection (one lane per draft, ballot), pick the final token, write the outputs.
+// Under the one-hot scheme a draft is rejected when it differs from its row's own sample, and
+// the final token is the stopping row's sample.
 template <typename E, bool VEC, bool QVEC, class G>
 __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
     const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
@@ -741,6 +744,8 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
                     if (x < 0 || x >= V) badtok = true;
                     if (greedy) {
                         rej = x != argm;
+                    } else if (A.onehot) {
+                        rej = x != bonus;   // the row's own sample
                     } else {
                         const float p = __ldcg(A.pq + (size_t)(d0 + i) * 2);
                         const float q = __ldcg(A.pq + (size_t)(d0 + i) * 2 + 1);
@@ -748,7 +753,9 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
                     }
                 }
                 if (!greedy && i <= k) {
-                    const float u0 = __ldg(A.uni + (size_t)(r0 + i) * 2), u1 = __ldg(A.uni + (size_t)(r0 + i) * 2 + 1);
+                    // the one-hot scheme reads only the draw slot
+                    const float u0 = A.onehot ? 0.f : __ldg(A.uni + (size_t)(r0 + i) * 2);
+                    const float u1 = __ldg(A.uni + (size_t)(r0 + i) * 2 + 1);
                     if (!(u0 >= 0.f && u0 < 1.f) || !(u1 >= 0.f && u1 < 1.f)) baduni = true;
                 }
                 const unsigned msk = __ballot_sync(0xffffffffu, rej);
@@ -764,7 +771,7 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
                     const int bonus_a = __shfl_sync(0xffffffffu, bonus, stop);
                     const int resid_a = __shfl_sync(0xffffffffu, resid, stop);
                     if (greedy) tok = argm_a;
-                    else if (a == k) tok = bonus_a;
+                    else if (a == k || A.onehot) tok = bonus_a;
                     else if (kind_a == KIND_LIST) tok = resid_a;   // drawn speculatively with the row
                     else need = 1;
                 }

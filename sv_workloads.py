@@ -318,6 +318,15 @@ def _pack(name, V, k_max, dtype, varlen, idx, sc, parts) -> Workload:
                     frequency=pick(sc["frequency"]), greedy=pick(sc["greedy"]))
 
 
+def with_argmax_drafts(w: Workload) -> Workload:
+    """The same batch with every draft token replaced by the argmax of its draft row's q: the
+    draft proposer proposing its most likely token, which is the input of the one-hot-draft
+    scheme (that scheme then reads no q).  Ties go to the lowest id.  Modifies w in place."""
+    if w.draft_tokens.size:
+        w.draft_tokens[:] = np.argmax(w.draft_probs, axis=1).astype(np.int32)
+    return w
+
+
 def layout(name: str):
     """(num_drafts, row_offsets or None, total_rows, total_drafts) of a full workload, cheaply."""
     sp = spec(name)

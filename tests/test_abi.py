@@ -76,6 +76,20 @@ def test_host_checks_reject_bad_calls(libsv):
     assert call(P=libsv.SvParams(None, 1, 1, None, None, 1)) == libsv.SV_ERR_INVALID_ARG
     assert call(ws=C.c_void_p(257)) == libsv.SV_ERR_WORKSPACE
     assert call(wsb=100) == libsv.SV_ERR_WORKSPACE
+    # the one-hot entry point: the same host checks, without draft_probs
+
+    def call1(**kw):
+        a = dict(base, **kw)
+        return l.spec_verify_onehot(a["tl"], a["dt"], a["tok"], a["nd"], a["ro"], a["B"], a["k"], a["V"], a["R"],
+                                    a.get("P", P), a["u"], a["ot"], a["al"], None, a.get("ws", ws),
+                                    a.get("wsb", 1 << 30), None)
+
+    assert call1(B=0) == libsv.SV_ERR_INVALID_ARG
+    assert call1(k=65, R=2 * 66) == libsv.SV_ERR_UNSUPPORTED
+    assert call1(R=11) == libsv.SV_ERR_INVALID_ARG
+    assert call1(tok=None) == libsv.SV_ERR_INVALID_ARG        # drafts are still needed
+    assert call1(u=None) == libsv.SV_ERR_INVALID_ARG
+    assert call1(wsb=100) == libsv.SV_ERR_WORKSPACE
     assert l.spec_rollback(None, C.c_void_p(16), C.c_void_p(16), 4, ws, None) == libsv.SV_ERR_INVALID_ARG
     assert l.sv_status_string(libsv.SV_ERR_WORKSPACE) == b"workspace too small or misaligned"
     # the measurement hook takes both events or neither (nothing is recorded by these calls)
