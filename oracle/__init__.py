@@ -18,6 +18,7 @@ _SRC = os.path.join(_HERE, "sv_oracle.c")
 _LIB = os.path.join(_HERE, "libsvoracle.so")
 
 ERR_LAYOUT, ERR_TOKEN, ERR_TEMP, ERR_TOPP, ERR_UNIFORM, ERR_PENALTY = 1, 2, 3, 4, 5, 6
+ERR_HISTORY = 8
 
 
 def build(force: bool = False) -> str:
@@ -36,7 +37,8 @@ class _Batch(C.Structure):
                 ("target_logits", C.c_void_p), ("draft_probs", C.c_void_p), ("draft_tokens", C.c_void_p),
                 ("num_drafts", C.c_void_p), ("row_offsets", C.c_void_p), ("temperature", C.c_void_p),
                 ("top_k", C.c_void_p), ("top_p", C.c_void_p), ("presence", C.c_void_p),
-                ("frequency", C.c_void_p), ("greedy", C.c_void_p), ("uniforms", C.c_void_p)]
+                ("frequency", C.c_void_p), ("greedy", C.c_void_p), ("uniforms", C.c_void_p),
+                ("prior_offsets", C.c_void_p), ("prior_tokens", C.c_void_p), ("prior_counts", C.c_void_p)]
 
 
 DIAG_FIELDS = ("decisions", "near_ties", "error", "near_accept", "near_cdf", "near_filter", "near_argmax",
@@ -90,7 +92,10 @@ class _Held:
             T=c(w.temperature, dtype=np.float32), tk=c(w.top_k, dtype=np.int32), tp=c(w.top_p, dtype=np.float32),
             pr=None if w.presence is None else c(w.presence, dtype=np.float32),
             fr=None if w.frequency is None else c(w.frequency, dtype=np.float32),
-            g=c(w.greedy, dtype=np.uint8), u=c(w.uniforms, dtype=np.float32))
+            g=c(w.greedy, dtype=np.uint8), u=c(w.uniforms, dtype=np.float32),
+            ho=None if getattr(w, "prior_offsets", None) is None else c(w.prior_offsets, dtype=np.int32),
+            ht=None if getattr(w, "prior_offsets", None) is None else c(w.prior_tokens, dtype=np.int32),
+            hc=None if getattr(w, "prior_offsets", None) is None else c(w.prior_counts, dtype=np.int32))
         a = self.arrays
         if w.dtype == "bf16":
             assert a["tl"].dtype == np.uint16
@@ -99,7 +104,7 @@ class _Held:
         self.batch = _Batch(w.B, w.k_max, w.V, w.total_rows, 1 if w.dtype == "bf16" else 0,
                             _ptr(a["tl"]), _ptr(a["dp"]), _ptr(a["dt"]), _ptr(a["nd"]), _ptr(a["ro"]),
                             _ptr(a["T"]), _ptr(a["tk"]), _ptr(a["tp"]), _ptr(a["pr"]), _ptr(a["fr"]),
-                            _ptr(a["g"]), _ptr(a["u"]))
+                            _ptr(a["g"]), _ptr(a["u"]), _ptr(a["ho"]), _ptr(a["ht"]), _ptr(a["hc"]))
 
 
 def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1, onehot: bool = False):

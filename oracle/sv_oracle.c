@@ -33,7 +33,9 @@
  *  - accept iff u < min(1, p/q) with no epsilon in the denominator; q == 0 < p accepts,
  *    p == 0 always rejects.
  *  - penalties are additive: z_v = logit_v - presence*[c_v > 0] - frequency*c_v, where c_v
- *    counts v among d_0..d_{i-1}; they apply before temperature and filtering, greedy rows too.
+ *    counts v among d_0..d_{i-1} plus the request's prior history count of v (an optional
+ *    input: distinct ascending ids with counts >= 1); they apply before temperature and
+ *    filtering, greedy rows too.
  *  - top-k keeps every token whose scaled logit is >= the k-th largest (ties kept); k <= 0 or
  *    k >= V disables it.  top-p then keeps v iff the renormalised mass of tokens strictly
  *    more likely than v is < top_p; top_p >= 1 disables it.  The kept set is renormalised.
@@ -75,6 +77,11 @@ typedef struct sv_oracle_batch {
     const float *frequency;       /* [B] or NULL */
     const uint8_t *greedy;        /* [B] */
     const float *uniforms;        /* [total_rows, 2] */
+    /* prior history, or NULL: request b generated tokens prior_tokens[o_b .. o_{b+1}) (distinct,
+     * ascending) prior_counts[] times each, o = prior_offsets */
+    const int32_t *prior_offsets; /* [B+1] */
+    const int32_t *prior_tokens;
+    const int32_t *prior_counts;
 } sv_oracle_batch;
 
 typedef struct sv_oracle_diag {
@@ -84,7 +91,7 @@ typedef struct sv_oracle_diag {
     int32_t near_accept, near_cdf, near_filter, near_argmax, near_w;  /* near_ties by kind */
 } sv_oracle_diag;
 
-enum { E_OK = 0, E_LAYOUT = 1, E_TOKEN = 2, E_TEMP = 3, E_TOPP = 4, E_UNIFORM = 5, E_PENALTY = 6 };
+enum { E_OK = 0, E_LAYOUT = 1, E_TOKEN = 2, E_TEMP = 3, E_TOPP = 4, E_UNIFORM = 5, E_PENALTY = 6, E_HISTORY = 8 };
 
 /* ---------------------------------------------------------------------------------- */
 
@@ -126,6 +133,16 @@ static int check_request_slots(const sv_oracle_batch *in, int32_t b, int slot_lo
     }
     if (in->presence && !isfinite(in->presence[b])) return E_PENALTY;
     if (in->frequency && !isfinite(in->frequency[b])) return E_PENALTY;
+    if (in->prior_offsets) {
+        /* the history: ascending distinct ids in [0, V), each with a count >= 1 */
+        int32_t lo = in->prior_offsets[b], hi = in->prior_offsets[b + 1];
+        if (lo < 0 || hi < lo || (b == 0 && lo != 0)) return E_HISTORY;
+        for (int32_t j = lo; j < hi; j++) {
+            int32_t x = in->prior_tokens[j];
+            if (x < 0 || x >= in->V || in->prior_counts[j] < 1) return E_HISTORY;
+            if (j > lo && in->prior_tokens[j - 1] >= x) return E_HISTORY;
+        }
+    }
     if (!in->greedy[b]) {
         float T = in->temperature[b];
         if (!(T > 0.0f) || !isfinite(T)) return E_TEMP;
@@ -142,22 +159,41 @@ static int check_request_slots(const sv_oracle_batch *in, int32_t b, int slot_lo
 
 static int check_request(const sv_oracle_batch *in, int32_t b) { return check_request_slots(in, b, 0); }
 
-/* z_v for row i of request b: the logit minus the presence/frequency penalty of the drafts
- * d_0..d_{i-1} [F1].  Returns 1 when some token of the row carries a nonzero penalty. */
+/* Count of token v in request b's prior history (0 without one). */
+static int32_t prior_count(const sv_oracle_batch *in, int32_t b, int32_t v) {
+    if (!in->prior_offsets) return 0;
+    for (int32_t j = in->prior_offsets[b]; j < in->prior_offsets[b + 1]; j++)
+        if (in->prior_tokens[j] == v) return in->prior_counts[j];
+    return 0;
+}
+
+/* z_v for row i of request b: the logit minus the presence/frequency penalty of what the
+ * request generated before the row -- its prior history and the drafts d_0..d_{i-1}, which
+ * count as already generated [F1]: c_v = prior_v + #{j < i : d_j = v}.  Returns 1 when some
+ * token of the row carries a nonzero penalty. */
 static int row_logits(const sv_oracle_batch *in, int32_t b, int32_t i, double *z) {
     int64_t row = row_start(in, b) + i;
     for (int32_t v = 0; v < in->V; v++) z[v] = logit_at(in, row, v);
     double pres = in->presence ? in->presence[b] : 0.0;
     double freq = in->frequency ? in->frequency[b] : 0.0;
-    if (i == 0 || (pres == 0.0 && freq == 0.0)) return 0;
+    if (pres == 0.0 && freq == 0.0) return 0;
     const int32_t *d = in->draft_tokens + (row_start(in, b) - b);
+    const int32_t h0 = in->prior_offsets ? in->prior_offsets[b] : 0;
+    const int32_t nh = in->prior_offsets ? in->prior_offsets[b + 1] - h0 : 0;
     int penalised = 0;
-    for (int32_t j = 0; j < i; j++) {
-        int32_t v = d[j];
-        int seen = 0;
-        for (int32_t t = 0; t < j; t++) seen |= (d[t] == v);
-        if (seen) continue;             /* apply once per distinct token */
-        int32_t c = 0;
+    /* every distinct token generated before the row: the history's, then the drafts' */
+    for (int32_t e = 0; e < nh + i; e++) {
+        int32_t v;
+        if (e < nh) {
+            v = in->prior_tokens[h0 + e];
+        } else {
+            int32_t j = e - nh;
+            v = d[j];
+            int seen = prior_count(in, b, v) > 0;
+            for (int32_t t = 0; t < j; t++) seen |= (d[t] == v);
+            if (seen) continue;             /* apply once per distinct token */
+        }
+        int32_t c = prior_count(in, b, v);
         for (int32_t t = 0; t < i; t++) c += (d[t] == v);
         double pen = pres * (c > 0 ? 1.0 : 0.0) + freq * (double)c;
         z[v] -= pen;

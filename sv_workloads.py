@@ -65,6 +65,11 @@ class Workload:
     presence: Optional[np.ndarray]  # [B] float32 or None
     frequency: Optional[np.ndarray]  # [B] float32 or None
     greedy: np.ndarray              # [B] uint8
+    # the requests' prior history for the penalties, or None: request b generated the tokens
+    # prior_tokens[o_b:o_{b+1}] (distinct, ascending) prior_counts[...] times each
+    prior_offsets: Optional[np.ndarray] = None   # [B+1] int32
+    prior_tokens: Optional[np.ndarray] = None    # [H] int32
+    prior_counts: Optional[np.ndarray] = None    # [H] int32
 
     @property
     def B(self) -> int:
@@ -316,6 +321,37 @@ def _pack(name, V, k_max, dtype, varlen, idx, sc, parts) -> Workload:
                     temperature=pick(sc["temperature"]), top_k=pick(sc["top_k"]),
                     top_p=pick(sc["top_p"]), presence=pick(sc["presence"]),
                     frequency=pick(sc["frequency"]), greedy=pick(sc["greedy"]))
+
+
+def with_history(w: Workload, seed: int, max_len: int, top_share: float = 0.5) -> Workload:
+    """Attach a seeded prior history to every request (in place): up to max_len distinct
+    tokens, about `top_share` of them among the largest logits of the request's first row (so
+    that they meet the kept sets and the drafts) and the rest uniform over the vocabulary,
+    each with a count of 1 + Geometric(0.5).  Some requests get an empty history."""
+    offs = np.zeros(w.B + 1, np.int32)
+    toks, cnts = [], []
+    lg = w.logits_f32()
+    for b in range(w.B):
+        r = _rng(7_400_000 + seed, b)
+        n = int(r.integers(0, max_len + 1)) if r.random() < 0.85 else 0
+        n = min(n, w.V)
+        n_top = min(int(round(n * top_share)), w.V)
+        top = np.argsort(-lg[w.row_start(b)], kind="stable")[: max(n_top * 2, 1)]
+        pick = set(r.choice(top, size=min(n_top, top.size), replace=False).tolist()) if n_top else set()
+        d0 = w.draft_start(b)
+        k = int(w.num_drafts[b])
+        if k and r.random() < 0.5:
+            pick.add(int(w.draft_tokens[d0 + int(r.integers(0, k))]))   # a drafted token too
+        while len(pick) < n:
+            pick.add(int(r.integers(0, w.V)))
+        t = np.array(sorted(pick), np.int32)
+        toks.append(t)
+        cnts.append((1 + r.geometric(0.5, size=t.size) - 1).astype(np.int32).clip(1, None))
+        offs[b + 1] = offs[b] + t.size
+    w.prior_offsets = offs
+    w.prior_tokens = np.concatenate(toks).astype(np.int32) if toks else np.zeros(0, np.int32)
+    w.prior_counts = np.concatenate(cnts).astype(np.int32) if cnts else np.zeros(0, np.int32)
+    return w
 
 
 def with_argmax_drafts(w: Workload) -> Workload:

@@ -30,8 +30,8 @@ MUTATIONS = [
     ("frequency penalty dropped", "double pen = pres * (c > 0 ? 1.0 : 0.0) + freq * (double)c;",
      "double pen = pres * (c > 0 ? 1.0 : 0.0);", [lambda o: pins.test_softmax_against_numpy(o)]),
     ("penalty counts the row's own draft",
-     [("for (int32_t j = 0; j < i; j++) {\n        int32_t v = d[j];",
-       "int32_t i1 = i < in->num_drafts[b] ? i + 1 : i;\n    for (int32_t j = 0; j < i1; j++) {\n        int32_t v = d[j];"),
+     [("for (int32_t e = 0; e < nh + i; e++) {",
+       "int32_t i1 = i < in->num_drafts[b] ? i + 1 : i;\n    for (int32_t e = 0; e < nh + i1; e++) {"),
       ("for (int32_t t = 0; t < i; t++) c += (d[t] == v);", "for (int32_t t = 0; t < i1; t++) c += (d[t] == v);")],
      None, [lambda o: pins.test_softmax_against_numpy(o)]),
     ("repeat counts capped at one", "for (int32_t t = 0; t < i; t++) c += (d[t] == v);",
@@ -44,7 +44,7 @@ MUTATIONS = [
      [lambda o: pins.test_filters_brute_force(o, 0), lambda o: pins.test_filters_edge_cases(o)]),
     ("top-p counts the level's own mass", "if (!cut && above / ZK < P) {",
      "if (!cut && (above + lm) / ZK < P) {",
-     [lambda o: pins.test_filters_brute_force(o, s) for s in range(8)]),
+     [lambda o, s=s: pins.test_filters_brute_force(o, s) for s in range(8)]),
     ("top-p normalised over the unfiltered row", "ZK += (p[v] >= tau) ? exp(p[v] - m) : 0.0;",
      "ZK += exp(p[v] - m);", [lambda o: pins.test_filters_edge_cases(o)]),
     ("draft row index shifted", "double qx = (double)in->draft_probs[(d0 + i) * (int64_t)V + x];",
@@ -73,6 +73,16 @@ MUTATIONS = [
      "if (i == k || (i + 1 < k && drafts[i] != t)) {",
      [lambda o: pins.test_onehot_matches_when_every_sample_matches(o),
       lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None)]),
+    ("history: its counts dropped", "int32_t c = prior_count(in, b, v);\n        for", "int32_t c = 0;\n        for",
+     [lambda o: pins.test_history_softmax_against_numpy(o)]),
+    ("history: drafts not added to its counts", "for (int32_t t = 0; t < i; t++) c += (d[t] == v);",
+     "if (e >= nh) for (int32_t t = 0; t < i; t++) c += (d[t] == v);",
+     [lambda o, s=s: pins.test_history_is_earlier_drafts(o, s) for s in range(4)]),
+    ("history: drafted tokens penalised twice", "int seen = prior_count(in, b, v) > 0;", "int seen = 0;",
+     [lambda o, s=s: pins.test_history_is_earlier_drafts(o, s) for s in range(4)]),
+    ("history: ignored on row 0", "for (int32_t e = 0; e < nh + i; e++) {",
+     "for (int32_t e = (i == 0 ? nh : 0); e < nh + i; e++) {",
+     [lambda o: pins.test_history_softmax_against_numpy(o), lambda o: pins.test_history_greedy_against_numpy(o)]),
     ("rollback keeps one row too many", "int64_t t = L - (k + 1) + 1 + a;", "int64_t t = L - (k + 1) + 2 + a;",
      [lambda o: pins.test_rollback_closed_form(o)]),
 ]

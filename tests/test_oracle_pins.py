@@ -589,3 +589,118 @@ def test_onehot_matches_when_every_sample_matches(oracle_lib):
     w2 = W.from_rows(V, logits, np.zeros((k, V), np.float32), drafts, u, temperature=0.9, top_p=0.95)
     r2 = oracle_lib.verify(w2, onehot=True)
     assert r2["accept_len"][0] == 2 and r2["out_tokens"][0, 2] == (drafts[0, 2] - 1) % V
+
+
+# ------------------------------------------------------------------------------------------
+# P10: prior history in the penalties (FreeToken PR #836, Design: what the request generated
+# before a row counts as generated; the history extends that to the tokens before the drafts)
+# ------------------------------------------------------------------------------------------
+
+def _history_request(V, logits, drafts, uni, hist, pres, freq, T=0.9, K=0, P=1.0, greedy=0):
+    """One request (uniform layout) with an explicit history {token: count}."""
+    k = drafts.shape[0]
+    w = W.from_rows(V, logits[None], np.zeros((1, k, V), np.float32), drafts[None], uni[None], temperature=T,
+                    top_k=K, top_p=P, presence=pres, frequency=freq, greedy=greedy)
+    toks = np.array(sorted(hist), np.int32)
+    w.prior_offsets = np.array([0, toks.size], np.int32)
+    w.prior_tokens = toks
+    w.prior_counts = np.array([hist[t] for t in toks.tolist()], np.int32)
+    return w
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_history_is_earlier_drafts(oracle_lib, seed):
+    """P10a: the first j drafts of a request, moved into its history as counts, leave every
+    later row unchanged: row i of the original equals row i - j of the request that starts at
+    draft j (same logits, drafts and uniforms), for sampled and greedy requests, and so do the
+    verify results.  Drafts repeat (V is small), so counts above one and tokens present both
+    in the history and among the remaining drafts occur."""
+    g = _rng(500 + seed)
+    V, k = 9, 6
+    logits = (g.standard_normal((k + 1, V)) * 1.3).astype(np.float32)
+    drafts = g.integers(0, V, k).astype(np.int32)
+    uni = g.random((k + 1, 2), dtype=np.float32)
+    pres, freq = float(g.uniform(0.1, 1.2)), float(g.uniform(0.1, 0.9))
+    for greedy in (0, 1):
+        full = _history_request(V, logits, drafts, uni, {}, pres, freq, greedy=greedy, K=[0, 5][seed % 2],
+                                P=[1.0, 0.85][seed // 2])
+        for j in range(1, k + 1):
+            hist = {}
+            for t in drafts[:j].tolist():
+                hist[t] = hist.get(t, 0) + 1
+            cut = _history_request(V, logits[j:], drafts[j:], uni[j:], hist, pres, freq, greedy=greedy,
+                                   K=[0, 5][seed % 2], P=[1.0, 0.85][seed // 2])
+            for i in range(j, k + 1):
+                np.testing.assert_array_equal(oracle_lib.row_probs(cut, 0, i - j), oracle_lib.row_probs(full, 0, i))
+
+
+def test_history_softmax_against_numpy(oracle_lib):
+    """P10b: with no filter, row i is numpy's float64 softmax((z - presence [c > 0] -
+    frequency c) / T) with c = history count + count among the drafts before the row; row 0
+    carries the history alone."""
+    w = W.random_batch(61, B=24, k_max=5, V=40, dtype="f32", greedy_frac=0.0, draft_sigma=0.2)
+    W.with_history(w, 61, 12)
+    w.top_k[:] = 0
+    w.top_p[:] = 1.0
+    w.presence[:] = np.linspace(0.0, 1.5, w.B).astype(np.float32)
+    w.frequency[:] = np.linspace(0.9, 0.0, w.B).astype(np.float32)
+    lg = w.logits_f32().astype(np.float64)
+    assert (np.diff(w.prior_offsets) > 0).sum() >= 10
+    for b in range(w.B):
+        r0, d0 = w.row_start(b), w.draft_start(b)
+        h = np.zeros(w.V)
+        lo, hi = w.prior_offsets[b], w.prior_offsets[b + 1]
+        h[w.prior_tokens[lo:hi]] = w.prior_counts[lo:hi]
+        for i in range(int(w.num_drafts[b]) + 1):
+            c = h + np.bincount(w.draft_tokens[d0:d0 + i], minlength=w.V)
+            z = lg[r0 + i] - (w.presence[b] * (c > 0) + w.frequency[b] * c)
+            np.testing.assert_allclose(oracle_lib.row_probs(w, b, i), _softmax(z / float(w.temperature[b])),
+                                       rtol=1e-12, atol=1e-15)
+
+
+def test_history_greedy_against_numpy(oracle_lib):
+    """P10c: a greedy request with a history accepts while the draft is numpy's argmax of the
+    penalised row, the history counted on every row including row 0."""
+    w = W.random_batch(62, B=40, k_max=4, V=30, dtype="f32", greedy_frac=1.0)
+    lg = w.logits_f32().astype(np.float64)
+    for b in range(w.B):          # drafts mostly the unpenalised argmax, so the history matters
+        r0, d0 = w.row_start(b), w.draft_start(b)
+        for i in range(int(w.num_drafts[b])):
+            w.draft_tokens[d0 + i] = int(np.argmax(lg[r0 + i]))
+    W.with_history(w, 62, 8, top_share=1.0)
+    w.presence[:] = 0.8
+    w.frequency[:] = 0.3
+    r = oracle_lib.verify(w)
+    for b in range(w.B):
+        r0, d0 = w.row_start(b), w.draft_start(b)
+        h = np.zeros(w.V)
+        lo, hi = w.prior_offsets[b], w.prior_offsets[b + 1]
+        h[w.prior_tokens[lo:hi]] = w.prior_counts[lo:hi]
+        a = 0
+        k = int(w.num_drafts[b])
+        while True:
+            c = h + np.bincount(w.draft_tokens[d0:d0 + a], minlength=w.V)
+            am = int(np.argmax(lg[r0 + a] - (0.8 * (c > 0) + 0.3 * c)))
+            if a == k or w.draft_tokens[d0 + a] != am:
+                break
+            a += 1
+        assert r["accept_len"][b] == a and r["out_tokens"][b, a] == am, b
+
+
+def test_history_errors(oracle_lib):
+    """A malformed history (ids not ascending, a repeat, an id outside [0, V), a count below
+    one, offsets that decrease) is a device-data error (code 8) of that request only."""
+    w = W.random_batch(63, B=8, k_max=3, V=50, greedy_frac=0.0)
+    W.with_history(w, 63, 6)
+    w.prior_offsets = np.array([0, 3, 6, 9, 12, 15, 18, 21, 24], np.int32)
+    w.prior_tokens = np.tile(np.array([3, 9, 20], np.int32), 8)
+    w.prior_counts = np.ones(24, np.int32)
+    w.prior_tokens[0:3] = [9, 3, 20]       # request 0: not ascending
+    w.prior_tokens[3:6] = [3, 3, 20]       # request 1: a repeat
+    w.prior_tokens[6:9] = [3, 9, 50]       # request 2: out of range
+    w.prior_counts[10] = 0                 # request 3: count below one
+    r = oracle_lib.verify(w)
+    assert list(r["error"]) == [8, 8, 8, 8, 0, 0, 0, 0]
+    w.prior_offsets[6] = 14                # request 5 ends before it starts
+    r = oracle_lib.verify(w)
+    assert r["error"][5] == 8 and r["error"][4] == 0
