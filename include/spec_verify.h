@@ -17,7 +17,8 @@
  *    mismatch.
  *  - FreeToken PR #836, section "Design": each verify row samples with its own request's
  *    temperature, top-k, top-p and greedy flag, and presence/frequency penalties count the
- *    drafts before the row as already generated.
+ *    drafts before the row as already generated (and, given a prior history, the tokens the
+ *    request generated before its drafts).
  *
  * Conventions shared by every entry point:
  *  - Pointers named as device arrays must be CUDA device memory (or managed memory) that the
@@ -28,9 +29,10 @@
  *    is too small or misaligned) return at once with nothing enqueued.
  *  - Errors in device data (a draft token outside [0, V), num_drafts outside its range,
  *    T <= 0 or non-finite on a sampled request, top_p outside (0, 1], a uniform outside [0, 1),
- *    a non-finite penalty, inconsistent row_offsets) are found by the kernels.  The affected
- *    request's outputs become -1 and a sticky error word in the workspace records the first
- *    code; the call itself still returns SV_OK.  sv_read_device_error() fetches the word.
+ *    a non-finite penalty, inconsistent row_offsets, a malformed prior history) are found by
+ *    the kernels.  The affected request's outputs become -1 and a sticky error word in the
+ *    workspace records the first code; the call itself still returns SV_OK.
+ *    sv_read_device_error() fetches the word.
  *    No kernel traps or asserts.
  */
 #ifndef SPEC_VERIFY_H
@@ -63,7 +65,9 @@ enum {
     SV_DEV_BAD_TOP_P = 4,
     SV_DEV_BAD_UNIFORM = 5,
     SV_DEV_BAD_PENALTY = 6,
-    SV_DEV_TIMEOUT = 7        /* a row's bulk copy did not complete within 2 s (bounded wait)  */
+    SV_DEV_TIMEOUT = 7,       /* a row's bulk copy did not complete within 2 s (bounded wait)  */
+    SV_DEV_BAD_HISTORY = 8    /* prior history: offsets decrease or pass prior_len, an id outside
+                                 [0, V), ids not strictly ascending, or a count below 1      */
 };
 
 /* Per-request sampling parameters: structure of device arrays, each of length B. */
@@ -74,6 +78,16 @@ typedef struct sv_params {
     const float *presence_penalty;  /* may be NULL (all 0): subtracted once from a drafted token */
     const float *frequency_penalty; /* may be NULL (all 0): subtracted per earlier occurrence    */
     const uint8_t *greedy;          /* 1 = greedy request (argmax prefix match), 0 = sampled     */
+    /* Optional prior history of each request for the penalties (all three NULL: none).
+     * Request b generated, before its drafts, the tokens prior_tokens[o_b .. o_{b+1}) --
+     * distinct ids in [0, V), strictly ascending -- prior_counts[...] >= 1 times each, with
+     * o = prior_offsets [B+1], o_0 = 0, non-decreasing, o_B <= prior_len.  A token's penalty
+     * count on row i is its history count plus its count among the drafts before row i. */
+    const int32_t *prior_offsets;
+    const int32_t *prior_tokens;
+    const int32_t *prior_counts;
+    int32_t prior_len;              /* entries in prior_tokens / prior_counts (offsets beyond it are
+                                       SV_DEV_BAD_HISTORY); ignored without a history            */
 } sv_params;
 
 /* Size in bytes of the device workspace spec_verify and spec_rollback need for a batch of B
@@ -114,12 +128,17 @@ size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V);
  *                  of a sampled request, whether or not the loop reached it; NaN for greedy
  *                  requests.  NULL skips it.
  *   workspace      device, sv_workspace_bytes() bytes, 256-byte aligned.
+ *                  With a prior history, params.prior_tokens and prior_counts must be non-NULL
+ *                  whenever prior_offsets is (SV_ERR_INVALID_ARG otherwise); a short prepass
+ *                  kernel then checks each request's history and indexes it by 256-token
+ *                  segment in the workspace.
  *   stream         cudaStream_t.
  *
  * Per row the target distribution is p = softmax(z / T) over the tokens kept by top-k (every
  * token >= the k-th largest, ties kept) and then top-p (tokens whose renormalised mass strictly
  * above them is < top_p), renormalised; z_v = logit_v - presence * [c_v > 0] - frequency * c_v
- * with c_v the count of v among the request's drafts before the row.  A draft is accepted iff
+ * with c_v the count of v among the request's drafts before the row plus its count in the
+ * request's prior history (params.prior_*, optional).  A draft is accepted iff
  * p > 0 and (q == 0 or u < min(1, p/q)).  Draws use the inverse CDF in token-id order.
  * Arithmetic is fp32 (exp via ex2); a greedy row's argmax breaks ties toward the lowest id.
  */

@@ -38,7 +38,8 @@ class _Batch(C.Structure):
                 ("num_drafts", C.c_void_p), ("row_offsets", C.c_void_p), ("temperature", C.c_void_p),
                 ("top_k", C.c_void_p), ("top_p", C.c_void_p), ("presence", C.c_void_p),
                 ("frequency", C.c_void_p), ("greedy", C.c_void_p), ("uniforms", C.c_void_p),
-                ("prior_offsets", C.c_void_p), ("prior_tokens", C.c_void_p), ("prior_counts", C.c_void_p)]
+                ("prior_offsets", C.c_void_p), ("prior_tokens", C.c_void_p), ("prior_counts", C.c_void_p),
+                ("prior_len", C.c_int32)]
 
 
 DIAG_FIELDS = ("decisions", "near_ties", "error", "near_accept", "near_cdf", "near_filter", "near_argmax",
@@ -104,7 +105,8 @@ class _Held:
         self.batch = _Batch(w.B, w.k_max, w.V, w.total_rows, 1 if w.dtype == "bf16" else 0,
                             _ptr(a["tl"]), _ptr(a["dp"]), _ptr(a["dt"]), _ptr(a["nd"]), _ptr(a["ro"]),
                             _ptr(a["T"]), _ptr(a["tk"]), _ptr(a["tp"]), _ptr(a["pr"]), _ptr(a["fr"]),
-                            _ptr(a["g"]), _ptr(a["u"]), _ptr(a["ho"]), _ptr(a["ht"]), _ptr(a["hc"]))
+                            _ptr(a["g"]), _ptr(a["u"]), _ptr(a["ho"]), _ptr(a["ht"]), _ptr(a["hc"]),
+                            0 if a["ht"] is None else int(a["ht"].shape[0]))
 
 
 def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1, onehot: bool = False):

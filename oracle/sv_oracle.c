@@ -82,6 +82,7 @@ typedef struct sv_oracle_batch {
     const int32_t *prior_offsets; /* [B+1] */
     const int32_t *prior_tokens;
     const int32_t *prior_counts;
+    int32_t prior_len;            /* entries in prior_tokens / prior_counts */
 } sv_oracle_batch;
 
 typedef struct sv_oracle_diag {
@@ -136,7 +137,7 @@ static int check_request_slots(const sv_oracle_batch *in, int32_t b, int slot_lo
     if (in->prior_offsets) {
         /* the history: ascending distinct ids in [0, V), each with a count >= 1 */
         int32_t lo = in->prior_offsets[b], hi = in->prior_offsets[b + 1];
-        if (lo < 0 || hi < lo || (b == 0 && lo != 0)) return E_HISTORY;
+        if (lo < 0 || hi < lo || hi > in->prior_len || (b == 0 && lo != 0)) return E_HISTORY;
         for (int32_t j = lo; j < hi; j++) {
             int32_t x = in->prior_tokens[j];
             if (x < 0 || x >= in->V || in->prior_counts[j] < 1) return E_HISTORY;

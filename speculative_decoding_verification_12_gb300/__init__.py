@@ -17,12 +17,14 @@ LIB_PATH = os.path.join(HERE, "libspecverify.so")
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_UNSUPPORTED, SV_ERR_DEVICE_DATA = range(6)
 SV_F32, SV_BF16 = 0, 1
 DEV_ERRORS = {0: "ok", 1: "bad layout", 2: "bad token", 3: "bad temperature", 4: "bad top_p",
-              5: "bad uniform", 6: "bad penalty"}
+              5: "bad uniform", 6: "bad penalty", 7: "timeout", 8: "bad history"}
 
 
 class SvParams(C.Structure):
     _fields_ = [("temperature", C.c_void_p), ("top_k", C.c_void_p), ("top_p", C.c_void_p),
-                ("presence_penalty", C.c_void_p), ("frequency_penalty", C.c_void_p), ("greedy", C.c_void_p)]
+                ("presence_penalty", C.c_void_p), ("frequency_penalty", C.c_void_p), ("greedy", C.c_void_p),
+                ("prior_offsets", C.c_void_p), ("prior_tokens", C.c_void_p), ("prior_counts", C.c_void_p),
+                ("prior_len", C.c_int32)]
 
 
 class SvError(RuntimeError):
@@ -98,8 +100,9 @@ def sv_workspace_bytes(B: int, total_rows: int, V: int) -> int:
 
 def _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max, temperature, top_k,
                   top_p, presence_penalty, frequency_penalty, greedy, uniforms, out_tokens, accept_len, out_pq,
-                  workspace):
-    """Checks the tensors of one verify call; returns (dtype code, B, V, R, SvParams)."""
+                  workspace, prior=None):
+    """Checks the tensors of one verify call; returns (dtype code, B, V, R, SvParams).
+    prior is None or (prior_offsets [B+1], prior_tokens [H], prior_counts [H]) int32."""
     import torch
     R, V = target_logits.shape
     B = num_drafts.numel()
@@ -126,24 +129,34 @@ def _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offs
     _check(accept_len, "accept_len", torch.int32, B)
     _check(out_pq, "out_pq", torch.float32, D * 2)
     _check(workspace, "workspace")
+    ho = ht = hc = None
+    H = 0
+    if prior is not None:
+        ho, ht, hc = prior
+        H = ht.numel()
+        _check(ho, "prior_offsets", torch.int32, B + 1)
+        _check(ht, "prior_tokens", torch.int32, H)
+        _check(hc, "prior_counts", torch.int32, H)
     params = SvParams(_ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(presence_penalty),
-                      _ptr(frequency_penalty), _ptr(greedy))
+                      _ptr(frequency_penalty), _ptr(greedy), _ptr(ho), _ptr(ht), _ptr(hc), H)
     return dt, B, V, R, params
 
 
 def spec_verify(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max: int,
                 temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy, uniforms,
-                out_tokens, accept_len, out_pq, workspace, stream=None) -> None:
+                out_tokens, accept_len, out_pq, workspace, stream=None, prior=None) -> None:
     """Verify a batch of drafts (see include/spec_verify.h for the layout and semantics).
 
     target_logits [R, V] bf16 or fp32; draft_probs [R-B, V] fp32; draft_tokens [R-B] int32;
     num_drafts [B] int32; row_offsets [B+1] int32 or None (uniform layout);
     per-request params [B]; uniforms [R, 2] fp32; outputs out_tokens [B, k_max+1] int32,
-    accept_len [B] int32, out_pq [R-B, 2] fp32 or None; workspace uint8 device tensor.
+    accept_len [B] int32, out_pq [R-B, 2] fp32 or None; workspace uint8 device tensor;
+    prior: None or (prior_offsets [B+1], prior_tokens [H], prior_counts [H]) int32, the
+    requests' prior history for the penalties.
     """
     dt, B, V, R, params = _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max,
                                         temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy,
-                                        uniforms, out_tokens, accept_len, out_pq, workspace)
+                                        uniforms, out_tokens, accept_len, out_pq, workspace, prior)
     st = lib().spec_verify(_ptr(target_logits), dt, _ptr(draft_probs), _ptr(draft_tokens), _ptr(num_drafts),
                            _ptr(row_offsets), B, k_max, V, R, params, _ptr(uniforms), _ptr(out_tokens),
                            _ptr(accept_len), _ptr(out_pq), _ptr(workspace),
@@ -154,14 +167,14 @@ def spec_verify(target_logits, draft_probs, draft_tokens, num_drafts, row_offset
 
 def spec_verify_onehot(target_logits, draft_tokens, num_drafts, row_offsets, k_max: int, temperature, top_k,
                        top_p, presence_penalty, frequency_penalty, greedy, uniforms, out_tokens, accept_len,
-                       out_pq, workspace, stream=None) -> None:
+                       out_pq, workspace, stream=None, prior=None) -> None:
     """Verify drafts proposed as one-hot (argmax) tokens: every row is sampled with slot 1 of
     its uniforms and the drafts are kept while they equal the samples; no q is read (see
     include/spec_verify.h).  Arguments as spec_verify without draft_probs; out_pq receives
     (p(x_i), 1)."""
     dt, B, V, R, params = _checked_args(target_logits, None, draft_tokens, num_drafts, row_offsets, k_max,
                                         temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy,
-                                        uniforms, out_tokens, accept_len, out_pq, workspace)
+                                        uniforms, out_tokens, accept_len, out_pq, workspace, prior)
     st = lib().spec_verify_onehot(_ptr(target_logits), dt, _ptr(draft_tokens), _ptr(num_drafts),
                                   _ptr(row_offsets), B, k_max, V, R, params, _ptr(uniforms), _ptr(out_tokens),
                                   _ptr(accept_len), _ptr(out_pq), _ptr(workspace),

@@ -27,7 +27,7 @@ class DeviceBatch:
     """Inputs, outputs and workspace of one batch, resident on a CUDA device."""
 
     def __init__(self, *, target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max,
-                 temperature, top_k, top_p, presence, frequency, greedy, uniforms, want_pq=True):
+                 temperature, top_k, top_p, presence, frequency, greedy, uniforms, want_pq=True, prior=None):
         self.target_logits = target_logits
         self.draft_probs = draft_probs
         self.draft_tokens = draft_tokens
@@ -37,6 +37,7 @@ class DeviceBatch:
         self.temperature, self.top_k, self.top_p = temperature, top_k, top_p
         self.presence, self.frequency, self.greedy = presence, frequency, greedy
         self.uniforms = uniforms
+        self.prior = prior          # None or (prior_offsets, prior_tokens, prior_counts)
         dev = target_logits.device
         R, V = target_logits.shape
         B = num_drafts.numel()
@@ -68,7 +69,10 @@ class DeviceBatch:
                    presence=_t(w.presence, device, torch.float32),
                    frequency=_t(w.frequency, device, torch.float32),
                    greedy=_t(w.greedy, device, torch.uint8),
-                   uniforms=_t(w.uniforms, device, torch.float32), want_pq=want_pq)
+                   uniforms=_t(w.uniforms, device, torch.float32), want_pq=want_pq,
+                   prior=None if getattr(w, "prior_offsets", None) is None else
+                   (_t(w.prior_offsets, device, torch.int32), _t(w.prior_tokens, device, torch.int32),
+                    _t(w.prior_counts, device, torch.int32)))
 
     def run(self, stream=None, target_logits=None, draft_probs=None, onehot=False) -> None:
         """Enqueue one verification (optionally on other copies of the two large inputs).
@@ -78,13 +82,14 @@ class DeviceBatch:
                                self.draft_tokens, self.num_drafts, self.row_offsets, self.k_max,
                                self.temperature, self.top_k, self.top_p, self.presence, self.frequency,
                                self.greedy, self.uniforms, self.out_tokens, self.accept_len, self.out_pq,
-                               self.workspace, stream)
+                               self.workspace, stream, self.prior)
             return
         spec_verify(self.target_logits if target_logits is None else target_logits,
                     self.draft_probs if draft_probs is None else draft_probs,
                     self.draft_tokens, self.num_drafts, self.row_offsets, self.k_max,
                     self.temperature, self.top_k, self.top_p, self.presence, self.frequency, self.greedy,
-                    self.uniforms, self.out_tokens, self.accept_len, self.out_pq, self.workspace, stream)
+                    self.uniforms, self.out_tokens, self.accept_len, self.out_pq, self.workspace, stream,
+                    self.prior)
 
     def results(self) -> dict:
         torch.cuda.synchronize(self.target_logits.device)
@@ -105,13 +110,15 @@ def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None, 
     if onehot:
         spec_verify_onehot(tl, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k,
                            db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens,
-                           db.accept_len, db.out_pq, db.workspace, stream)
+                           db.accept_len, db.out_pq, db.workspace, stream, db.prior)
     else:
         spec_verify(tl, dp, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k,
                     db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens, db.accept_len,
-                    db.out_pq, db.workspace, stream)
+                    db.out_pq, db.workspace, stream, db.prior)
     p = lambda t: None if t is None else t.data_ptr()
-    params = SvParams(p(db.temperature), p(db.top_k), p(db.top_p), p(db.presence), p(db.frequency), p(db.greedy))
+    ho, ht, hc = db.prior if db.prior is not None else (None, None, None)
+    params = SvParams(p(db.temperature), p(db.top_k), p(db.top_p), p(db.presence), p(db.frequency), p(db.greedy),
+                      p(ho), p(ht), p(hc), 0 if ht is None else ht.numel())
     head = (p(tl), SV_BF16 if tl.dtype == torch.bfloat16 else SV_F32) + (() if onehot else (p(dp),))
     args = head + (p(db.draft_tokens), p(db.num_drafts), p(db.row_offsets), db.B, db.k_max, db.V, db.R, params,
                    p(db.uniforms), p(db.out_tokens), p(db.accept_len), p(db.out_pq), p(db.workspace),

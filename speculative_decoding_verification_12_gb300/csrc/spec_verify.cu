@@ -164,7 +164,7 @@ __device__ __forceinline__ void sfail(const Args &A, SShared &P, int b) {
 template <typename E>
 __host__ __device__ constexpr int stream_ctas() { return sizeof(E) == 2 ? SCTA : (SCTA < 2 ? SCTA : 2); }
 
-template <typename E>
+template <typename E, bool HIST>
 __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args A) {
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ SShared P;
@@ -264,10 +264,12 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
             locate_row(A, R, r);
             if (R.active) build_penalties(A, R, R.i);
             __syncwarp();
-            if (R.active && R.npen > 0) {
-                // segments holding a penalised token take the streamers' slow path
+            if (R.active && (R.npen > 0 || R.hdir)) {
+                // segments holding a penalised token take the streamers' slow path: those of
+                // the request's history (indexed by the prepass), then the drafts'
                 uint32_t *dmask = masks + slot * mask_words(np);
-                for (int w = lane; w < np / 32; w += 32) dmask[w] = 0u;
+                const uint32_t *hm = R.hdir ? A.hmask + (size_t)R.b * mask_words(np) : nullptr;
+                for (int w = lane; w < np / 32; w += 32) dmask[w] = hm ? __ldg(hm + w) : 0u;
                 __syncwarp();
                 for (int h = lane; h < R.npen; h += 32) {
                     const int x = R.pid[h];
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
 #ifdef SV_TIMING
             tslot = A.timing + (size_t)R.tix * NTIME;
 #endif
-            if (!stream_row_any<E>(P.full, P.empty, ring, PNS, rp, R.c0, R.c1, nseg, V, sw, R, o,
+            if (!stream_row_any<E, HIST>(P.full, P.empty, ring, PNS, rp, R.c0, R.c1, nseg, V, sw, R, o,
                                    masks + slot * mask_words(np), A.rowarg + R.r, tslot)) {
                 if (lane == 0) sfail(A, P, R.b);
                 return;
@@ -365,6 +367,53 @@ __global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_ke
     SV_MARK(A, 4 * A.R + r, 5);
 }
 
+// History prepass (calls with a prior history), one CTA per request: checks the request's
+// history (offsets inside [0, prior_len], ids in [0, V) strictly ascending, counts >= 1) and
+// indexes it by segment -- hdir[s] = the first entry whose token lies in segment s or later,
+// so segment s holds entries hdir[s] .. hdir[s+1] -- plus a bitmask of the segments that hold
+// any.  A bad history sets the request's status and the sticky error word.
+__global__ void __launch_bounds__(256) history_kernel(const Args A, int prior_len) {
+    __shared__ int bad;
+    const int b = blockIdx.x;
+    const int np = nseg_pad(A.nseg);
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    const int lo = __ldg(A.hoff + b), hi = __ldg(A.hoff + b + 1);
+    if (lo < 0 || hi < lo || hi > prior_len || (b == 0 && lo != 0)) {
+        if (threadIdx.x == 0) bad = 1;
+    } else {
+        for (int j = lo + (int)threadIdx.x; j < hi; j += blockDim.x) {
+            const int x = __ldg(A.htok + j);
+            if (x < 0 || x >= A.V || __ldg(A.hcnt + j) < 1 || (j > lo && __ldg(A.htok + j - 1) >= x)) bad = 1;
+        }
+    }
+    __syncthreads();
+    if (bad) {
+        if (threadIdx.x == 0) {
+            A.hstat[b] = 8;
+            record_error(A, 8, b);
+        }
+        return;
+    }
+    int32_t *dir = A.hdir + (size_t)b * (np + 1);
+    // entry j is the first of segments seg(x_{j-1}) + 1 .. seg(x_j); the end (j == hi) closes
+    // the directory through segment np
+    for (int j = lo + (int)threadIdx.x; j <= hi; j += blockDim.x) {
+        const int s_lo = j == lo ? 0 : __ldg(A.htok + j - 1) / SEG + 1;
+        const int s_hi = j == hi ? np : __ldg(A.htok + j) / SEG;
+        for (int s = s_lo; s <= s_hi; s++) dir[s] = j;
+    }
+    __syncthreads();
+    uint32_t *mask = A.hmask + (size_t)b * (np / 32);
+    for (int w = threadIdx.x; w < np / 32; w += blockDim.x) {
+        uint32_t bits = 0u;
+        for (int t = 0; t < 32; t++)
+            if (dir[w * 32 + t + 1] > dir[w * 32 + t]) bits |= 1u << t;
+        mask[w] = bits;
+    }
+    if (threadIdx.x == 0) A.hstat[b] = 0;
+}
+
 __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *nd, int B, int32_t *hdr) {
     int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
@@ -412,7 +461,7 @@ static cudaEvent_t g_phase_start = nullptr, g_phase_end = nullptr;
 // resident for this vocabulary.
 template <typename E, bool QVEC>
 static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
-    static size_t enabled1 = 0, enabled2 = 0;
+    static size_t enabled1[2] = {0, 0}, enabled2 = 0;
     static int sms[64] = {0};
     int dev = 0;
     cudaError_t e;
@@ -433,9 +482,11 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
     while (B.pns > 3 && stream_smem(A.nseg, B.pns) > budget) B.pns--;
     const size_t smem1 = stream_smem(A.nseg, B.pns), smem2 = select_smem(A.nseg);
     if (smem1 > budget || smem2 > (size_t)232448 - sizeof(RowCtx)) return cudaErrorNotSupported;
-    auto k1 = stream_kernel<E>;
+    // the stream kernel with the history variants only when the call passes a history
+    const int hist = A.hoff ? 1 : 0;
+    auto k1 = hist ? stream_kernel<E, true> : stream_kernel<E, false>;
     auto k2 = select_kernel<E, QVEC>;
-    if ((e = ensure_smem(k1, smem1, enabled1)) != cudaSuccess) return e;
+    if ((e = ensure_smem(k1, smem1, enabled1[hist])) != cudaSuccess) return e;
     if ((e = ensure_smem(k2, smem2, enabled2)) != cudaSuccess) return e;
     const long long units = (long long)A.R - B.nsplit + (long long)B.nsplit * B.nparts;
     const int grid = (int)(ctas < units ? ctas : units);
@@ -493,6 +544,8 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     if (!target_logits || !num_drafts || !uniforms || !out_tokens || !accept_len || !workspace) return SV_ERR_INVALID_ARG;
     if (D > 0 && ((!onehot && !draft_probs) || !draft_tokens)) return SV_ERR_INVALID_ARG;
     if (!params.temperature || !params.top_k || !params.top_p || !params.greedy) return SV_ERR_INVALID_ARG;
+    if (params.prior_offsets && (!params.prior_tokens || !params.prior_counts || params.prior_len < 0))
+        return SV_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(B, total_rows, V);
     if (((uintptr_t)workspace & 255) != 0 || workspace_bytes < L.total) return SV_ERR_WORKSPACE;
 
@@ -509,6 +562,9 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     A.pres = params.presence_penalty;
     A.freq = params.frequency_penalty;
     A.greedy = params.greedy;
+    A.hoff = params.prior_offsets;
+    A.htok = params.prior_tokens;
+    A.hcnt = params.prior_counts;
     A.uni = uniforms;
     A.out_tok = out_tokens;
     A.acc = accept_len;
@@ -517,6 +573,9 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     A.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     A.rowarg = reinterpret_cast<unsigned long long *>(ws + L.rowarg);
     A.prep = reinterpret_cast<int4 *>(ws + L.prep);
+    A.hdir = reinterpret_cast<int32_t *>(ws + L.hdir);
+    A.hmask = reinterpret_cast<uint32_t *>(ws + L.hmask);
+    A.hstat = reinterpret_cast<int32_t *>(ws + L.hstat);
     A.gstats = reinterpret_cast<float *>(ws + L.gstats);
     A.stats = reinterpret_cast<RowStat *>(ws + L.stats);
     A.pq = reinterpret_cast<float *>(ws + L.pq);
@@ -538,6 +597,10 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     // clear the error word, the work claim counter, the per-request arrival counters, the
     // per-row part counters and the greedy rows' argmax keys
     if (cudaMemsetAsync(ws, 0, L.rowarg + (size_t)total_rows * 8, st) != cudaSuccess) return SV_ERR_CUDA;
+    if (A.hoff) {
+        history_kernel<<<B, 256, 0, st>>>(A, params.prior_len);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    }
     cudaError_t e = cudaErrorNotSupported;
     if (vec) {
         if (logits_dtype == SV_BF16) e = qvec ? launch_two_kernels<uint16_t, true>(A, st) : launch_two_kernels<uint16_t, false>(A, st);

@@ -100,7 +100,7 @@ struct __align__(16) RowStat {
 };
 
 struct WsLayout {
-    size_t counters, rowarg, stats, pq, prep, gstats, timing, total;
+    size_t counters, rowarg, stats, pq, prep, gstats, hdir, hmask, hstat, timing, total;
 };
 
 // Phase timestamps (globaltimer ns) per work unit, recorded only in builds with SV_TIMING.
@@ -114,9 +114,11 @@ __host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
 // Workspace: [header 256 B: error word, first bad request, work claim counter]
 // [per-request arrival counters][per-row argmax keys of greedy rows]
 // [RowStat per row][(p, q) per draft][prepared row context, 640 B per row]
-// [segment statistics: 3 words per padded segment
-// per row][timing, SV_TIMING builds only].  The header, the counters and the argmax keys are
-// cleared by every call.
+// [segment statistics: 3 words per padded segment per row]
+// [history index: np+1 words per request][history segment mask: np/32 words per request]
+// [history status: 1 word per request][timing, SV_TIMING builds only].  The header, the
+// counters and the argmax keys are cleared by every call; the history regions are written by
+// the history prepass of calls that pass a history.
 __host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     WsLayout L;
     const size_t np = (size_t)nseg_pad(nseg_of(V));
@@ -133,6 +135,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     o = up256(o + size_t(R) * 640);
     L.gstats = o;
     o = up256(o + size_t(R) * np * 12);
+    L.hdir = o;
+    o = up256(o + size_t(B) * (np + 1) * 4);
+    L.hmask = o;
+    o = up256(o + size_t(B) * (np / 32) * 4);
+    L.hstat = o;
+    o = up256(o + size_t(B) * 4);
     L.timing = o;
 #ifdef SV_TIMING
     o = up256(o + size_t(R) * PMAX * NTIME * 8);
@@ -153,6 +161,9 @@ struct Args {
     const float *pres;        // may be NULL
     const float *freq;        // may be NULL
     const uint8_t *greedy;
+    const int32_t *hoff;      // prior history [B+1] offsets, or NULL (then htok, hcnt unused)
+    const int32_t *htok;      // history token ids, ascending within each request
+    const int32_t *hcnt;      // history counts
     const float *uni;
     int32_t *out_tok;
     int32_t *acc;
@@ -162,6 +173,9 @@ struct Args {
     unsigned long long *rowarg;   // greedy rows' (max key, ~lowest position), from the stream kernel
     float *gstats;            // per-row segment statistics [R][3][npad] (stream -> select kernel)
     int4 *prep;               // per-row prepared context, 640 B each (stream -> select kernel)
+    int32_t *hdir;            // per request: [np+1] history index of each 256-token segment's first entry
+    uint32_t *hmask;          // per request: [np/32] bitmask of the segments holding history tokens
+    int32_t *hstat;           // per request: 0, or SV_DEV_BAD_HISTORY
     RowStat *stats;
     float *pq;
     unsigned long long *timing;   // SV_TIMING builds only

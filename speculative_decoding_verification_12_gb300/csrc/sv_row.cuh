@@ -32,7 +32,11 @@ struct __align__(16) RowCtx {
     float u1;       // slot-1 uniform of the row (sampled rows: extra-token, residual or
                     // one-hot-scheme draw)
     int tix;        // index of the row's (or unit's) timing record
-    int pad0[6];
+    // the request's prior history (penalised rows with a non-empty history, else all NULL):
+    // hdir[s] .. hdir[s+1] index the entries of 256-token segment s in htok / hcnt
+    const int32_t *hdir;
+    const int32_t *htok;
+    const int32_t *hcnt;
     int pid[MAXK];
     float ppen[MAXK];
     // ---- stream kernel: the work unit
@@ -102,6 +106,19 @@ __device__ __forceinline__ void load_request(const Args &A, RowCtx &S, int b) {
     int status = 0;
     if (k < 0 || k > A.k_max || k > S.nrows - 1) status = 1;           // SV_DEV_BAD_LAYOUT
     if (!isfinite(pres) || !isfinite(freq)) status = status ? status : 6;
+    // the prior history, checked and indexed by the prepass
+    S.hdir = nullptr;
+    S.htok = nullptr;
+    S.hcnt = nullptr;
+    if (A.hoff) {
+        if (__ldg(A.hstat + b) != 0) {
+            status = status ? status : 8;
+        } else if (__ldg(A.hoff + b + 1) > __ldg(A.hoff + b) && (pres != 0.f || freq != 0.f)) {
+            S.hdir = A.hdir + (size_t)b * (nseg_pad(A.nseg) + 1);
+            S.htok = A.htok;
+            S.hcnt = A.hcnt;
+        }
+    }
     S.k = k;
     S.greedy = greedy;
     S.pres = pres;
@@ -173,8 +190,25 @@ __device__ __forceinline__ void locate_row(const Args &A, RowCtx &S, int r) {
     __syncwarp();
 }
 
+// History entry of token x in the request's prior history, or -1 (one thread).
+__device__ __forceinline__ int hist_find(const RowCtx &S, int x) {
+    const int seg = x / SEG;
+    const int lo = __ldg(S.hdir + seg), hi = __ldg(S.hdir + seg + 1);
+    for (int j = lo; j < hi; j++)
+        if (__ldg(S.htok + j) == x) return j;
+    return -1;
+}
+
+// Penalty of history entry j: presence once plus frequency per occurrence.
+__device__ __forceinline__ float hist_pen(const RowCtx &S, int j) {
+    return __fadd_rn(S.pres, __fmul_rn(S.freq, (float)__ldg(S.hcnt + j)));
+}
+
 // Penalties of row i: the distinct drafts d_0..d_{i-1} with pen = presence + frequency * count
-// (FreeToken PR #836, "Design": earlier drafts count as already generated).  Run by one warp.
+// (FreeToken PR #836, "Design": earlier drafts count as already generated).  A draft that is
+// also in the request's prior history already carries that entry's penalty (presence and its
+// history count), so its list entry adds only frequency * its count among the drafts.  Run by
+// one warp.
 __device__ __forceinline__ void build_penalties(const Args &A, RowCtx &S, int i) {
     const int lane = lane_id();
     if (lane == 0) S.npen = 0;
@@ -198,8 +232,10 @@ __device__ __forceinline__ void build_penalties(const Args &A, RowCtx &S, int i)
                     if (t < j) first = false;
                 }
             }
-            pen = __fadd_rn(S.pres, __fmul_rn(S.freq, (float)c));
-            keep = first && v >= 0 && v < A.V && pen != 0.f;
+            const bool ok = v >= 0 && v < A.V;
+            const bool inhist = ok && first && S.hdir && hist_find(S, v) >= 0;
+            pen = inhist ? __fmul_rn(S.freq, (float)c) : __fadd_rn(S.pres, __fmul_rn(S.freq, (float)c));
+            keep = first && ok && pen != 0.f;
         }
         unsigned msk = __ballot_sync(0xffffffffu, keep);
         int pos = S.npen + __popc(msk & ((1u << lane) - 1));
@@ -215,10 +251,47 @@ __device__ __forceinline__ void build_penalties(const Args &A, RowCtx &S, int i)
 
 // Applies the penalties to the 8 values this lane holds for the segment starting at seg_lo
 // (lane owns elements seg_lo + 8*lane .. +7).  Whole warp must call it.
+// The history entries of the segment starting at seg_lo, applied to this lane's 8 values.
+// Whole warp.
+__device__ __forceinline__ void patch_hist(const RowCtx &S, int seg_lo, float v[8]) {
+    const int lane = lane_id();
+    {
+        const int seg = seg_lo / SEG;
+        const int lo = __ldg(S.hdir + seg), hi = __ldg(S.hdir + seg + 1);
+        const int my = seg_lo + lane * 8;
+        for (int j0 = lo; j0 < hi; j0 += 32) {
+            const int j = j0 + lane;
+            int x = -1;
+            float pen = 0.f;
+            if (j < hi) {
+                x = __ldg(S.htok + j);
+                pen = hist_pen(S, j);
+            }
+            unsigned m = __ballot_sync(0xffffffffu, j < hi);
+            while (m) {
+                const int h = __ffs(m) - 1;
+                m &= m - 1;
+                const int d = __shfl_sync(0xffffffffu, x, h) - my;
+                const float ph = __shfl_sync(0xffffffffu, pen, h);
+#pragma unroll
+                for (int t = 0; t < 8; t++)
+                    if (d == t) v[t] = __fsub_rn(v[t], ph);
+            }
+        }
+    }
+}
+
+// History entries (the request's prior history) are applied first, then the drafts' list;
+// every site that penalises values uses this order, so all of them compute the same floats.
+// HIST = false leaves the history out (callers that know the row has none).
+template <bool HIST = true>
 __device__ __forceinline__ void patch_seg(const RowCtx &S, int seg_lo, float v[8]) {
     const int npen = S.npen;
-    if (npen == 0) return;
     const int lane = lane_id();
+    if constexpr (HIST) {
+        if (S.hdir) patch_hist(S, seg_lo, v);
+    }
+    if (npen == 0) return;
     bool h0 = lane < npen && (unsigned)(S.pid[lane] - seg_lo) < (unsigned)SEG;
     bool h1 = lane + 32 < npen && (unsigned)(S.pid[lane + 32] - seg_lo) < (unsigned)SEG;
     unsigned m0 = __ballot_sync(0xffffffffu, h0);
@@ -241,19 +314,44 @@ __device__ __forceinline__ void patch_seg(const RowCtx &S, int seg_lo, float v[8
     }
 }
 
-// Penalised value of token x from its raw stored element.
+// The 8 values one thread holds at tokens base .. base+7 (base a multiple of 8, inside one
+// segment), penalised in patch_seg's order.  One thread.
+__device__ __forceinline__ void pen_lane8(const RowCtx &S, int base, float v[8]) {
+    if (S.hdir) {
+        const int seg = base / SEG;
+        const int lo = __ldg(S.hdir + seg), hi = __ldg(S.hdir + seg + 1);
+        for (int j = lo; j < hi; j++) {
+            const int d = __ldg(S.htok + j) - base;
+            if ((unsigned)d < 8u) {
+                const float pen = hist_pen(S, j);
+#pragma unroll
+                for (int t = 0; t < 8; t++)
+                    if (d == t) v[t] = __fsub_rn(v[t], pen);
+            }
+        }
+    }
+    for (int h = 0; h < S.npen; h++) {
+        const int d = S.pid[h] - base;
+#pragma unroll
+        for (int t = 0; t < 8; t++)
+            if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
+    }
+}
+
+// Penalised value of token x (in [0, V)) from its stored value, in patch_seg's order.
+__device__ __forceinline__ float elem_z(const RowCtx &S, float z, int x) {
+    if (S.hdir) {
+        const int j = hist_find(S, x);
+        if (j >= 0) z = __fsub_rn(z, hist_pen(S, j));
+    }
+    for (int h = 0; h < S.npen; h++)
+        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
+    return z;
+}
 __device__ __forceinline__ float elem_z_raw(const RowCtx &S, uint16_t raw, int x) {
-    float z = __uint_as_float((uint32_t)raw << 16);
-    for (int h = 0; h < S.npen; h++)
-        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
-    return z;
+    return elem_z(S, __uint_as_float((uint32_t)raw << 16), x);
 }
-__device__ __forceinline__ float elem_z_raw(const RowCtx &S, float raw, int x) {
-    float z = raw;
-    for (int h = 0; h < S.npen; h++)
-        if (S.pid[h] == x) z = __fsub_rn(z, S.ppen[h]);
-    return z;
-}
+__device__ __forceinline__ float elem_z_raw(const RowCtx &S, float raw, int x) { return elem_z(S, raw, x); }
 
 // One thread: the row's draft token and, for a valid one, its penalised target value and q.
 template <typename E>
@@ -336,7 +434,7 @@ __device__ __forceinline__ void seg_stats(const Raw8<E> &raw, int seg, int V, co
     float m1, m2 = -INFINITY, sum = 0.f;
     bool done = false;
     if constexpr (sizeof(E) == 2) {
-        if (mode != MODE_SUM && S.npen == 0 && seg * SEG + SEG <= V) {
+        if (mode != MODE_SUM && S.npen == 0 && !S.hdir && seg * SEG + SEG <= V) {
             const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw.a);
             const __nv_bfloat162 a = __hmax2(p[0], p[1]), c = __hmax2(p[2], p[3]);
             const __nv_bfloat162 M = __hmax2(a, c);
@@ -403,12 +501,7 @@ __device__ __forceinline__ int find_in_lane(const RowCtx &S, const E *row, int V
     Raw8<E> raw = load_raw8<VEC>(row, base, V);
     float v[8];
     unpack8(raw, v);
-    for (int h = 0; h < S.npen; h++) {
-        const int d = S.pid[h] - base;
-#pragma unroll
-        for (int t = 0; t < 8; t++)
-            if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
-    }
+    pen_lane8(S, base, v);
     int pos = -1;
 #pragma unroll
     for (int t = 7; t >= 0; t--)

@@ -259,14 +259,7 @@ __device__ __forceinline__ int lane_candidates(RowCtx &S, unsigned long long *ca
     const int lane = lane_id();
     float v[8];
     unpack8(raw, v);
-    if (base >= 0) {
-        for (int h = 0; h < S.npen; h++) {
-            const int d = S.pid[h] - base;
-#pragma unroll
-            for (int t = 0; t < 8; t++)
-                if (d == t) v[t] = __fsub_rn(v[t], S.ppen[h]);
-        }
-    }
+    if (base >= 0) pen_lane8(S, base, v);
     int c = 0;
 #pragma unroll
     for (int t = 0; t < 8; t++) c += (base >= 0 && base + t < V && fkey(v[t]) >= tkey) ? 1 : 0;
@@ -296,7 +289,7 @@ template <typename E, bool VEC, class G>
 __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const Scratch &X, const E *row,
                                      const SegStats &o, RowStat &st, bool want_bonus) {
     const int warp = g.warp(), lane = g.lane();
-    const int V = A.V, nseg = A.nseg, K = S.K, row_idx = S.r, tix = S.tix;
+    const int V = A.V, nseg = A.nseg, K = S.K, tix = S.tix;
     (void)tix;
     const float m = S.m, s = S.s;
     const float *segA = o.mx;

@@ -95,7 +95,18 @@ __device__ __forceinline__ void arg_clean(const Raw8<E> &raw, int seg, ArgRun<E>
     if constexpr (sizeof(E) == 4) a.raw.b = up ? raw.b : a.raw.b;
 }
 
-template <typename E>
+// The history part of patch_seg out of line, for the inlined greedy path (keeps its registers
+// out of the streaming loop; v goes through memory only for rows that have a history).
+__device__ __noinline__ void patch_hist_ext(const RowCtx &R, int seg_lo, float *v) {
+    float w[8];
+#pragma unroll
+    for (int t = 0; t < 8; t++) w[t] = v[t];
+    patch_hist(R, seg_lo, w);
+#pragma unroll
+    for (int t = 0; t < 8; t++) v[t] = w[t];
+}
+
+template <typename E, bool HIST>
 __device__ __forceinline__ void arg_dirty(const Raw8<E> &raw, int seg, int V, const RowCtx &R, ArgRun<E> &a) {
     float v[8];
     unpack8(raw, v);
@@ -103,7 +114,8 @@ __device__ __forceinline__ void arg_dirty(const Raw8<E> &raw, int seg, int V, co
 #pragma unroll
     for (int t = 0; t < 8; t++)
         if (base + t >= V) v[t] = -INFINITY;
-    patch_seg(R, seg * SEG, v);
+    if constexpr (HIST) patch_hist_ext(R, seg * SEG, v);   // history first, as patch_seg orders them
+    patch_seg<false>(R, seg * SEG, v);
     const float m1 = max8(v);
     if (m1 > a.best) {
         int t = 7;
@@ -142,7 +154,7 @@ __device__ __forceinline__ void seg_clean(const Raw8<E> &raw, int seg, float s, 
 }
 
 // Segment that is ragged (ends past V) or holds a penalised token.
-template <typename E, int MODE>
+template <typename E, int MODE, bool HIST>
 __device__ __noinline__ void seg_dirty(const Raw8<E> raw, int seg, int V, const RowCtx &R, float s,
                                        const SegStats o) {
     float v[8];
@@ -151,7 +163,7 @@ __device__ __noinline__ void seg_dirty(const Raw8<E> raw, int seg, int V, const 
 #pragma unroll
     for (int t = 0; t < 8; t++)
         if (base + t >= V) v[t] = -INFINITY;
-    patch_seg(R, seg * SEG, v);
+    patch_seg<HIST>(R, seg * SEG, v);
     seg_from_values<MODE>(v, seg, s, o);
 }
 
@@ -168,8 +180,10 @@ struct RingPos {
 };
 
 // One streamer warp's share of a row: waits for each chunk, copies its segments to registers,
-// releases the stage, then reduces them.  Returns false when a wait timed out.
-template <typename E, int MODE, bool PEN>
+// releases the stage, then reduces them.  Returns false when a wait timed out.  PEN: 0 no
+// penalised token, 1 penalised drafts, 2 penalised drafts and a prior history (only the
+// last instantiates the history code, which keeps it out of the others' registers).
+template <typename E, int MODE, int PEN>
 __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned long long *empty,
                                            const unsigned char *ring, int pns, RingPos &rp, int c0, int c1, int nseg,
                                            int V, int sw, const RowCtx &R, const SegStats &o, const uint32_t *dmask,
@@ -211,13 +225,13 @@ __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned lo
             const int seg = c * SPC + jj;
             if ((!EVEN && jj >= SPC) || seg >= nseg) continue;
             bool clean = seg < nfull;
-            if constexpr (PEN) clean = clean && !((dmask[seg >> 5] >> (seg & 31)) & 1u);
+            if constexpr (PEN != 0) clean = clean && !((dmask[seg >> 5] >> (seg & 31)) & 1u);
             if constexpr (MODE == MODE_ARG) {
                 if (clean) arg_clean<E>(raw[u], seg, arg);
-                else arg_dirty<E>(raw[u], seg, V, R, arg);
+                else arg_dirty<E, PEN == 2>(raw[u], seg, V, R, arg);
             } else {
                 if (clean) seg_clean<E, MODE>(raw[u], seg, s, o);
-                else seg_dirty<E, MODE>(raw[u], seg, V, R, s, o);
+                else seg_dirty<E, MODE, PEN == 2>(raw[u], seg, V, R, s, o);
             }
         }
     }
@@ -225,28 +239,33 @@ __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned lo
     return true;
 }
 
-// Dispatch on the row's statistics mode and on whether it has penalised tokens.
-template <typename E>
+// Dispatch on the row's statistics mode and on whether it has penalised tokens.  Only the
+// HIST instance of the stream kernel (launched for calls with a prior history) holds the
+// history variants: their code slows every row of a kernel that contains it.
+template <typename E, bool HIST>
 __device__ __forceinline__ bool stream_row_any(unsigned long long *full, unsigned long long *empty,
                                                const unsigned char *ring, int pns, RingPos &rp, int c0, int c1,
                                                int nseg, int V, int sw, const RowCtx &R, const SegStats &o,
                                                const uint32_t *dmask, unsigned long long *argslot,
                                                unsigned long long *tslot) {
     const int mode = R.mode;
-    if (R.npen > 0) {
-        switch (mode) {
-            case MODE_ARG: return stream_row<E, MODE_ARG, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-            case MODE_TOP2: return stream_row<E, MODE_TOP2, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-            case MODE_SUM: return stream_row<E, MODE_SUM, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-            default: return stream_row<E, MODE_MAX, true>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-        }
+#define SV_STREAM_ROW(PEN_)                                                                                        \
+    switch (mode) {                                                                                                \
+        case MODE_ARG: return stream_row<E, MODE_ARG, PEN_>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, \
+                                                             dmask, argslot, tslot);                              \
+        case MODE_TOP2: return stream_row<E, MODE_TOP2, PEN_>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, \
+                                                              o, dmask, argslot, tslot);                          \
+        case MODE_SUM: return stream_row<E, MODE_SUM, PEN_>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, \
+                                                             dmask, argslot, tslot);                              \
+        default: return stream_row<E, MODE_MAX, PEN_>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o,      \
+                                                      dmask, argslot, tslot);                                     \
     }
-    switch (mode) {
-        case MODE_ARG: return stream_row<E, MODE_ARG, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-        case MODE_TOP2: return stream_row<E, MODE_TOP2, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-        case MODE_SUM: return stream_row<E, MODE_SUM, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
-        default: return stream_row<E, MODE_MAX, false>(full, empty, ring, pns, rp, c0, c1, nseg, V, sw, R, o, dmask, argslot, tslot);
+    if constexpr (HIST) {
+        if (R.hdir) SV_STREAM_ROW(2)
     }
+    if (R.npen > 0) SV_STREAM_ROW(1)
+    SV_STREAM_ROW(0)
+#undef SV_STREAM_ROW
 }
 
 }  // namespace sv

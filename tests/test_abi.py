@@ -47,9 +47,9 @@ def test_workspace_size(libsv):
     b = libsv.sv_workspace_bytes(512, 2560, 151936)
     assert 0 < a < b and a % 256 == 0
     # per row: statistics, a kept list and 12 bytes per (padded) 256-token segment; per
-    # request: a counter
+    # request: a counter and the history index (a word per segment, a mask bit per segment)
     nsegp = ((128256 + 255) // 256 + 31) // 32 * 32
-    assert a < 1280 * (4096 + 12 * nsegp) + 256 * 64 + 65536
+    assert a < 1280 * (4096 + 12 * nsegp) + 256 * (64 + 4 * (nsegp + 1) + nsegp // 8) + 65536
 
 
 def test_host_checks_reject_bad_calls(libsv):
@@ -74,6 +74,9 @@ def test_host_checks_reject_bad_calls(libsv):
     assert call(tl=None) == libsv.SV_ERR_INVALID_ARG
     assert call(dp=None) == libsv.SV_ERR_INVALID_ARG
     assert call(P=libsv.SvParams(None, 1, 1, None, None, 1)) == libsv.SV_ERR_INVALID_ARG
+    # a history needs all three arrays and a length >= 0
+    assert call(P=libsv.SvParams(1, 1, 1, None, None, 1, 16, None, 16, 4)) == libsv.SV_ERR_INVALID_ARG
+    assert call(P=libsv.SvParams(1, 1, 1, None, None, 1, 16, 16, 16, -1)) == libsv.SV_ERR_INVALID_ARG
     assert call(ws=C.c_void_p(257)) == libsv.SV_ERR_WORKSPACE
     assert call(wsb=100) == libsv.SV_ERR_WORKSPACE
     # the one-hot entry point: the same host checks, without draft_probs
