@@ -154,6 +154,22 @@ def cpu_baseline(workload: str, seconds_target: float = 12.0, max_requests: int 
                       f"{cores} threads, {dt:.1f} s"}
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time: the job's time is the max over its ranks (replicas each time
+    their own K steps; the whole job ends when the slowest does)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, ms_max: float) -> float:
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return units_per_rank * world * steps / (ms_max / 1e3)
+
+
 def workload_config(sp, w, world: int, onehot=False) -> dict:
     """The `config` object of a JSON line: the workload by name and its shape and filters."""
     def one(a):
@@ -264,14 +280,11 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
     rows = int((w.num_drafts.astype(np.int64) + 1).sum())
     drafts = int(w.num_drafts.sum())
     per_step_ms = ms_max / args.steps
-    value = rows * world * args.steps / (ms_max / 1e3)
+    value = whole_job_rate(rows, world, args.steps, ms_max)
 
     nb = algorithmic_bytes(w, acc, onehot)
     peak, peak_kind = peaks()
@@ -332,11 +345,7 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        te = torch.tensor([e_ms], device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e_value = rows * world * args.e2e_steps / (float(te.item()) / 1e3)
+        e2e_value = whole_job_rate(rows, world, args.e2e_steps, max_over_ranks(e0.elapsed_time(e1), dev))
         assert np.array_equal(pins_out[1].numpy(), acc), "end-to-end results differ from the device-resident run"
 
     if rank == 0:
@@ -347,7 +356,7 @@ def run_ours(args):
             "config": dict(workload_config(sp, w, world, onehot),
                            l2=f"{args.copies} rotating device copies of the inputs "
                               f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + (0 if onehot else db.draft_probs.numel() * 4)) / 1e9:.2f} GB > L2)"),
-            "draft_tokens_per_s": drafts * world * args.steps / (ms_max / 1e3),
+            "draft_tokens_per_s": whole_job_rate(drafts, world, args.steps, ms_max),
             "hbm_gbs": achieved,
             "accept": {"mean_accept_len": float(acc.mean()), "accept_rate": float(acc.sum() / max(drafts, 1)),
                        "tokens_per_step": float(acc.mean() + 1)},
