@@ -192,6 +192,9 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
         mbar_fence_init();
     }
     __syncthreads();
+    // the workspace words this kernel counts on were cleared by the kernel before it (this one
+    // may start early, as its programmatic dependent): wait for them
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         // ---- issuer (one thread): bulk copies of each prepared unit, chunk by chunk
@@ -441,6 +444,14 @@ static cudaError_t ensure_smem(K kern, size_t smem, size_t &enabled) {
     return cudaSuccess;
 }
 
+// Clears n16 16-byte words at p (the workspace header, counters and argmax keys).  Lets its
+// programmatic dependent (the stream kernel) start at once; that kernel waits before use.
+__global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 template <typename E, bool VEC, bool QVEC>
 static cudaError_t launch_rows(const Args &A, cudaStream_t stream) {
     static size_t enabled = 0;
@@ -491,8 +502,20 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
     const long long units = (long long)A.R - B.nsplit + (long long)B.nsplit * B.nparts;
     const int grid = (int)(ctas < units ? ctas : units);
     if (g_phase_start && (e = cudaEventRecord(g_phase_start, stream)) != cudaSuccess) return e;
-    k1<<<grid, ST, smem1, stream>>>(B);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+        // a programmatic dependent of the clearing kernel (or of the history prepass)
+        cudaLaunchConfig_t cfg1 = {};
+        cfg1.gridDim = dim3((unsigned)grid);
+        cfg1.blockDim = dim3(ST);
+        cfg1.dynamicSmemBytes = smem1;
+        cfg1.stream = stream;
+        cudaLaunchAttribute attr1[1];
+        attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr1[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg1.attrs = attr1;
+        cfg1.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg1, k1, B)) != cudaSuccess) return e;
+    }
     if (g_phase_end && (e = cudaEventRecord(g_phase_end, stream)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)A.R);
@@ -596,7 +619,13 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // clear the error word, the work claim counter, the per-request arrival counters, the
     // per-row part counters and the greedy rows' argmax keys
-    if (cudaMemsetAsync(ws, 0, L.rowarg + (size_t)total_rows * 8, st) != cudaSuccess) return SV_ERR_CUDA;
+    {
+        // (the clear ends below the statistics region, which starts at a 256-byte boundary)
+        const size_t n16 = (L.rowarg + (size_t)total_rows * 8 + 15) / 16;
+        const unsigned blocks = (unsigned)((n16 + 255) / 256 < 304 ? (n16 + 255) / 256 : 304);
+        clear_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4 *>(ws), n16);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    }
     if (A.hoff) {
         history_kernel<<<B, 256, 0, st>>>(A, params.prior_len);
         if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
