@@ -49,7 +49,7 @@ typedef enum {
     SV_OK = 0,
     SV_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size, bad dtype  */
     SV_ERR_WORKSPACE = 2,     /* workspace too small or not 256-byte aligned             */
-    SV_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch or memset)           */
+    SV_ERR_CUDA = 3,          /* a CUDA runtime call failed (a kernel launch)            */
     SV_ERR_UNSUPPORTED = 4,   /* shape outside what the kernels handle (V, k_max, B)     */
     SV_ERR_DEVICE_DATA = 5    /* returned only by sv_read_device_error: bad device data  */
 } sv_status;
