@@ -43,7 +43,7 @@ class _Batch(C.Structure):
 
 
 DIAG_FIELDS = ("decisions", "near_ties", "error", "near_accept", "near_cdf", "near_filter", "near_argmax",
-               "near_w")
+               "near_w", "near_rows_lo", "near_rows_hi", "near_final")
 
 
 class _Diag(C.Structure):
@@ -113,9 +113,11 @@ def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1, onehot
     """Run the oracle on a workload (all requests or a subset); returns a dict of arrays.
 
     out_tokens [B, k_max+1] int32 (-1 padded), accept_len [B] int32, pq [D, 2] float64
-    (p(x_i), q(x_i); NaN for greedy requests), pq_near [D] uint8 (the row's kept set sits
-    on a near-tie), decisions / near_ties / error [B] int32.  Requests not in `requests`
-    are left at -1 / NaN.
+    (p(x_i), q(x_i); NaN for greedy requests), pq_near [D] uint8 (p(x_i) sits on a near-tie
+    of the row's kept set), decisions / near_ties / error [B] int32 and the near-ties by
+    kind; near_rows [B] uint64 (bit i: row i's decision whether to keep draft i is a
+    near-tie) and near_final [B] int32 (the final token's draw or argmax is one).  Requests
+    not in `requests` are left at -1 / NaN.
 
     onehot=True runs the one-hot-draft scheme: every row is sampled with its draw uniform
     and the drafts are accepted while they match those samples; draft_probs is not read and
@@ -155,6 +157,9 @@ def verify(w, requests: Optional[Sequence[int]] = None, threads: int = 1, onehot
     res = dict(out_tokens=out, accept_len=acc, pq=pq[:D], pq_near=near[:D])
     for j, f in enumerate(DIAG_FIELDS):
         res[f] = dg[:, j].copy()
+    # bit i: the decision of row i whether to keep draft i is a near-tie
+    res["near_rows"] = (res.pop("near_rows_lo").view(np.uint32).astype(np.uint64)
+                        | (res.pop("near_rows_hi").view(np.uint32).astype(np.uint64) << np.uint64(32)))
     return res
 
 

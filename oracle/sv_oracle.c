@@ -90,7 +90,24 @@ typedef struct sv_oracle_diag {
     int32_t near_ties;  /* decisions within the near-tie band */
     int32_t error;      /* 0, or the device-data error code of the request */
     int32_t near_accept, near_cdf, near_filter, near_argmax, near_w;  /* near_ties by kind */
+    /* where on the request's path the near-ties are: bit i of the 64-bit mask (lo | hi << 32)
+     * is set when the decision of row i whether to keep draft i (accept test, greedy compare,
+     * or the one-hot scheme's sample compare) is a near-tie; near_final when the final token's
+     * decision (the residual, extra-token or argmax draw of the stopping row) is one */
+    uint32_t near_rows_lo, near_rows_hi;
+    int32_t near_final;
 } sv_oracle_diag;
+
+/* Records a near-tie at row i's keep decision (final = 0) or at the final token (final = 1). */
+static void mark_near(sv_oracle_diag *d, int32_t i, int final) {
+    if (final) {
+        d->near_final = 1;
+    } else if (i < 32) {
+        d->near_rows_lo |= 1u << i;
+    } else if (i < 64) {
+        d->near_rows_hi |= 1u << (i - 32);
+    }
+}
 
 enum { E_OK = 0, E_LAYOUT = 1, E_TOKEN = 2, E_TEMP = 3, E_TOPP = 4, E_UNIFORM = 5, E_PENALTY = 6, E_HISTORY = 8 };
 
@@ -327,9 +344,10 @@ static int in_amb(const row_amb *a, double zprime) { return a->lo <= a->hi && zp
 
 /* Inverse CDF over w[0..V) in token-index order [R1]: the smallest v whose running sum is
  * > u * W, where W is the running sum's total; the largest positive-weight v if rounding
- * leaves none.  *near is set when the running sum at the boundary is within 1e-5 (of W)
- * of u * W. */
-static int32_t inverse_cdf(const double *w, int32_t V, double u, int *near) {
+ * leaves none.  *near is set when the running sum at the boundary is within 1e-5 (of W) of
+ * u * W (1), or within 1e-5 + shift (2): `shift` is how far (in units of W) the running sums
+ * can move when the row's ambiguous kept-set levels flip (0 when there are none). */
+static int32_t inverse_cdf(const double *w, int32_t V, double u, double shift, int *near) {
     double W = 0.0;
     for (int32_t v = 0; v < V; v++) W += w[v];
     double target = u * W, c = 0.0;
@@ -338,7 +356,9 @@ static int32_t inverse_cdf(const double *w, int32_t V, double u, int *near) {
         double prev = c;
         c += w[v];
         if (c > target) {
-            if (fabs(prev / W - u) < NEAR_TOL || fabs(c / W - u) < NEAR_TOL) *near = 1;
+            const double dist = fmin(fabs(prev / W - u), fabs(c / W - u));
+            if (dist < NEAR_TOL) *near = 1;
+            else if (dist < NEAR_TOL + shift) *near = 2;
             return v;
         }
     }
@@ -357,7 +377,7 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
     const int32_t V = in->V;
     const int32_t kmax1 = in->k_max + 1;
     for (int32_t j = 0; j < kmax1; j++) out_tok[(int64_t)b * kmax1 + j] = -1;
-    sv_oracle_diag d = {0, 0, 0, 0, 0, 0, 0, 0};
+    sv_oracle_diag d = {0, 0, 0, 0, 0, 0, 0, 0, 0u, 0u, 0};
     int err = check_request(in, b);
     const int64_t r0 = row_start(in, b), d0 = r0 - b;
     const int32_t k = in->num_drafts[b];
@@ -390,7 +410,12 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                 d.decisions++;
                 d.near_ties += nt;
                 d.near_argmax += nt;
-                if (i == k || drafts[i] != g) { a = i; token = g; decided = 1; }
+                const int stop = (i == k || drafts[i] != g);
+                /* a near-tied argmax could move both the compare with the draft and, at the
+                 * stopping row, the final token */
+                if (nt && i < k) mark_near(&d, i, 0);
+                if (nt && stop) mark_near(&d, i, 1);
+                if (stop) { a = i; token = g; decided = 1; }
             }
         }
     } else {
@@ -404,24 +429,33 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                 double px = p[x];
                 double qx = (double)in->draft_probs[(d0 + i) * (int64_t)V + x];
                 /* the draft's own membership in the kept set is on a near-tie */
-                int nt = in_amb(&amb, z[x] / in->temperature[b]);
+                const int nt = in_amb(&amb, z[x] / in->temperature[b]);
                 if (out_pq) { out_pq[(d0 + i) * 2] = px; out_pq[(d0 + i) * 2 + 1] = qx; }
-                if (pq_near) pq_near[d0 + i] = (uint8_t)nt;
+                /* p(x) is not comparable when x's membership is ambiguous, or when flipping the
+                 * ambiguous levels would move the normaliser enough to shift p(x) by 1e-6 */
+                if (pq_near) pq_near[d0 + i] = (uint8_t)(nt || px * amb.mass >= 1e-6);
                 if (decided) continue;
                 d.decisions += dec + 1;
-                d.near_ties += nt;
-                d.near_filter += nt;
                 double u = in->uniforms[(r0 + i) * 2 + 0];
-                int accept;
+                int accept, kind = nt ? 2 : 0;   /* near-tie kind: 1 accept band, 2 kept set */
                 if (px > 0.0 && qx == 0.0) {
                     accept = 1;
                 } else if (px > 0.0) {
                     double ratio = px / qx;
                     double thr = ratio < 1.0 ? ratio : 1.0;
                     accept = u < thr;
-                    if (fabs(u - thr) < NEAR_TOL) { d.near_ties++; d.near_accept++; }
+                    if (!kind && fabs(u - thr) < NEAR_TOL) kind = 1;
+                    /* flipping an ambiguous level of the kept set moves Z, and with it
+                     * p(x)/q(x), by up to amb.mass relative */
+                    else if (!kind && fabs(u - thr) < NEAR_TOL + amb.mass * thr) kind = 2;
                 } else {
                     accept = 0;
+                }
+                if (kind == 1) d.near_accept++;
+                if (kind == 2) d.near_filter++;
+                if (kind) {
+                    d.near_ties++;
+                    mark_near(&d, i, 0);
                 }
                 if (!accept) {
                     /* [R1] residual max(0, p - q) at the rejected row, normalised by its sum */
@@ -434,16 +468,20 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                     }
                     double u1 = in->uniforms[(r0 + i) * 2 + 1];
                     int cn = 0;
+                    /* flipping the ambiguous levels moves p, hence r's running sums, by up to
+                     * amb.mass (in units of p's total), i.e. amb.mass / W of r's */
                     if (W > 0.0) {
-                        token = inverse_cdf(r, V, u1, &cn);
+                        token = inverse_cdf(r, V, u1, amb.mass / W, &cn);
                     } else {
-                        token = inverse_cdf(p, V, u1, &cn);   /* empty residual: draw from p */
+                        token = inverse_cdf(p, V, u1, amb.mass, &cn);   /* empty residual: draw from p */
                     }
-                    if (W < NEAR_W) { cn = 1; d.near_w++; } else { d.near_cdf += cn; }
-                    /* tokens of ambiguous membership could shift the running sums */
-                    if (!cn && amb.mass >= NEAR_TOL * (W > 0.0 ? W : 1.0)) { cn = 1; d.near_filter++; }
+                    if (W < NEAR_W) { cn = 1; d.near_w++; }
+                    else if (cn == 1) d.near_cdf++;
+                    else if (cn == 2) d.near_filter++;
+                    cn = cn != 0;
                     d.decisions++;
                     d.near_ties += cn;
+                    if (cn) mark_near(&d, i, 1);
                     a = i;
                     decided = 1;
                 }
@@ -451,10 +489,12 @@ static void verify_one(const sv_oracle_batch *in, int32_t b, int32_t *out_tok, i
                 /* [R2] every draft accepted: the extra token comes from row k */
                 int cn = 0;
                 d.decisions += dec + 1;
-                token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], &cn);
-                d.near_cdf += cn;
-                if (!cn && amb.mass >= NEAR_TOL) { cn = 1; d.near_filter++; }
+                token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], amb.mass, &cn);
+                if (cn == 1) d.near_cdf++;
+                if (cn == 2) d.near_filter++;
+                cn = cn != 0;
                 d.near_ties += cn;
+                if (cn) mark_near(&d, k, 1);
                 a = k;
                 decided = 1;
             }
@@ -478,7 +518,7 @@ static void verify_one_onehot(const sv_oracle_batch *in, int32_t b, int32_t *out
     const int32_t V = in->V;
     const int32_t kmax1 = in->k_max + 1;
     for (int32_t j = 0; j < kmax1; j++) out_tok[(int64_t)b * kmax1 + j] = -1;
-    sv_oracle_diag d = {0, 0, 0, 0, 0, 0, 0, 0};
+    sv_oracle_diag d = {0, 0, 0, 0, 0, 0, 0, 0, 0u, 0u, 0};
     int err = check_request_slots(in, b, 1);
     const int64_t r0 = row_start(in, b), d0 = r0 - b;
     const int32_t k = in->num_drafts[b];
@@ -516,17 +556,25 @@ static void verify_one_onehot(const sv_oracle_batch *in, int32_t b, int32_t *out
             if (i < k) {
                 int32_t x = drafts[i];
                 if (out_pq) { out_pq[(d0 + i) * 2] = p[x]; out_pq[(d0 + i) * 2 + 1] = 1.0; }
-                if (pq_near) pq_near[d0 + i] = (uint8_t)in_amb(&amb, z[x] / in->temperature[b]);
+                if (pq_near)
+                    pq_near[d0 + i] = (uint8_t)(in_amb(&amb, z[x] / in->temperature[b]) || p[x] * amb.mass >= 1e-6);
             }
             if (decided) continue;
-            t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 1], &cn);
-            d.near_cdf += cn;
             /* tokens whose membership of the kept set is on a near-tie could move the boundary */
-            if (!cn && amb.mass >= NEAR_TOL) { cn = 1; d.near_filter++; }
+            t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 1], amb.mass, &cn);
+            if (cn == 1) d.near_cdf++;
+            if (cn == 2) d.near_filter++;
+            cn = cn != 0;
             d.decisions += dec + 1;
             d.near_ties += cn;
+            nt = cn;
         }
-        if (i == k || drafts[i] != t) {
+        const int stop = (i == k || drafts[i] != t);
+        /* a near-tied sample (or argmax) could move the compare with the draft and, at the
+         * stopping row, the final token */
+        if (nt && i < k) mark_near(&d, i, 0);
+        if (nt && stop) mark_near(&d, i, 1);
+        if (stop) {
             a = i;
             token = t;
             decided = 1;

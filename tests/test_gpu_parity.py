@@ -1,7 +1,6 @@
 """CUDA path vs the float64 oracle, element by element, through the C ABI.
 
-Small batches are compared in full; the workloads at their measured sizes are compared on a
-sample of requests the oracle computes one by one, plus properties that hold at any size.
+Every request of every batch is compared, the workloads at their measured sizes included.
 """
 import numpy as np
 import pytest
@@ -190,41 +189,36 @@ def test_rollback_of_draft_cache_lengths(sv, oracle_lib):
 
 
 # ------------------------------------------------------------------------------------------
-# the measured workloads: full compare where the oracle is quick, sampled otherwise
+# the measured workloads at full size, every request against the oracle
 # ------------------------------------------------------------------------------------------
 
-def _sampled(oracle_lib, name, n_sample, seed=0):
+def _full_workload(oracle_lib, name):
     w = W.make(name)
     g, _ = run_gpu(w)
     check_invariants(w, g)
-    rng = np.random.default_rng(seed)
-    reqs = np.sort(rng.choice(w.B, size=min(n_sample, w.B), replace=False))
-    o = oracle_lib.verify(w, requests=reqs, threads=16)
-    s = compare(w, g, o, requests=reqs, check_share=True)
+    o = oracle_lib.verify(w, threads=16)
+    s = compare(w, g, o, check_share=True)
     print(name, s)
+    assert s["requests"] == w.B
     return s, g, w
 
 
 def test_peaks_b64_k5_v32000_full(sv, oracle_lib):
-    w = W.make("peaks")
-    s, g, o, _ = full_compare(oracle_lib, w, check_share=True)
+    s, g, w = _full_workload(oracle_lib, "peaks")
     acc = g["accept_len"].mean() / 5
     assert 0.2 < acc < 1.0
 
 
-def test_zipf_b256_k4_v128256_sampled(sv, oracle_lib):
-    s, g, w = _sampled(oracle_lib, "zipf", 48)
-    assert s["requests"] >= 40
+def test_zipf_b256_k4_v128256_full(sv, oracle_lib):
+    _full_workload(oracle_lib, "zipf")
 
 
-def test_ragged_b512_v151936_sampled(sv, oracle_lib):
-    s, g, w = _sampled(oracle_lib, "ragged", 64)
-    assert s["requests"] >= 50
+def test_ragged_b512_v151936_full(sv, oracle_lib):
+    _full_workload(oracle_lib, "ragged")
 
 
-def test_stream_b1024_k7_v128256_sampled(sv, oracle_lib):
-    s, g, w = _sampled(oracle_lib, "stream", 12)
-    assert s["requests"] >= 10
+def test_stream_b1024_k7_v128256_full(sv, oracle_lib):
+    _full_workload(oracle_lib, "stream")
 
 
 def test_max_vocabulary(sv, oracle_lib):

@@ -2,7 +2,7 @@
 
 Each case plants one mistake into a copy of oracle/sv_oracle.c (a dropped term, a wrong
 sign, index or comparison, a transposed operand), compiles the copy on the CPU, and checks
-that at least one pin from test_oracle_pins.py fails against it.  The real oracle is never
+that at least one pin from test_oracle_pins.py or test_oracle_near_ties.py fails against it.  The real oracle is never
 modified.
 """
 import os
@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_near_ties as nt
 import test_oracle_pins as pins
 
 SRC = open(os.path.join(os.path.dirname(oracle.__file__), "sv_oracle.c")).read()
@@ -57,20 +58,21 @@ MUTATIONS = [
      [lambda o: pins.test_greedy_ties_go_to_lowest_id(o)]),
     ("inverse CDF not strict", "if (c > target) {", "if (c >= target) {",
      [lambda o: pins.test_inverse_cdf_never_picks_zero_weight(o)]),
-    ("extra token from the wrong row", "token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], &cn);",
-     "token = inverse_cdf(r, V, in->uniforms[(r0 + k) * 2 + 1], &cn);",
+    ("extra token from the wrong row", "token = inverse_cdf(p, V, in->uniforms[(r0 + k) * 2 + 1], amb.mass, &cn);",
+     "token = inverse_cdf(r, V, in->uniforms[(r0 + k) * 2 + 1], amb.mass, &cn);",
      [lambda o: pins.test_expected_tokens_closed_form(o),
       lambda o: pins.test_lossless_monte_carlo(o, 4, 1, 1.0, 0, 1.0, None, None)]),
-    ("one-hot: accepts on a mismatch", "if (i == k || drafts[i] != t) {", "if (i == k || drafts[i] == t) {",
+    ("one-hot: accepts on a mismatch", "const int stop = (i == k || drafts[i] != t);",
+     "const int stop = (i == k || drafts[i] == t);",
      [lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None)]),
-    ("one-hot: samples with the accept slot", "t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 1], &cn);",
-     "t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 0], &cn);",
+    ("one-hot: samples with the accept slot", "t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 1], amb.mass, &cn);",
+     "t = inverse_cdf(p, V, in->uniforms[(r0 + i) * 2 + 0], amb.mass, &cn);",
      [lambda o: pins.test_onehot_reduces_to_pinned_paths(o)]),
     ("one-hot: emits the draft at the stopping row", "token = t;", "token = i < k ? drafts[i] : t;",
      [lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None),
       lambda o: pins.test_onehot_matches_when_every_sample_matches(o)]),
-    ("one-hot: scan ignores the last draft", "if (i == k || drafts[i] != t) {",
-     "if (i == k || (i + 1 < k && drafts[i] != t)) {",
+    ("one-hot: scan ignores the last draft", "const int stop = (i == k || drafts[i] != t);",
+     "const int stop = (i == k || (i + 1 < k && drafts[i] != t));",
      [lambda o: pins.test_onehot_matches_when_every_sample_matches(o),
       lambda o: pins.test_onehot_joint_law(o, 5, 2, 1.0, 0, 1.0, None, None)]),
     ("history: its counts dropped", "int32_t c = prior_count(in, b, v);\n        for", "int32_t c = 0;\n        for",
@@ -85,6 +87,24 @@ MUTATIONS = [
      [lambda o: pins.test_history_softmax_against_numpy(o), lambda o: pins.test_history_greedy_against_numpy(o)]),
     ("rollback keeps one row too many", "int64_t t = L - (k + 1) + 1 + a;", "int64_t t = L - (k + 1) + 2 + a;",
      [lambda o: pins.test_rollback_closed_form(o)]),
+    # the near-tie classifier: a band too wide hides GPU mistakes, one too narrow fails correct
+    # fp32 results; the flags must land where the GPU can part from the oracle
+    ("near-tie band 100x wide", "#define NEAR_TOL 1e-5", "#define NEAR_TOL 1e-3",
+     [lambda o: nt.test_accept_band(o, 1e-4, False), lambda o: nt.test_cdf_band(o, 1e-4, False, 2)]),
+    ("near-tie band 100x narrow", "#define NEAR_TOL 1e-5", "#define NEAR_TOL 1e-7",
+     [lambda o: nt.test_accept_band(o, 1e-6, True)]),
+    ("residual-mass band 1000x wide", "#define NEAR_W 1e-6", "#define NEAR_W 1e-3",
+     [lambda o: nt.test_small_residual_band(o, 1e-4, False)]),
+    ("residual-mass band 10x narrow", "#define NEAR_W 1e-6", "#define NEAR_W 1e-7",
+     [lambda o: nt.test_small_residual_band(o, 5e-7, True)]),
+    ("accept band ignores the kept set's ambiguity", "fabs(u - thr) < NEAR_TOL + amb.mass * thr",
+     "fabs(u - thr) < NEAR_TOL", [lambda o: nt.test_top_p_band_flags_accept_tests(o, 1e-6, True)]),
+    ("greedy gap not relative", "return fabs(a - b) <= NEAR_TOL * s;", "return fabs(a - b) <= NEAR_TOL;",
+     [lambda o: nt.test_greedy_gap_band(o, 1e-6, True)]),
+    ("extra-token near-tie not located", "if (cn) mark_near(&d, k, 1);", ";",
+     [lambda o: nt.test_cdf_band(o, 1e-6, True, 2)]),
+    ("greedy compare near-tie not located", "if (nt && i < k) mark_near(&d, i, 0);\n                if (nt && stop)",
+     "if (nt && stop)", [lambda o: nt.test_greedy_gap_flags_the_compare(o)]),
 ]
 
 
