@@ -65,7 +65,8 @@ enum {
     SV_DEV_BAD_TOP_P = 4,
     SV_DEV_BAD_UNIFORM = 5,
     SV_DEV_BAD_PENALTY = 6,
-    SV_DEV_TIMEOUT = 7,       /* a row's bulk copy did not complete within 2 s (bounded wait)  */
+    SV_DEV_TIMEOUT = 7,       /* a wait of the streaming kernel ran out (2 s): every request
+                                 of the call then has -1 outputs                            */
     SV_DEV_BAD_HISTORY = 8    /* prior history: offsets decrease or pass prior_len, an id outside
                                  [0, V), ids not strictly ascending, or a count below 1      */
 };
@@ -243,6 +244,15 @@ sv_status sv_read_device_error(const void *workspace, int32_t *code, int32_t *fi
  * little slower.  Pass NULL, NULL to stop.  Process-wide, not thread-safe; the events stay
  * owned by the caller.  Returns SV_ERR_INVALID_ARG if only one handle is NULL. */
 sv_status sv_set_phase_events(void *stream_kernel_start, void *stream_kernel_end);
+
+/* Testing aid for the failure path: while `on` is nonzero, the streaming kernel of every
+ * spec_verify / spec_verify_onehot call that takes the two-kernel path (16-byte aligned rows)
+ * withholds one work unit from its copy and reduction warps, as a stalled scheduler would.
+ * Their bounded waits run out after 2 s; the call then completes with -1 for every request's
+ * outputs and SV_DEV_TIMEOUT in the workspace's error word, and the device stays usable.  No
+ * page has a counterpart: it exists so that the timeout path can be tested without a GPU
+ * fault.  Process-wide, for every device; returns SV_OK.  Never set it in production. */
+sv_status sv_set_test_withhold(int32_t on);
 
 /* Human-readable name of a status code. */
 const char *sv_status_string(sv_status s);

@@ -61,6 +61,8 @@ def lib():
         l.spec_rollback.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]
         l.sv_read_device_error.restype = C.c_int
         l.sv_read_device_error.argtypes = [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+        l.sv_set_test_withhold.restype = C.c_int
+        l.sv_set_test_withhold.argtypes = [C.c_int32]
         l.sv_set_phase_events.restype = C.c_int
         l.sv_set_phase_events.argtypes = [C.c_void_p, C.c_void_p]
         l.sv_status_string.restype = C.c_char_p

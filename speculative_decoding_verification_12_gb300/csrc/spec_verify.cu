@@ -26,6 +26,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/spec_verify.h"
 #include "sv_select.cuh"
 #include "sv_stream.cuh"
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(RT, 4) verify_rows_kernel(const Args A) {
     const int r = blockIdx.x;
     const int np = nseg_pad(A.nseg);
     const SegStats o = carve_segstats(dsm, np);
-    const Scratch X = carve_scratch(dsm + segstats_bytes(np), np);
+    const Scratch X = carve_scratch(dsm + segstats_bytes(np), np, dsm, rows_smem(A.nseg));
     SV_MARK(A, r, 0);
     if (g.warp() == 0) locate_row(A, S, r);
     g.sync();
@@ -153,9 +155,25 @@ __device__ __forceinline__ void part_chunks(int nc, int P, int p, int &c0, int &
     c1 = (int)((long long)nc * (p + 1) / P);
 }
 
+// A stream CTA gave up on a bounded wait: record SV_DEV_TIMEOUT and raise the call's stream
+// failure flag (header word 3), from which every select CTA marks its row KIND_FAIL -- rows
+// this CTA had claimed were never reduced, so no request of the call can be trusted.
 __device__ __forceinline__ void sfail(const Args &A, SShared &P, int b) {
     P.fail = 1;
     record_error(A, 7, b < 0 ? 0 : b);
+    // every writer stores the same value; the select kernel reads it once the stream grid is done
+    *reinterpret_cast<volatile int32_t *>(A.hdr + 3) = 1;
+}
+
+// The issuer's last act on a failure: waits (bounded) until every bulk copy it issued has
+// landed, so that the CTA never exits while a copy still writes its shared memory.  The copy
+// numbered j went to stage j mod pns in phase (j / pns) mod 2; only the last pns can be
+// outstanding.
+__device__ __noinline__ void drain_copies(unsigned long long *full, int q, int pns) {
+    for (int t = 0; t < q && t < pns; t++) {
+        const int j = q - 1 - t;
+        mbar_wait(&full[j % pns], (uint32_t)(j / pns) & 1u);
+    }
 }
 
 // Work unit u: row u while u < R - nsplit, then part (t mod nparts) of row R - nsplit + t / nparts
@@ -206,6 +224,7 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
             const int slot = j % NRB;
             if (!mbar_wait(&P.rb_desc[slot], (uint32_t)(j / NRB) & 1u)) {
                 sfail(A, P, -1);
+                drain_copies(P.full, q, PNS);
                 return;
             }
             const RowCtx &R = P.rc[slot];
@@ -216,6 +235,7 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
                 // the stage's previous fill (one lap earlier) must have been released
                 if (q >= PNS && !mbar_wait(&P.empty[st], rp.ph ^ 1u)) {
                     sfail(A, P, R.b);
+                    drain_copies(P.full, q, PNS);
                     return;
                 }
                 const uint32_t off = (uint32_t)c * SB;
@@ -291,7 +311,9 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
                 if (R.active) part_chunks(nc, npu, part, c0, c1);
                 R.c0 = c0;
                 R.c1 = c1;
-                mbar_arrive(&P.rb_desc[slot]);
+                // (a test of the failure path withholds the first unit of CTA 0 from its copy
+                // and reduction warps: their bounded waits run out, as a stalled scheduler's would)
+                if (!(A.withhold && blockIdx.x == 0 && j == 0)) mbar_arrive(&P.rb_desc[slot]);
             }
             if (part == 0) {
                 // the row's prepared context for the select kernel, with its draft gathers
@@ -344,7 +366,7 @@ __global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_ke
     const int r = blockIdx.x;
     const int np = nseg_pad(A.nseg);
     float *sb = reinterpret_cast<float *>(dsm);
-    const Scratch X = carve_scratch(dsm + up128((size_t)3 * np * 4), np);
+    const Scratch X = carve_scratch(dsm + up128((size_t)3 * np * 4), np, dsm, select_smem(A.nseg));
     SV_MARK(A, 4 * A.R + r, 0);
     // the stream kernel's results (and every earlier write on the stream) are visible past here
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -364,7 +386,14 @@ __global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_ke
     SV_MARK(A, 4 * A.R + r, 2);
     if (S.b < 0) return;   // a row outside every request: nothing to count
     fail_empty_requests(g, A, S);
-    if (S.active) select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
+    if (S.active) {
+        if (__ldcg(A.hdr + 3) == 0) {
+            select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
+        } else if (g.t == 0) {
+            // a stream CTA gave up on a wait: this row's statistics cannot be trusted
+            fail_row(A, S);
+        }
+    }
     SV_MARK(A, 4 * A.R + r, 4);
     arrive_and_finalize<E, true, QVEC>(g, A, S, X);
     SV_MARK(A, 4 * A.R + r, 5);
@@ -434,14 +463,28 @@ __global__ void rollback_kernel(int32_t *kv, const int32_t *acc, const int32_t *
 // host side
 // ------------------------------------------------------------------------------------------
 
+// Devices a process may drive (a device index at or beyond it is SV_ERR_UNSUPPORTED).
+constexpr int MAX_DEVICES = 64;
+
+// Opts the kernel into `smem` bytes of dynamic shared memory where it needs more than the
+// default 48 KB.  The opt-in belongs to the kernel in the current context, so it is looked up
+// there on every call (no per-process cache): a call on another device, or on a context
+// created again after a reset, opts in afresh.
 template <typename K>
-static cudaError_t ensure_smem(K kern, size_t smem, size_t &enabled) {
-    if (smem > 48 * 1024 && smem > enabled) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        enabled = smem;
-    }
-    return cudaSuccess;
+static cudaError_t ensure_smem(K kern, size_t smem) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+// The current device, checked against MAX_DEVICES.
+static cudaError_t current_device(int &dev) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return (dev < 0 || dev >= MAX_DEVICES) ? cudaErrorNotSupported : cudaSuccess;
 }
 
 // Clears n16 16-byte words at p (the workspace header, counters and argmax keys).  Lets its
@@ -454,34 +497,37 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16) {
 
 template <typename E, bool VEC, bool QVEC>
 static cudaError_t launch_rows(const Args &A, cudaStream_t stream) {
-    static size_t enabled = 0;
     const size_t smem = rows_smem(A.nseg);
     auto kern = verify_rows_kernel<E, VEC, QVEC>;
-    cudaError_t e = ensure_smem(kern, smem, enabled);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<A.R, RT, smem, stream>>>(A);
     return cudaGetLastError();
 }
 
-// Events recorded around the stream kernel when set (sv_set_phase_events).  Recording them
+// Events recorded around the stream kernel when set (sv_set_phase_events): process-wide, for
+// every device and stream (a measurement aid for one caller at a time).  Recording them
 // separates the two kernels, so the select kernel no longer overlaps the stream's end.
-static cudaEvent_t g_phase_start = nullptr, g_phase_end = nullptr;
+static std::atomic<cudaEvent_t> g_phase_start{nullptr}, g_phase_end{nullptr};
+
+// Testing aid (sv_set_test_withhold): process-wide; while set, every stream kernel withholds
+// one work unit so that its bounded waits run out.
+static std::atomic<bool> g_withhold{false};
 
 // Launches the stream kernel (SCTA CTAs per SM) and the select kernel as its programmatic
 // dependent; returns cudaErrorNotSupported (nothing launched) when the kernels cannot be
 // resident for this vocabulary.
 template <typename E, bool QVEC>
-static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
-    static size_t enabled1[2] = {0, 0}, enabled2 = 0;
-    static int sms[64] = {0};
-    int dev = 0;
+static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream, int dev) {
+    static std::atomic<int> sms[MAX_DEVICES];   // multiprocessors per device (0: not read yet)
     cudaError_t e;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
-    if (!sms[dev] && (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return e;
+    int nsm = sms[dev].load(std::memory_order_relaxed);
+    if (!nsm) {
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        sms[dev].store(nsm, std::memory_order_relaxed);
+    }
     Args B = A;
-    const long long ctas = (long long)sms[dev] * stream_ctas<E>();
+    const long long ctas = (long long)nsm * stream_ctas<E>();
     // the last wave of rows (one per CTA) is split into parts of at least 2 chunks
     const long long nc = ((long long)A.V * sizeof(E) + SB - 1) / SB;
     B.nparts = (int)(nc / 2 < SPLIT_PARTS ? nc / 2 : SPLIT_PARTS);
@@ -497,11 +543,12 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
     const int hist = A.hoff ? 1 : 0;
     auto k1 = hist ? stream_kernel<E, true> : stream_kernel<E, false>;
     auto k2 = select_kernel<E, QVEC>;
-    if ((e = ensure_smem(k1, smem1, enabled1[hist])) != cudaSuccess) return e;
-    if ((e = ensure_smem(k2, smem2, enabled2)) != cudaSuccess) return e;
+    if ((e = ensure_smem(k1, smem1)) != cudaSuccess) return e;
+    if ((e = ensure_smem(k2, smem2)) != cudaSuccess) return e;
     const long long units = (long long)A.R - B.nsplit + (long long)B.nsplit * B.nparts;
     const int grid = (int)(ctas < units ? ctas : units);
-    if (g_phase_start && (e = cudaEventRecord(g_phase_start, stream)) != cudaSuccess) return e;
+    const cudaEvent_t ph0 = g_phase_start.load(), ph1 = g_phase_end.load();
+    if (ph0 && (e = cudaEventRecord(ph0, stream)) != cudaSuccess) return e;
     {
         // a programmatic dependent of the clearing kernel (or of the history prepass)
         cudaLaunchConfig_t cfg1 = {};
@@ -516,7 +563,7 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream) {
         cfg1.numAttrs = 1;
         if ((e = cudaLaunchKernelEx(&cfg1, k1, B)) != cudaSuccess) return e;
     }
-    if (g_phase_end && (e = cudaEventRecord(g_phase_end, stream)) != cudaSuccess) return e;
+    if (ph1 && (e = cudaEventRecord(ph1, stream)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)A.R);
     cfg.blockDim = dim3(SELT);
@@ -612,11 +659,14 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     A.nparts = 1;
     A.nsplit = 0;
     A.onehot = onehot ? 1 : 0;
+    A.withhold = g_withhold.load() ? 1 : 0;
     const size_t esz = logits_dtype == SV_BF16 ? 2 : 4;
     const bool vec = ((uintptr_t)target_logits % 16 == 0) && ((size_t)V * esz) % 16 == 0;
     const bool qvec = (!draft_probs || (uintptr_t)draft_probs % 16 == 0) && ((size_t)V * 4) % 16 == 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (current_device(dev) != cudaSuccess) return SV_ERR_UNSUPPORTED;
     // clear the error word, the work claim counter, the per-request arrival counters, the
     // per-row part counters and the greedy rows' argmax keys
     {
@@ -632,8 +682,10 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     }
     cudaError_t e = cudaErrorNotSupported;
     if (vec) {
-        if (logits_dtype == SV_BF16) e = qvec ? launch_two_kernels<uint16_t, true>(A, st) : launch_two_kernels<uint16_t, false>(A, st);
-        else e = qvec ? launch_two_kernels<float, true>(A, st) : launch_two_kernels<float, false>(A, st);
+        if (logits_dtype == SV_BF16)
+            e = qvec ? launch_two_kernels<uint16_t, true>(A, st, dev) : launch_two_kernels<uint16_t, false>(A, st, dev);
+        else
+            e = qvec ? launch_two_kernels<float, true>(A, st, dev) : launch_two_kernels<float, false>(A, st, dev);
     }
     if (e == cudaErrorNotSupported) {
         cudaGetLastError();   // clear a sticky "not supported" from the probe, if any
@@ -701,30 +753,36 @@ extern "C" sv_status spec_verify_static(const void *target_logits, sv_dtype logi
                                         const int32_t *row_offsets, int32_t B, int32_t k_max, int32_t V,
                                         int32_t total_rows, sv_params params, const float *uniforms,
                                         int32_t *out_tokens, int32_t *accept_len, float *out_pq, void *stream) {
-    // the array's address on each device, looked up once with that device current
-    static void *base[64] = {nullptr};
+    // the array's address on each device, looked up once with that device current (host
+    // threads that race on the first lookup store the same address)
+    static std::atomic<void *> base[MAX_DEVICES];
     if (B < 1 || k_max < 0 || V < 1 || total_rows < B) return SV_ERR_INVALID_ARG;
     const size_t need = sv_workspace_bytes(B, total_rows, V);
     if (need == 0) return SV_ERR_INVALID_ARG;
     if (need > (size_t)SV_STATIC_WORKSPACE_BYTES) return SV_ERR_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
-    if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
-    if (!base[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, sv_static_workspace) != cudaSuccess || !p) return SV_ERR_CUDA;
-        base[dev] = p;
+    if (dev < 0 || dev >= MAX_DEVICES) return SV_ERR_UNSUPPORTED;
+    void *ws = base[dev].load(std::memory_order_acquire);
+    if (!ws) {
+        if (cudaGetSymbolAddress(&ws, sv_static_workspace) != cudaSuccess || !ws) return SV_ERR_CUDA;
+        base[dev].store(ws, std::memory_order_release);
     }
     // spec_verify clears what must start at zero (error word, claim and arrival counters,
     // greedy argmax keys) on `stream` before its kernels run
     return spec_verify(target_logits, logits_dtype, draft_probs, draft_tokens, num_drafts, row_offsets, B, k_max, V,
-                       total_rows, params, uniforms, out_tokens, accept_len, out_pq, base[dev],
+                       total_rows, params, uniforms, out_tokens, accept_len, out_pq, ws,
                        (size_t)SV_STATIC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" sv_status sv_set_test_withhold(int32_t on) {
+    g_withhold.store(on != 0);
+    return SV_OK;
 }
 
 extern "C" sv_status sv_set_phase_events(void *stream_kernel_start, void *stream_kernel_end) {
     if ((stream_kernel_start == nullptr) != (stream_kernel_end == nullptr)) return SV_ERR_INVALID_ARG;
-    g_phase_start = static_cast<cudaEvent_t>(stream_kernel_start);
-    g_phase_end = static_cast<cudaEvent_t>(stream_kernel_end);
+    g_phase_start.store(static_cast<cudaEvent_t>(stream_kernel_start));
+    g_phase_end.store(static_cast<cudaEvent_t>(stream_kernel_end));
     return SV_OK;
 }

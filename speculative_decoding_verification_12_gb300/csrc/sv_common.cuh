@@ -111,7 +111,7 @@ __host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(2
 __host__ __device__ inline int nseg_of(int V) { return (V + SEG - 1) / SEG; }
 __host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
 
-// Workspace: [header 256 B: error word, first bad request, work claim counter]
+// Workspace: [header 256 B: error word, first bad request, work claim counter, stream failure flag]
 // [per-request arrival counters][per-row argmax keys of greedy rows]
 // [RowStat per row][(p, q) per draft][prepared row context, 640 B per row]
 // [segment statistics: 3 words per padded segment per row]
@@ -168,7 +168,8 @@ struct Args {
     int32_t *out_tok;
     int32_t *acc;
     float *out_pq;            // may be NULL
-    int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] work claim counter
+    int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] work claim counter,
+                              // [3] stream failure flag (a stream CTA gave up on a bounded wait)
     int32_t *counters;
     unsigned long long *rowarg;   // greedy rows' (max key, ~lowest position), from the stream kernel
     float *gstats;            // per-row segment statistics [R][3][npad] (stream -> select kernel)
@@ -185,6 +186,7 @@ struct Args {
     int nsplit;               // stream kernel: the last nsplit rows are split
     int onehot;               // 1: one-hot drafts -- every row is sampled and the drafts are
                               // accepted while they equal the samples (q is not read)
+    int withhold;             // testing aid: the stream kernel's CTA 0 withholds its first unit
 };
 
 }  // namespace sv

@@ -57,6 +57,8 @@ struct __align__(16) RowCtx {
     double sel_target;
     int last, a, tok, need_resid, plast;
     int prepped;    // select path: the candidate segment lists are already built
+    double redd[16];          // per-warp partials of fp64 reductions
+    double dtarget, dbefore;  // draws over segments: u * W and the running total before the crossing
 };
 
 constexpr int PREP_BYTES = 32 * 4 + 2 * MAXK * 4;
@@ -830,31 +832,83 @@ struct WResid {      // max(0, p_v - q_v)
     }
 };
 
-// Draw from a whole row with per-segment weight sums segw[0..nseg) (overwritten by their
-// prefix sums).  The crossing segment is re-read by the group's first warp and scanned lane
-// by lane.  Returns the token, or -1 when no weight is positive.
-template <typename E, bool VEC, bool QVEC, typename WF, class G>
-__device__ int draw_by_segments(const G &g, RowCtx &S, const E *row, const float *qrow, int V, int nseg,
-                                float *segw, float u, const WF &wf) {
-    g_scan_incl(g, segw, nseg, S.redf);
-    const float W = segw[nseg - 1];
-    if (!(W > 0.f)) return -1;
-    const float target = __fmul_rn(u, W);
+// The segment of a draw over per-segment weights segw[0..nseg): the first segment whose running
+// total exceeds u * W (W = the total), with the running totals in fp64 and a fixed association
+// (thread chunks, then lanes, then warps), so that the boundary does not drift over a long row.
+// S.dtarget receives u * W, S.dbefore the running total before the segment.  With no segment
+// above the target (rounding), the last segment of positive weight, and *fallback is set.
+// Returns -1 when no weight is positive.
+template <class G>
+__device__ int crossing_segment(const G &g, RowCtx &S, const float *segw, int nseg, float u, bool &fallback) {
+    const int lane = g.lane(), warp = g.warp();
+    const int per = (nseg + G::kThreads - 1) / G::kThreads;
+    const int lo = min(nseg, g.t * per), hi = min(nseg, lo + per);
+    double t = 0.0;
+    for (int j = lo; j < hi; j++) t += (double)segw[j];
+    double incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) S.redd[warp] = incl;
+    g.sync();
+    double W = 0.0, run = 0.0;
+#pragma unroll
+    for (int w = 0; w < G::kWarps; w++) {
+        if (w < warp) run += S.redd[w];
+        W += S.redd[w];
+    }
+    run += incl - t;   // this thread's chunk starts here
+    const double target = (double)u * W;
     int best = 0x7fffffff;
-    for (int j = g.t; j < nseg; j += G::kThreads)
-        if (segw[j] > target) best = min(best, j);
-    best = g_min_i(g, best, S.redi);
-    bool fallback = false;
-    if (best == 0x7fffffff) {
-        int last = -1;
-        for (int j = g.t; j < nseg; j += G::kThreads) {
-            float prev = j ? segw[j - 1] : 0.f;
-            if (segw[j] > prev) last = max(last, j);
+    double before = 0.0;
+    if (W > 0.0) {
+        for (int j = lo; j < hi; j++) {
+            const double nx = run + (double)segw[j];
+            if (nx > target) {
+                best = j;
+                before = run;
+                break;
+            }
+            run = nx;
         }
+    }
+    g.sync();
+    best = g_min_i(g, best, S.redi);
+    fallback = false;
+    if (best != 0x7fffffff) {
+        if (best >= lo && best < hi) {
+            S.dtarget = target;
+            S.dbefore = before;
+        }
+    } else {
+        if (!(W > 0.0)) return -1;
+        int last = -1;
+        for (int j = g.t; j < nseg; j += G::kThreads)
+            if (segw[j] > 0.f) last = max(last, j);
         best = g_max_i(g, last, S.redi);
         fallback = true;
         if (best < 0) return -1;
+        if (g.t == 0) {
+            S.dtarget = target;
+            S.dbefore = 0.0;
+        }
     }
+    g.sync();
+    return best;
+}
+
+// Draw from a whole row with per-segment weight sums segw[0..nseg): the crossing segment from
+// fp64 running totals (crossing_segment), then that segment re-read by the group's first warp
+// and scanned lane by lane against what remains of u * W.  Returns the token, or -1 when no
+// weight is positive.
+template <typename E, bool VEC, bool QVEC, typename WF, class G>
+__device__ int draw_by_segments(const G &g, RowCtx &S, const E *row, const float *qrow, int V, int nseg,
+                                const float *segw, float u, const WF &wf) {
+    bool fallback = false;
+    const int best = crossing_segment(g, S, segw, nseg, u, fallback);
+    if (best < 0) return -1;
     if (g.warp() == 0) {
         const int lane = g.lane();
         const int seg = best;
@@ -882,13 +936,14 @@ __device__ int draw_by_segments(const G &g, RowCtx &S, const E *row, const float
         }
         float run = __shfl_up_sync(0xffffffffu, incl, 1);
         if (lane == 0) run = 0.f;
-        run += seg ? segw[seg - 1] : 0.f;
+        // what remains of the target inside this segment (small: the segment's own scale)
+        const float rem = (float)(S.dtarget - S.dbefore);
         int pick = 0x7fffffff, lastpos = -1;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             int idx = seg * SEG + lane * 8 + j;
             run += w[j];
-            if (!fallback && run > target && pick == 0x7fffffff) pick = idx;
+            if (!fallback && run > rem && pick == 0x7fffffff) pick = idx;
             if (w[j] > 0.f) lastpos = idx;
         }
         pick = warp_min_i(pick);

@@ -26,11 +26,17 @@ struct Scratch {
     uint32_t *hcnt;               // radix histogram (aliases aux)
     unsigned long long *hmass;    // fixed-point mass histogram (aliases aux)
     uint32_t *hlimb;              // its 32-bit limb counters, 4 x HB (aliases cand and hcnt)
+    unsigned char *big;           // the group's whole dynamic shared memory (row statistics, then
+    size_t big_bytes;             // the areas above), for passes that need it after the row max
 };
 
-// Carves a Scratch out of `p`: segX/segY (nsegp floats each) then 32 KB of candidate area.
-__device__ __forceinline__ Scratch carve_scratch(unsigned char *p, int nsegp) {
+// Carves a Scratch out of `p`: segX/segY (nsegp floats each) then the candidate area.  `base`
+// and `bytes` give the group's whole dynamic shared memory (it starts with the row's segment
+// statistics and ends with this scratch).
+__device__ __forceinline__ Scratch carve_scratch(unsigned char *p, int nsegp, unsigned char *base, size_t bytes) {
     Scratch c;
+    c.big = base;
+    c.big_bytes = bytes;
     c.segX = reinterpret_cast<float *>(p);
     c.segY = c.segX + nsegp;
     unsigned char *area = reinterpret_cast<unsigned char *>(c.segY + nsegp);
@@ -670,6 +676,24 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
         }
     }
     if (g.t == 0) A.stats[row_idx] = st;
+}
+
+// Marks a row whose statistics cannot be trusted (a stream CTA gave up on a bounded wait):
+// its request's finaliser then writes -1 outputs and records SV_DEV_TIMEOUT.  One thread.
+__device__ __forceinline__ void fail_row(const Args &A, const RowCtx &S) {
+    RowStat st;
+    st.m = 0.f; st.s = 0.f; st.tau = -INFINITY; st.Z = 1.f; st.invZ = 1.f; st.taukey = 0;
+    st.argmax = -1; st.bonus = -1; st.kind = KIND_FAIL; st.nlist = 0; st.resid = -1; st.pad1 = 0;
+    A.stats[S.r] = st;
+    if (S.i < S.k) {
+        const size_t d = (size_t)(S.d0 + S.i);
+        A.pq[d * 2] = NAN;
+        A.pq[d * 2 + 1] = NAN;
+        if (A.out_pq) {
+            A.out_pq[d * 2] = NAN;
+            A.out_pq[d * 2 + 1] = NAN;
+        }
+    }
 }
 
 // A RowStat written by another CTA, read through L2.
