@@ -95,6 +95,36 @@ __device__ __forceinline__ void append_candidates(RowCtx &S, unsigned long long 
     }
 }
 
+// Appends this lane's tokens of segment seg whose value is above -inf (the caller masks the
+// rest with -inf) to the candidate buffer; as append_candidates.
+__device__ __forceinline__ void append_candidates_if(RowCtx &S, unsigned long long *cand, int seg, const float v[8],
+                                                     int V) {
+    const int lane = lane_id();
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) c += (v[j] > -INFINITY) ? 1 : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if (lane == 0 && total) base = atomicAdd(&S.ncand, total);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    int pos = base + incl - c;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const int idx = seg * SEG + lane * 8 + j;
+        if (v[j] > -INFINITY) {
+            if (pos < CAP) cand[pos] = ((unsigned long long)fkey(v[j]) << 32) | (uint32_t)(~(uint32_t)idx);
+            pos++;
+        }
+    }
+    (void)V;
+}
+
 // One warp: top-k cut, top-p cut and kept mass over n <= WCAP candidates sorted by value
 // (descending), 8 per lane.  Writes S.n2 (kept count), S.zk (kept mass), S.cutkey.
 __device__ __forceinline__ void warp_cut(RowCtx &S, const unsigned long long *srt, int n, int K, float m, float s,
@@ -546,12 +576,197 @@ __device__ bool kept_from_candidates(const G &g, const Args &A, RowCtx &S, const
     return true;
 }
 
+// Mass bin of a token from a = (z - m) s, the log2 of its weight (<= 0): bins of 1/bpu of a
+// unit of log2 weight from the row max down, the last bin collecting everything lower.  The
+// bin is monotone in z: a token of a lower bin is strictly more likely than one of a higher.
+__device__ __forceinline__ int mass_bin(float a, float bpu, int nb) {
+    const float t = __fmul_rn(-a, bpu);
+    return t >= (float)(nb - 1) ? nb - 1 : (int)t;
+}
+
+// Fixed-point (2^-40) weight of a token from a = (z - m) s: the value weight() rounds to.
+__device__ __forceinline__ unsigned long long fixed_weight(float a) {
+    return __float2ull_rz(__fmul_rn(ex2(a), (float)FIXED_ONE));
+}
+
+// Exclusive prefix sums of v[0..n) (n <= G::kThreads * 4), 64-bit and exact, in place.
+template <class G>
+__device__ __forceinline__ void g_scan_u64_excl(const G &g, unsigned long long *v, int n, RowCtx &S) {
+    const int lane = g.lane(), warp = g.warp();
+    const int per = (n + G::kThreads - 1) / G::kThreads;
+    const int lo = min(n, g.t * per), hi = min(n, lo + per);
+    unsigned long long t = 0;
+    for (int j = lo; j < hi; j++) t += v[j];
+    unsigned long long incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    unsigned long long *red = reinterpret_cast<unsigned long long *>(S.redd);
+    if (lane == 31) red[warp] = incl;
+    g.sync();
+    unsigned long long run = incl - t;
+    for (int w = 0; w < warp; w++) run += red[w];
+    for (int j = lo; j < hi; j++) {
+        const unsigned long long x = v[j];
+        v[j] = run;
+        run += x;
+    }
+    g.sync();
+}
+
+// Top-p rows without top-k (FreeToken PR #836, "Design": keep the tokens while the mass
+// strictly above them is below top_p).  Two passes over the row instead of a radix select:
+//  1. mass bins relative to the row max (64 per unit of log2 weight over 16 units, or fewer
+//     when the group's scratch is small), with fixed-point weights summed exactly -- the bin
+//     where the running mass from the top reaches P * (total) holds the cut;
+//  2. that bin's tokens, sorted: the cut falls between two of its value levels, and the kept
+//     mass (the normaliser Z) is the exact fixed-point sum above the cut.
+// A draw from the row (want_bonus) adds the weight pass and the draw of kept_by_select.
+// Returns false, with nothing written to st, when the cut's bin holds more than CAP tokens or
+// the scratch holds fewer than 256 bins; the caller then takes the radix select (which
+// rewrites every scratch area it uses).
+template <typename E, bool VEC, class G>
+__device__ bool kept_by_mass_bins(const G &g, const Args &A, RowCtx &S, const Scratch &X, const E *row, RowStat &st,
+                                  bool want_bonus) {
+    const int V = A.V, nseg = A.nseg, lane = g.lane();
+    const float m = S.m, s = S.s;
+    const int lbits = V > 1 ? __clz(V - 1) : 31;        // V tokens of < 2^lbits fit one 32-bit limb
+    const int nl = (41 + lbits - 1) / lbits;            // limbs covering 2^40
+    int nb = 1024;
+    while (nb >= 256 && (size_t)nb * (nl + 1) * 4 > X.big_bytes) nb >>= 1;
+    if (nb < 256) return false;
+    const float bpu = (float)(nb / 16);
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(X.big);   // nb counts, then nl arrays of nb limbs
+    uint32_t *limb = cnt + nb;
+    const unsigned long long lmask = (1ull << lbits) - 1ull;
+    g.sync();   // the row statistics in X.big are no longer read
+    for (int d = g.t; d < nb * (nl + 1); d += G::kThreads) cnt[d] = 0u;
+    g.sync();
+    pass_segments<E, VEC, false, false, sizeof(E) == 2 ? 2 : 1>(
+        g, S, row, nullptr, V, nseg, [&](int seg, const float *v, const float *) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (seg * SEG + lane * 8 + j < V) {
+                    const float a = __fmul_rn(__fsub_rn(v[j], m), s);
+                    const int bin = mass_bin(a, bpu, nb);
+                    const unsigned long long f = fixed_weight(a);
+                    atomicAdd(&cnt[bin], 1u);
+#pragma unroll
+                    for (int l = 0; l < 4; l++) {
+                        const uint32_t part = (uint32_t)((f >> (lbits * l)) & lmask);
+                        if (l < nl && part) atomicAdd(&limb[l * nb + bin], part);
+                    }
+                }
+            }
+        });
+    g.sync();
+    // each thread totals a run of bins; the run holding the cut then finds its bin
+    const int per = nb / G::kThreads;
+    unsigned long long tot = 0;
+    for (int d = g.t * per; d < g.t * per + per; d++)
+        for (int l = 0; l < nl; l++) tot += (unsigned long long)limb[l * nb + d] << (lbits * l);
+    unsigned long long incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    unsigned long long *red = reinterpret_cast<unsigned long long *>(S.redd);
+    if (lane == 31) red[g.warp()] = incl;
+    g.sync();
+    unsigned long long T = 0, run = incl - tot;
+    for (int w = 0; w < G::kWarps; w++) {
+        if (w < g.warp()) run += red[w];
+        T += red[w];
+    }
+    const double PT = (double)S.P * (double)T;
+    if (g.t == 0) S.ncand = -1;
+    g.sync();
+    if ((double)run < PT && (double)(run + tot) >= PT) {
+        // this run holds the first bin whose running mass reaches P * T
+        for (int d = g.t * per; d < g.t * per + per; d++) {
+            unsigned long long md = 0;
+            for (int l = 0; l < nl; l++) md += (unsigned long long)limb[l * nb + d] << (lbits * l);
+            if ((double)(run + md) >= PT) {
+                S.sel_digit = d;
+                S.sel_mass = run;          // the mass of every bin above d
+                S.nsel = (int)cnt[d];      // tokens in bin d
+                S.ncand = 0;
+                break;
+            }
+            run += md;
+        }
+    }
+    g.sync();
+    if (S.ncand < 0 || S.nsel > CAP) return false;
+    const int bstar = S.sel_digit;
+    const unsigned long long above = S.sel_mass;
+    g.sync();   // the bins are dead: the candidates take their place
+    // 2. the tokens of the cut's bin
+    pass_segments<E, VEC, false, false, sizeof(E) == 2 ? 2 : 1>(
+        g, S, row, nullptr, V, nseg, [&](int seg, const float *v, const float *) {
+            float vv[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const bool in = seg * SEG + lane * 8 + j < V &&
+                                mass_bin(__fmul_rn(__fsub_rn(v[j], m), s), bpu, nb) == bstar;
+                vv[j] = in ? v[j] : -INFINITY;
+            }
+            append_candidates_if(S, X.cand, seg, vv, V);
+        });
+    g.sync();
+    const int n = S.ncand;
+    if (n > CAP || n < 1) return false;     // too many tokens share the cut's bin
+    const int np2 = pow2_at_least(n);
+    for (int j = n + g.t; j < np2; j += G::kThreads) X.cand[j] = 0ull;
+    g.sync();
+    g_sort_desc(g, X.cand, np2);
+    // fixed-point weights of the sorted candidates, then their exclusive running sums
+    unsigned long long *fw = reinterpret_cast<unsigned long long *>(X.cand + CAP);
+    for (int j = g.t; j < n; j += G::kThreads)
+        fw[j] = fixed_weight(__fmul_rn(__fsub_rn(key2f((uint32_t)(X.cand[j] >> 32)), m), s));
+    g.sync();
+    unsigned long long fn = 0;
+    if (g.t == 0) fn = fw[n - 1];
+    g_scan_u64_excl(g, fw, n, S);
+    // the first value level (after the first) whose mass strictly above reaches P * T is cut
+    int cut = 0x7fffffff;
+    for (int j = g.t; j < n; j += G::kThreads)
+        if (j > 0 && (uint32_t)(X.cand[j] >> 32) != (uint32_t)(X.cand[j - 1] >> 32) && (double)(above + fw[j]) >= PT)
+            cut = min(cut, j);
+    cut = g_min_i(g, cut, S.redi);
+    const int n2 = cut != 0x7fffffff ? cut : n;
+    if (g.t == 0) {
+        const unsigned long long zf = above + (n2 < n ? fw[n2] : fw[n - 1] + fn);
+        S.sel_mass = zf;
+        S.cutkey = (uint32_t)(X.cand[n2 - 1] >> 32);
+    }
+    g.sync();
+    const float Z = (float)((double)S.sel_mass / FIXED_ONE);
+    const uint32_t taukey = S.cutkey;
+    st.Z = Z;
+    st.invZ = __frcp_rn(Z);
+    st.taukey = taukey;
+    st.tau = key2f(taukey);
+    st.kind = KIND_THRESH;
+    st.nlist = 0;
+    if (want_bonus) {
+        WKept wk{m, s, taukey};
+        seg_sums<E, VEC, false>(g, S, row, nullptr, V, nseg, X.segY, wk, nullptr, wk);
+        st.bonus = draw_by_segments<E, VEC, false>(g, S, row, nullptr, V, nseg, X.segY, S.u1, wk);
+    }
+    return true;
+}
+
 // Kept set by radix select over the whole row (any top-k / top-p).
 template <typename E, bool VEC, class G>
 __device__ void kept_by_select(const G &g, const Args &A, RowCtx &S, const Scratch &X, const E *row, RowStat &st,
                                bool want_bonus) {
     const int V = A.V, nseg = A.nseg;
     const float m = S.m, s = S.s;
+    if (S.topp_on && !S.topk_on && kept_by_mass_bins<E, VEC>(g, A, S, X, row, st, want_bonus)) return;
     uint32_t key_lo = 0;
     if (S.topk_on) key_lo = select_kth_row<E, VEC>(g, S, row, V, nseg, S.K, X.hcnt);
     if (S.topp_on) key_lo = select_mass_row<E, VEC>(g, S, row, V, nseg, key_lo, m, s, S.P, X.hmass, X.hlimb);
