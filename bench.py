@@ -8,7 +8,8 @@ of the two large inputs (0.85 GB each set) rotate between steps so no step reads
 in L2 by the one before.
 
 --scheme onehot times the one-hot-draft entry point instead (drafts = the argmax of each draft
-row's q; every row is sampled and the matching prefix kept; q is not read).
+row's q; every row is sampled and the matching prefix kept; q is not read).  --scheme lazy times
+spec_verify_lazy, which reads no row after a request's first rejection.
 
 Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle instead.
 """
@@ -46,23 +47,29 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def algorithmic_bytes(w, accept_len, onehot=False) -> dict:
+def algorithmic_bytes(w, accept_len, onehot=False, lazy=False) -> dict:
     """Bytes the method must move for one call (see the design notes, 'Measurement').
 
     Every target row of every request (the one-pass design cannot skip rows before knowing
     where the rejection falls); one 32-byte sector of q per sampled draft (q(x_i)); at a
-    rejected sampled row, q over the residual's support: the kept set of a filtered row
-    (<= top-k tokens, one sector each) or the whole q row plus a re-read of the target row when
-    the row keeps every token; small per-row/per-request I/O.  The one-hot scheme reads no q:
-    the target rows and the I/O only.
+    rejected sampled row whose kept set is cut by top-k (0 < top_k < V), one 32-byte q sector
+    per kept token (at most top_k: the residual max(0, p - q) is zero outside the kept set);
+    at a rejected sampled row without top-k, the whole q row plus a re-read of the target row;
+    small per-row/per-request I/O (8 B per row, 4 B per draft, 4 (k_max + 2) + 24 B per
+    request).  The one-hot scheme reads no q: the target rows and the I/O only.  The lazy scheme
+    needs only each request's rows up to the one where it stops (a_b + 1 rows, with a_b its
+    accept length) and the q sectors of the drafts on that path; `rows_read` is what its two
+    phases read: every row 0, then rows 1..k of the requests that kept draft 0.
     """
     esz = 2 if w.dtype == "bf16" else 4
     V = w.V
     nd = w.num_drafts.astype(np.int64)
     rows = int((nd + 1).sum())
     sampled = w.greedy == 0
-    b_rows = rows * V * esz
-    b_q = 0 if onehot else int(nd[sampled].sum()) * 32
+    a = np.where(accept_len >= 0, np.minimum(accept_len, nd), nd).astype(np.int64)
+    b_rows = (int((a + 1).sum()) if lazy else rows) * V * esz
+    on_path = np.minimum(a + 1, nd) if lazy else nd
+    b_q = 0 if onehot else int(on_path[sampled].sum()) * 32
     b_rej = 0
     for b in ([] if onehot else np.nonzero(sampled & (accept_len < nd) & (accept_len >= 0))[0]):
         K = int(w.top_k[b])
@@ -73,7 +80,21 @@ def algorithmic_bytes(w, accept_len, onehot=False) -> dict:
     b_io = rows * 8 + int(nd.sum()) * 4 + w.B * (4 * (w.k_max + 2) + 24)
     total = b_rows + b_q + b_rej + b_io
     b_json = rows * V * esz + int(nd.sum()) * V * 4 + int(((accept_len < nd) & (accept_len >= 0)).sum()) * V * esz
-    return dict(total=total, rows=b_rows, q_sectors=b_q, rejected=b_rej, io=b_io, baseline_json_formula=b_json)
+    out = dict(total=total, rows=b_rows, q_sectors=b_q, rejected=b_rej, io=b_io, baseline_json_formula=b_json)
+    if lazy:
+        kept0 = (accept_len >= 1) & (nd >= 1)
+        out["rows_read"] = int(w.B + nd[kept0].sum()) * V * esz
+    return out
+
+
+def launches_per_call(w, scheme: str) -> int:
+    """Kernels one call launches: the workspace clear, the history prepass with a history, then
+    the stream and select kernels (the lazy scheme: both for row 0, both for the queued rows,
+    and the residual kernel; only the first pair when no request has drafts)."""
+    n = 1 + (1 if getattr(w, "prior_offsets", None) is not None else 0)
+    if scheme == "lazy":
+        return n + (2 if int(w.num_drafts.sum()) == 0 else 5)
+    return n + 2
 
 
 class ClockSampler:
@@ -170,12 +191,14 @@ def whole_job_rate(units_per_rank: int, world: int, steps: int, ms_max: float) -
     return units_per_rank * world * steps / (ms_max / 1e3)
 
 
-def workload_config(sp, w, world: int, onehot=False) -> dict:
+def workload_config(sp, w, world: int, onehot=False, lazy=False) -> dict:
     """The `config` object of a JSON line: the workload by name and its shape and filters."""
     def one(a):
         u = np.unique(np.asarray(a))
         return u.item() if u.size == 1 else "mixed"
     extra = {"scheme": "one-hot drafts (argmax of q): every row sampled, matching prefix kept"} if onehot else {}
+    if lazy:
+        extra = {"scheme": "lazy: row 0 of every request, then rows 1..k of those that kept draft 0"}
     return {**extra, "workload": sp.name, "B": int(w.B), "k": int(sp.k_max), "V": int(sp.V), "logits": sp.dtype,
             "top_k": one(w.top_k), "top_p": round(float(one(w.top_p)), 4) if one(w.top_p) != "mixed" else "mixed",
             "greedy_share": round(float(np.mean(w.greedy != 0)), 4), "ragged_k": w.row_offsets is not None,
@@ -244,6 +267,7 @@ def run_ours(args):
 
     sp = W.spec(args.workload)
     onehot = args.scheme == "onehot"
+    lazy = args.scheme == "lazy"
     w = W.make(args.workload, requests=None if args.requests is None else list(range(args.requests)))
     if onehot:
         W.with_argmax_drafts(w)
@@ -254,7 +278,7 @@ def run_ours(args):
         # the one-hot scheme reads no q: only the target logits rotate
         copies.append((db.target_logits.clone(), db.draft_probs if onehot else db.draft_probs.clone()))
     with torch.cuda.stream(stream):
-        calls = [bound_call(db, stream, t, d, onehot=onehot) for t, d in copies]
+        calls = [bound_call(db, stream, t, d, onehot=onehot, lazy=lazy) for t, d in copies]
     torch.cuda.synchronize(dev)
 
     def barrier():
@@ -286,7 +310,7 @@ def run_ours(args):
     per_step_ms = ms_max / args.steps
     value = whole_job_rate(rows, world, args.steps, ms_max)
 
-    nb = algorithmic_bytes(w, acc, onehot)
+    nb = algorithmic_bytes(w, acc, onehot, lazy)
     peak, peak_kind = peaks()
     achieved = nb["total"] / (ms / args.steps / 1e3) / 1e9
 
@@ -295,7 +319,7 @@ def run_ours(args):
     # is a pass of its own after the timed region.
     lib = sv.lib()
     phase = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(args.phase_steps)]
+             for _ in range(0 if lazy else args.phase_steps)]
     for a, b in phase:
         a.record(stream)
         b.record(stream)
@@ -348,12 +372,32 @@ def run_ours(args):
         e2e_value = whole_job_rate(rows, world, args.e2e_steps, max_over_ranks(e0.elapsed_time(e1), dev))
         assert np.array_equal(pins_out[1].numpy(), acc), "end-to-end results differ from the device-resident run"
 
+    entry = {"accept": "spec_verify", "onehot": "spec_verify_onehot", "lazy": "spec_verify_lazy"}[args.scheme]
+    call = {"achieved": achieved, "frac": achieved / peak, "bytes": nb["total"], "us": per_step_ms * 1e3,
+            "what": f"whole {entry} call: " + ("clear_kernel, stream_kernel + select_kernel over every row 0, "
+                                               "the same over the queued rows, resid_kernel (PDL chain)" if lazy else
+                                               "clear_kernel + stream_kernel + select_kernel (PDL chain)")}
+    if lazy:
+        # the lazy call's kernels overlap in one programmatic chain; its roofline is the call's
+        roofline = {"bound": "hbm", "kernel": "whole spec_verify_lazy call", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind, "algorithmic_bytes": nb["total"],
+                    "kernel_us": per_step_ms * 1e3, "timed": "CUDA events around whole calls on the launching stream",
+                    "traffic": args.traffic, "traffic_unit": "bytes per call (ncu dram read+write)", "call": call}
+    else:
+        roofline = {"bound": "hbm", "kernel": f"stream_kernel<{sp.dtype}>", "achieved": stream_gbs,
+                    "peak": peak, "unit": "GB/s", "frac": stream_gbs / peak, "peak_source": peak_kind,
+                    "algorithmic_bytes": nb["rows"], "kernel_us": stream_ms * 1e3,
+                    "timed": f"CUDA events recorded by the library around the stream kernel on its stream, "
+                             f"mean of {args.phase_steps} calls",
+                    "traffic": args.traffic if args.traffic is not None else
+                    (TRAFFIC_STREAM_KERNEL.get(sp.name) if args.requests is None and not onehot else None),
+                    "traffic_unit": "bytes per launch (ncu dram read+write)", "call": call}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(workload_config(sp, w, world, onehot),
+            "config": dict(workload_config(sp, w, world, onehot, lazy),
                            l2=f"{args.copies} rotating device copies of the inputs "
                               f"({args.copies * (db.target_logits.numel() * db.target_logits.element_size() + (0 if onehot else db.draft_probs.numel() * 4)) / 1e9:.2f} GB > L2)"),
             "draft_tokens_per_s": whole_job_rate(drafts, world, args.steps, ms_max),
@@ -361,23 +405,10 @@ def run_ours(args):
             "accept": {"mean_accept_len": float(acc.mean()), "accept_rate": float(acc.sum() / max(drafts, 1)),
                        "tokens_per_step": float(acc.mean() + 1)},
             "bytes_per_step": nb,
-            "roofline": {"bound": "hbm", "kernel": f"stream_kernel<{sp.dtype}>", "achieved": stream_gbs,
-                         "peak": peak, "unit": "GB/s", "frac": stream_gbs / peak, "peak_source": peak_kind,
-                         "algorithmic_bytes": nb["rows"], "kernel_us": stream_ms * 1e3,
-                         "timed": f"CUDA events recorded by the library around the stream kernel on its stream, "
-                                  f"mean of {args.phase_steps} calls",
-                         "traffic": args.traffic if args.traffic is not None else
-                         (TRAFFIC_STREAM_KERNEL.get(sp.name) if args.requests is None and not onehot else None),
-                         "traffic_unit": "bytes per launch (ncu dram read+write)",
-                         "call": {"achieved": achieved, "frac": achieved / peak, "bytes": nb["total"],
-                                  "us": per_step_ms * 1e3,
-                                  "what": f"whole {'spec_verify_onehot' if onehot else 'spec_verify'} call: "
-                                          f"clear_kernel + stream_kernel + select_kernel (PDL chain)"}},
+            "roofline": roofline,
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            # each spec_verify call launches three kernels: the clearing of the workspace
-            # header, the stream kernel and the select kernel (each a programmatic dependent of
-            # the one before)
-            "gpu_launches": 3 * args.steps,
+            # every kernel one call launches (launches_per_call), times the timed calls
+            "gpu_launches": launches_per_call(w, args.scheme) * args.steps,
             "clocks": clk,
         }
         if not args.no_cpu_baseline and world == 1:
@@ -403,8 +434,9 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per launch of the verify kernel, if captured")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--scheme", default="accept", choices=["accept", "onehot"],
-                    help="accept: spec_verify (accept test against q); onehot: spec_verify_onehot")
+    ap.add_argument("--scheme", default="accept", choices=["accept", "onehot", "lazy"],
+                    help="accept: spec_verify (accept test against q); onehot: spec_verify_onehot; "
+                         "lazy: spec_verify_lazy (no row after a request's first rejection is read)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

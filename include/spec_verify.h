@@ -150,6 +150,31 @@ sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const fl
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify_lazy -- spec_verify that reads no row after a request's first rejection.
+ *
+ * "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust", section
+ * "The Verification Algorithm": the verification loop returns at the first rejected draft, so
+ * the target rows after it are never needed.  spec_verify reads every row in one pass, because
+ * it cannot know the rejection point in advance; this entry point reads each request's row 0
+ * first, decides that row, and then reads rows 1..k only of the requests whose draft 0 was
+ * kept.  A rejection that needs the residual max(0, p - q) over a whole row (a row whose kept
+ * set is too large for a list) is drawn by a last launch that splits the row over several
+ * CTAs.  Fewer bytes are read when drafts are often rejected early; the second phase costs a
+ * second round of row selection, so with high acceptance spec_verify is the faster call.
+ *
+ *   Arguments, layout, results, errors and workspace are those of spec_verify, and the results
+ *   are the same, except out_pq: a request whose draft 0 is rejected has (p, q) for draft 0
+ *   and NaN for the drafts after it (their rows are never read); the others have every draft's.
+ *   The phase-event measurement aid does not apply.  Rows that are not 16-byte aligned, or a
+ *   vocabulary the two-kernel path cannot hold, take spec_verify's one-pass path.
+ */
+sv_status spec_verify_lazy(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
+                           const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,
+                           int32_t B, int32_t k_max, int32_t V, int32_t total_rows, sv_params params,
+                           const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *out_pq,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * spec_verify_onehot -- verify drafts proposed as one-hot (argmax) tokens.
  *
  * FreeToken PR #836, section "Design": when the draft model proposes its argmax, q_i is one-hot

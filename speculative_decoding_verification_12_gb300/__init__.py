@@ -49,6 +49,8 @@ def lib():
         l.spec_verify.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                   C.c_int32, C.c_int32, C.c_int32, C.c_int32, SvParams, C.c_void_p,
                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+        l.spec_verify_lazy.restype = C.c_int
+        l.spec_verify_lazy.argtypes = l.spec_verify.argtypes
         l.spec_verify_onehot.restype = C.c_int
         l.spec_verify_onehot.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
                                          C.c_int32, C.c_int32, C.c_int32, C.c_int32, SvParams, C.c_void_p,
@@ -165,6 +167,22 @@ def spec_verify(target_logits, draft_probs, draft_tokens, num_drafts, row_offset
                            workspace.numel() * workspace.element_size(), _stream(stream))
     if st != SV_OK:
         raise SvError(st, "spec_verify")
+
+
+def spec_verify_lazy(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max: int,
+                     temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy, uniforms,
+                     out_tokens, accept_len, out_pq, workspace, stream=None, prior=None) -> None:
+    """spec_verify that reads each request's rows 1..k only when its draft 0 was kept (the rows
+    after a first rejection are never read); same arguments and results as spec_verify."""
+    dt, B, V, R, params = _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max,
+                                        temperature, top_k, top_p, presence_penalty, frequency_penalty, greedy,
+                                        uniforms, out_tokens, accept_len, out_pq, workspace, prior)
+    st = lib().spec_verify_lazy(_ptr(target_logits), dt, _ptr(draft_probs), _ptr(draft_tokens), _ptr(num_drafts),
+                                _ptr(row_offsets), B, k_max, V, R, params, _ptr(uniforms), _ptr(out_tokens),
+                                _ptr(accept_len), _ptr(out_pq), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != SV_OK:
+        raise SvError(st, "spec_verify_lazy")
 
 
 def spec_verify_onehot(target_logits, draft_tokens, num_drafts, row_offsets, k_max: int, temperature, top_k,

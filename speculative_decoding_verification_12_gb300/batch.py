@@ -11,7 +11,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import sv_workspace_bytes, spec_verify, spec_verify_onehot
+from . import sv_workspace_bytes, spec_verify, spec_verify_lazy, spec_verify_onehot
 
 
 def _t(a: Optional[np.ndarray], device, dtype=None):
@@ -74,9 +74,10 @@ class DeviceBatch:
                    (_t(w.prior_offsets, device, torch.int32), _t(w.prior_tokens, device, torch.int32),
                     _t(w.prior_counts, device, torch.int32)))
 
-    def run(self, stream=None, target_logits=None, draft_probs=None, onehot=False) -> None:
+    def run(self, stream=None, target_logits=None, draft_probs=None, onehot=False, lazy=False) -> None:
         """Enqueue one verification (optionally on other copies of the two large inputs).
-        onehot=True runs the one-hot-draft scheme, which reads no draft_probs."""
+        onehot=True runs the one-hot-draft scheme, which reads no draft_probs; lazy=True runs
+        spec_verify_lazy (no row after a request's first rejection is read)."""
         if onehot:
             spec_verify_onehot(self.target_logits if target_logits is None else target_logits,
                                self.draft_tokens, self.num_drafts, self.row_offsets, self.k_max,
@@ -84,7 +85,8 @@ class DeviceBatch:
                                self.greedy, self.uniforms, self.out_tokens, self.accept_len, self.out_pq,
                                self.workspace, stream, self.prior)
             return
-        spec_verify(self.target_logits if target_logits is None else target_logits,
+        (spec_verify_lazy if lazy else spec_verify)(
+                    self.target_logits if target_logits is None else target_logits,
                     self.draft_probs if draft_probs is None else draft_probs,
                     self.draft_tokens, self.num_drafts, self.row_offsets, self.k_max,
                     self.temperature, self.top_k, self.top_p, self.presence, self.frequency, self.greedy,
@@ -99,10 +101,10 @@ class DeviceBatch:
         return out
 
 
-def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None, onehot=False):
-    """A zero-argument callable that enqueues spec_verify (spec_verify_onehot with onehot=True)
-    for `db` with every pointer already marshalled (for tight timing loops; argument checks
-    happen once, here)."""
+def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None, onehot=False, lazy=False):
+    """A zero-argument callable that enqueues spec_verify (spec_verify_onehot with onehot=True,
+    spec_verify_lazy with lazy=True) for `db` with every pointer already marshalled (for tight
+    timing loops; argument checks happen once, here)."""
     from . import SV_BF16, SV_F32, SV_OK, SvError, SvParams, lib
     tl = db.target_logits if target_logits is None else target_logits
     dp = db.draft_probs if draft_probs is None else draft_probs
@@ -123,7 +125,7 @@ def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None, 
     args = head + (p(db.draft_tokens), p(db.num_drafts), p(db.row_offsets), db.B, db.k_max, db.V, db.R, params,
                    p(db.uniforms), p(db.out_tokens), p(db.accept_len), p(db.out_pq), p(db.workspace),
                    db.workspace.numel(), getattr(stream, "cuda_stream", stream))
-    f = lib().spec_verify_onehot if onehot else lib().spec_verify
+    f = lib().spec_verify_onehot if onehot else (lib().spec_verify_lazy if lazy else lib().spec_verify)
 
     def call():
         st = f(*args)

@@ -100,7 +100,7 @@ struct __align__(16) RowStat {
 };
 
 struct WsLayout {
-    size_t counters, rowarg, stats, pq, prep, gstats, hdir, hmask, hstat, timing, total;
+    size_t counters, jobcnt, rowarg, stats, pq, prep, gstats, hdir, hmask, hstat, listb, jobs, jobsum, timing, total;
 };
 
 // Phase timestamps (globaltimer ns) per work unit, recorded only in builds with SV_TIMING.
@@ -111,19 +111,25 @@ __host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(2
 __host__ __device__ inline int nseg_of(int V) { return (V + SEG - 1) / SEG; }
 __host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
 
-// Workspace: [header 256 B: error word, first bad request, work claim counter, stream failure flag]
-// [per-request arrival counters][per-row argmax keys of greedy rows]
+// Workspace: [header 256 B: error word, first bad request, work claim counter, stream failure
+// flag, lazy scheme: queued row count, residual job count, second work claim counter]
+// [per-request arrival counters][per-job slice arrival counters][per-row argmax keys of greedy rows]
 // [RowStat per row][(p, q) per draft][prepared row context, 640 B per row]
 // [segment statistics: 3 words per padded segment per row]
 // [history index: np+1 words per request][history segment mask: np/32 words per request]
-// [history status: 1 word per request][timing, SV_TIMING builds only].  The header, the
-// counters and the argmax keys are cleared by every call; the history regions are written by
-// the history prepass of calls that pass a history.
+// [history status: 1 word per request]
+// [lazy scheme: queued rows, 1 word per row; residual jobs, 2 words per request; the jobs'
+// per-segment residual and target sums, 2 words per padded segment per request]
+// [timing, SV_TIMING builds only].  The header, the counters and the argmax keys are cleared
+// by every call; the history regions are written by the history prepass of calls that pass a
+// history, the lazy regions only by the lazy scheme.
 __host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     WsLayout L;
     const size_t np = (size_t)nseg_pad(nseg_of(V));
     size_t o = 256;
     L.counters = o;
+    o += size_t(B) * 4;
+    L.jobcnt = o;
     o = (o + size_t(B) * 4 + 7) & ~size_t(7);
     L.rowarg = o;
     o = up256(o + size_t(R) * 8);
@@ -141,6 +147,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     o = up256(o + size_t(B) * (np / 32) * 4);
     L.hstat = o;
     o = up256(o + size_t(B) * 4);
+    L.listb = o;
+    o = up256(o + size_t(R) * 4);
+    L.jobs = o;
+    o = up256(o + size_t(B) * 8);
+    L.jobsum = o;
+    o = up256(o + size_t(B) * np * 8);
     L.timing = o;
 #ifdef SV_TIMING
     o = up256(o + size_t(R) * PMAX * NTIME * 8);
@@ -169,7 +181,9 @@ struct Args {
     int32_t *acc;
     float *out_pq;            // may be NULL
     int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] work claim counter,
-                              // [3] stream failure flag (a stream CTA gave up on a bounded wait)
+                              // [3] stream failure flag (a stream CTA gave up on a bounded wait),
+                              // [4] lazy scheme: rows queued for phase 2, [5] residual jobs queued,
+                              // [6] phase 2's work claim counter
     int32_t *counters;
     unsigned long long *rowarg;   // greedy rows' (max key, ~lowest position), from the stream kernel
     float *gstats;            // per-row segment statistics [R][3][npad] (stream -> select kernel)
@@ -187,6 +201,13 @@ struct Args {
     int onehot;               // 1: one-hot drafts -- every row is sampled and the drafts are
                               // accepted while they equal the samples (q is not read)
     int withhold;             // testing aid: the stream kernel's CTA 0 withholds its first unit
+    // lazy scheme (rows after a request's first rejection are never read):
+    int phase;                // 0: every row at once; 1: each request's row 0; 2: the queued rows
+    int ctas;                 // stream kernel: CTAs the launch would use for every row
+    int32_t *jobcnt;          // per residual job: slices done
+    int32_t *listb;           // rows queued for phase 2 (count in hdr[4])
+    int32_t *jobs;            // residual jobs (request, row), count in hdr[5]
+    float *jobsum;            // per job and segment: sum of max(0, p - q), then sum of p
 };
 
 }  // namespace sv

@@ -382,15 +382,15 @@ __device__ __forceinline__ void seg_values(const RowCtx &S, const E *row, int V,
     patch_seg(S, seg * SEG, v);
 }
 
-// Calls f(seg, v, qv) for every segment of a row held in global memory (v: the lane's 8
-// penalised values; qv: the draft row's 8 values when WITHQ, else zeros).  Each warp takes
-// segments warp, warp + kWarps, ... and has U of them in flight before it uses any, so a
-// full pass is not one memory latency per segment.
+// Calls f(seg, v, qv) for every segment s_lo <= seg < nseg of a row held in global memory (v:
+// the lane's 8 penalised values; qv: the draft row's 8 values when WITHQ, else zeros).  Each
+// warp takes segments s_lo + warp, s_lo + warp + kWarps, ... and has U of them in flight
+// before it uses any, so a full pass is not one memory latency per segment.
 template <typename E, bool VEC, bool QVEC, bool WITHQ, int U, class G, class F>
-__device__ __forceinline__ void pass_segments(const G &g, const RowCtx &S, const E *row, const float *qrow, int V,
-                                              int nseg, F &&f) {
+__device__ __forceinline__ void pass_segment_range(const G &g, const RowCtx &S, const E *row, const float *qrow,
+                                                   int V, int s_lo, int nseg, F &&f) {
     const int lane = g.lane();
-    for (int s0 = g.warp(); s0 < nseg; s0 += G::kWarps * U) {
+    for (int s0 = s_lo + g.warp(); s0 < nseg; s0 += G::kWarps * U) {
         Raw8<E> raw[U];
         float qv[U][8];
 #pragma unroll
@@ -416,6 +416,13 @@ __device__ __forceinline__ void pass_segments(const G &g, const RowCtx &S, const
             }
         }
     }
+}
+
+// As pass_segment_range over the whole row.
+template <typename E, bool VEC, bool QVEC, bool WITHQ, int U, class G, class F>
+__device__ __forceinline__ void pass_segments(const G &g, const RowCtx &S, const E *row, const float *qrow, int V,
+                                              int nseg, F &&f) {
+    pass_segment_range<E, VEC, QVEC, WITHQ, U>(g, S, row, qrow, V, 0, nseg, f);
 }
 
 // Per-segment statistics of a row, written by the streaming pass.

@@ -944,8 +944,11 @@ __device__ __forceinline__ bool accept_test(float p, float q, float u) {
 // first rejection (one lane per draft, ballot), pick the final token, write the outputs.
 // Under the one-hot scheme a draft is rejected when it differs from its row's own sample, and
 // the final token is the stopping row's sample.
-template <typename E, bool VEC, bool QVEC, class G>
-__device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
+// `lim`: the last row whose statistics exist (the lazy scheme finalises a request that stops at
+// row 0 before its other rows are read); rows past it are never the stopping row.
+// LAZY: the lazy scheme's finaliser, which queues a whole-row residual instead of drawing it.
+template <typename E, bool VEC, bool QVEC, bool LAZY = false, class G>
+__device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X, int lim = 0x7fffffff) {
     const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
     int *xs = reinterpret_cast<int *>(X.cand);   // the request's draft tokens, for the outputs
     if (g.warp() == 0) {
@@ -962,7 +965,7 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
                 const int i = i0 + lane;
                 bool rej = false;
                 int kind = KIND_SKIP, argm = -1, bonus = -1, resid = -1;
-                if (i <= k) {
+                if (i <= k && i <= lim) {
                     const RowStat *st = A.stats + r0 + i;
                     kind = __ldcg(&st->kind);
                     argm = __ldcg(&st->argmax);
@@ -1028,7 +1031,15 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
         }
     }
     g.sync();
-    if (S.need_resid) {
+    if (LAZY && S.need_resid) {
+        // the lazy scheme queues the whole-row residual for its residual kernel, which draws
+        // the final token (out_tokens[b][a] holds -1 until then)
+        if (g.t == 0) {
+            const int jj = atomicAdd(A.hdr + 5, 1);
+            A.jobs[2 * jj] = b;
+            A.jobs[2 * jj + 1] = S.a;
+        }
+    } else if (S.need_resid) {
         // residual max(0, p - q) over a whole row (rows that keep too many tokens for a list)
         const int a = S.a;
         const RowStat st = load_stat(A.stats + r0 + a);
@@ -1058,6 +1069,42 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X)
     }
 }
 
+// Lazy scheme ("Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in
+// Rust", "The Verification Algorithm": the loop returns at the first rejection, so the rows
+// after it are never needed).  After a request's row 0: it stops there -- it is invalid, has
+// no drafts, or row 0 rejects its draft -- and is finalised from that row alone; or it queues
+// its rows 1..k for the second phase, having counted row 0 as arrived.  The whole group calls.
+template <typename E, bool VEC, bool QVEC, class G>
+__device__ void first_row_decision(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
+    g.sync();
+    if (g.t == 0) {
+        bool stop = S.status != 0 || S.k == 0 || !S.active;
+        if (!stop) {
+            const int x = __ldg(A.tokens + S.d0);
+            if (x < 0 || x >= A.V) stop = true;   // (the finaliser reports the bad token)
+            else if (S.greedy) stop = x != __ldcg(&A.stats[S.r].argmax);
+            else if (A.onehot) stop = x != __ldcg(&A.stats[S.r].bonus);
+            else stop = !accept_test(__ldcg(A.pq + (size_t)S.d0 * 2), __ldcg(A.pq + (size_t)S.d0 * 2 + 1),
+                                     __ldg(A.uni + (size_t)S.r * 2));
+        }
+        S.last = stop ? 1 : 0;
+        if (!stop) {
+            const int pos = atomicAdd(A.hdr + 4, S.k);
+            for (int i = 1; i <= S.k; i++) A.listb[pos + i - 1] = S.r0 + i;
+            A.counters[S.b] = 1;
+        } else if (A.out_pq && S.status == 0) {
+            // drafts past the stopping row are never read: no (p, q) for them
+            for (int i = 1; i < S.k; i++) {
+                A.out_pq[(size_t)(S.d0 + i) * 2] = NAN;
+                A.out_pq[(size_t)(S.d0 + i) * 2 + 1] = NAN;
+            }
+        }
+    }
+    g.sync();
+    if (S.last) finalize<E, VEC, QVEC, true>(g, A, S, X, 0);
+    g.sync();
+}
+
 // Writes -1 outputs for request b (no rows, or inconsistent row_offsets).
 template <class G>
 __device__ __forceinline__ void fail_request(const G &g, const Args &A, int b) {
@@ -1081,7 +1128,7 @@ __device__ __forceinline__ void fail_empty_requests(const G &g, const Args &A, c
 
 // After a row: count it towards its request; the group that brings the count to the
 // request's row count finalises it.  Every thread of the group must call this.
-template <typename E, bool VEC, bool QVEC, class G>
+template <typename E, bool VEC, bool QVEC, bool LAZY = false, class G>
 __device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
     g.sync();
     if (g.t == 0) {
@@ -1089,11 +1136,13 @@ __device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, R
         // before by the barrier above)
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(A.counters + S.b) : "memory");
-        S.last = (old == S.nrows - 1);
+        // every row of the request's slot counts, except under the lazy scheme's second phase,
+        // which reads rows 1..k after the first phase counted row 0
+        S.last = (old == (LAZY ? S.k : S.nrows - 1));
     }
     g.sync();
     if (S.last) {
-        finalize<E, VEC, QVEC>(g, A, S, X);
+        finalize<E, VEC, QVEC, LAZY>(g, A, S, X);
 #ifdef SV_TIMING
         if (g.t == 0) A.timing[(size_t)S.tix * NTIME + 7] = 1;
 #endif

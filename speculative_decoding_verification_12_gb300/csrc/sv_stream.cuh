@@ -97,7 +97,7 @@ __device__ __forceinline__ void arg_clean(const Raw8<E> &raw, int seg, ArgRun<E>
 
 // The history part of patch_seg out of line, for the inlined greedy path (keeps its registers
 // out of the streaming loop; v goes through memory only for rows that have a history).
-__device__ __noinline__ void patch_hist_ext(const RowCtx &R, int seg_lo, float *v) {
+static __device__ __noinline__ void patch_hist_ext(const RowCtx &R, int seg_lo, float *v) {
     float w[8];
 #pragma unroll
     for (int t = 0; t < 8; t++) w[t] = v[t];

@@ -47,8 +47,10 @@ def flagged(ora, b, where):
     return bool((int(ora["near_rows"][b]) >> i) & 1) if i < 64 else False
 
 
-def compare(w, gpu, ora, requests=None, check_share=False):
-    """Asserts parity; returns a summary dict (requests compared, near-ties by kind, ...)."""
+def compare(w, gpu, ora, requests=None, check_share=False, pq_on_path=False):
+    """Asserts parity; returns a summary dict (requests compared, near-ties by kind, ...).
+    pq_on_path: compare p(x_i), q(x_i) only for the drafts both sides read (i <= the smaller
+    accept length) -- the lazy scheme reads no row after a request's stopping row."""
     reqs = [int(b) for b in (range(w.B) if requests is None else requests)]
     n_cmp = n_near_req = n_excused = 0
     mism, excused = [], []
@@ -76,7 +78,10 @@ def compare(w, gpu, ora, requests=None, check_share=False):
             if ora["error"][b] or w.greedy[b]:
                 continue
             d0 = w.draft_start(b)
-            for i in range(int(w.num_drafts[b])):
+            n_i = int(w.num_drafts[b])
+            if pq_on_path:
+                n_i = min(n_i, 1 + min(int(gpu["accept_len"][b]), int(ora["accept_len"][b])))
+            for i in range(n_i):
                 d = d0 + i
                 if ora["pq_near"][d]:
                     continue
