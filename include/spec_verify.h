@@ -66,7 +66,10 @@ enum {
     SV_DEV_BAD_UNIFORM = 5,
     SV_DEV_BAD_PENALTY = 6,
     SV_DEV_TIMEOUT = 7,       /* a wait of the streaming kernel ran out (2 s): every request
-                                 of the call then has -1 outputs                            */
+                                 has -1 outputs (spec_verify_lazy: every one not yet decided),
+                                 except in one-pass calls over more rows than the select kernel
+                                 holds at once (9 per SM), where only the requests with a row
+                                 that was not streamed do; the others' outputs are exact    */
     SV_DEV_BAD_HISTORY = 8    /* prior history: offsets decrease or pass prior_len, an id outside
                                  [0, V), ids not strictly ascending, or a count below 1      */
 };
@@ -104,7 +107,10 @@ size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V);
  * Layout.  Request b owns target rows [row_offsets[b], row_offsets[b+1]) of target_logits and
  * the draft rows [row_offsets[b] - b, row_offsets[b+1] - b - 1) of draft_probs/draft_tokens; it
  * uses its first num_drafts[b] + 1 rows and num_drafts[b] drafts (ragged batches: pack with
- * row_offsets[b+1] - row_offsets[b] = num_drafts[b] + 1).  With row_offsets == NULL the
+ * row_offsets[b+1] - row_offsets[b] = num_drafts[b] + 1).  A request that owns no rows is a
+ * layout error (-1 outputs); the draft rows of the request after it then start one slot early,
+ * on the last draft slot of the requests before it, and either may write that slot's out_pq.
+ * With row_offsets == NULL the
  * batch is uniform: target_logits [B, k_max+1, V], draft_probs [B, k_max, V], draft_tokens
  * [B, k_max], uniforms [B, k_max+1, 2], total_rows = B * (k_max + 1); requests may still use
  * fewer than k_max drafts.
@@ -271,12 +277,13 @@ sv_status sv_read_device_error(const void *workspace, int32_t *code, int32_t *fi
 sv_status sv_set_phase_events(void *stream_kernel_start, void *stream_kernel_end);
 
 /* Testing aid for the failure path: while `on` is nonzero, the streaming kernel of every
- * spec_verify / spec_verify_onehot call that takes the two-kernel path (16-byte aligned rows)
- * withholds one work unit from its copy and reduction warps, as a stalled scheduler would.
- * Their bounded waits run out after 2 s; the call then completes with -1 for every request's
- * outputs and SV_DEV_TIMEOUT in the workspace's error word, and the device stays usable.  No
- * page has a counterpart: it exists so that the timeout path can be tested without a GPU
- * fault.  Process-wide, for every device; returns SV_OK.  Never set it in production. */
+ * spec_verify / spec_verify_onehot / spec_verify_lazy call that takes the streaming path
+ * (16-byte aligned rows) withholds one work unit from its copy and reduction warps, as a
+ * stalled scheduler would.  Their bounded waits run out after 2 s; the call then completes
+ * with -1 outputs for the requests SV_DEV_TIMEOUT describes, that code in the workspace's
+ * error word, and the device stays usable.  No page has a counterpart: it exists so that the
+ * timeout path can be tested without a GPU fault.  Process-wide, for every device; returns
+ * SV_OK.  Never set it in production. */
 sv_status sv_set_test_withhold(int32_t on);
 
 /* Human-readable name of a status code. */

@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <chrono>
 
 #include "../../include/spec_verify.h"
 #include "sv_launch.h"
@@ -85,12 +86,34 @@ static cudaError_t current_device(int &dev) {
     if (e != cudaSuccess) return e;
     return (dev < 0 || dev >= MAX_DEVICES) ? cudaErrorNotSupported : cudaSuccess;
 }
-// Clears n16 16-byte words at p (the workspace header, counters and argmax keys).  Lets its
+// Clears n16 16-byte words at p (the workspace header, counters and argmax keys); with
+// `order`, block 0 also builds the one-pass call's streaming order (build_order).  Lets its
 // programmatic dependent (the stream kernel) start at once; that kernel waits before use.
-__global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16) {
+__global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const Args A, int order) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);
+#ifdef SV_TIMING
+    if (order && blockIdx.x == 0 && threadIdx.x == 0) A.timing[(size_t)5 * A.R * NTIME + 0] = global_ns();
+#endif
+    if (order && blockIdx.x == 0) build_order<256>(A);
+#ifdef SV_TIMING
+    if (order && blockIdx.x == 0 && threadIdx.x == 0) A.timing[(size_t)5 * A.R * NTIME + 1] = global_ns();
+#endif
+}
+
+// Per-call epochs (tags of the ready words; never 0) and the per-process key of the order flag.
+static std::atomic<uint32_t> g_epoch{0};
+static uint32_t process_key() {
+    static const uint32_t key = [] {
+        uint64_t x = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() ^
+                     ((uint64_t)(uintptr_t)&g_epoch << 17) ^ 0x9E3779B97F4A7C15ull;
+        x ^= x >> 33;
+        x *= 0xFF51AFD7ED558CCDull;
+        x ^= x >> 33;
+        return (uint32_t)x | 1u;
+    }();
+    return key;
 }
 // Events recorded around the stream kernel when set (sv_set_phase_events): process-wide, for
 // every device and stream (a measurement aid for one caller at a time).  Recording them
@@ -190,6 +213,14 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     A.withhold = g_withhold.load() ? 1 : 0;
     A.phase = 0;
     A.ctas = 0;
+    A.partcnt = reinterpret_cast<int32_t *>(ws + L.partcnt);
+    A.ready = reinterpret_cast<uint32_t *>(ws + L.ready);
+    A.ordflag = reinterpret_cast<unsigned long long *>(ws + L.order);
+    A.rowmap = reinterpret_cast<int32_t *>(ws + L.order + 16);
+    uint32_t ep = g_epoch.fetch_add(1) + 1;
+    if ((ep & 0x7fffffffu) == 0) ep = g_epoch.fetch_add(1) + 1;   // (2 * epoch + 1 fits 32 bits; never 0)
+    A.epoch = ep & 0x7fffffffu;
+    A.key = process_key();
     const size_t esz = logits_dtype == SV_BF16 ? 2 : 4;
     const bool vec = ((uintptr_t)target_logits % 16 == 0) && ((size_t)V * esz) % 16 == 0;
     const bool qvec = (!draft_probs || (uintptr_t)draft_probs % 16 == 0) && ((size_t)V * 4) % 16 == 0;
@@ -197,25 +228,31 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int dev = 0;
     if (current_device(dev) != cudaSuccess) return SV_ERR_UNSUPPORTED;
-    // clear the error word, the work claim counter, the per-request arrival counters, the
-    // per-row part counters and the greedy rows' argmax keys
-    {
-        // (the clear ends below the statistics region, which starts at a 256-byte boundary)
-        const size_t n16 = (L.rowarg + (size_t)total_rows * 8 + 15) / 16;
-        const unsigned blocks = (unsigned)((n16 + 255) / 256 < 304 ? (n16 + 255) / 256 : 304);
-        clear_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4 *>(ws), n16);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-    }
-    if (A.hoff) {
-        history_kernel<<<B, 256, 0, st>>>(A, params.prior_len);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-    }
     // multiprocessors per device, read once (0: not read yet)
     static std::atomic<int> sms[MAX_DEVICES];
     int nsm = sms[dev].load(std::memory_order_relaxed);
     if (!nsm) {
         if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SV_ERR_CUDA;
         sms[dev].store(nsm, std::memory_order_relaxed);
+    }
+    // The one-pass two-kernel path selects each row as soon as it is streamed when the batch has
+    // more rows than the select kernel holds at once: its first wave then runs while the stream
+    // ends.  With one wave, early select CTAs would only share the SMs with the stream's last
+    // units, so every row is selected once the whole stream is done.
+    A.perrow = (vec && !lazy && (long long)total_rows > (long long)SEL_PER_SM * nsm) ? 1 : 0;
+    // clear the error word, the work claim counter, the per-request arrival counters, the
+    // per-row part counters and the greedy rows' argmax keys
+    {
+        // (the clear ends below the statistics region, which starts at a 256-byte boundary)
+        const size_t n16 = (L.rowarg + (size_t)total_rows * 8 + 15) / 16;
+        const unsigned blocks = (unsigned)((n16 + 255) / 256 < 304 ? (n16 + 255) / 256 : 304);
+        // (with per-row selection, block 0 also builds the streaming order)
+        clear_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4 *>(ws), n16, A, A.perrow);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    }
+    if (A.hoff) {
+        history_kernel<<<B, 256, 0, st>>>(A, params.prior_len);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     }
     const LaunchOpts o{nsm, g_phase_start.load(), g_phase_end.load()};
     const bool bf16 = logits_dtype == SV_BF16;

@@ -31,29 +31,36 @@ constexpr double FIXED_ONE = 1099511627776.0;   // 2^40: fixed-point scale of to
 constexpr int RT = 256;
 
 // Stream kernel (16-byte aligned rows), SCTA CTAs per SM: warp 0 issues bulk copies, warp 1
-// schedules work units, PSTREAM warps reduce the streamed chunks.  Select kernel: SELT threads
-// per row.
+// schedules work units, pstream<E>() warps reduce the streamed chunks (8 for bf16; 6 for fp32,
+// whose 12 segments per chunk then split evenly).  Select kernel: SELT threads per row.
 #ifndef SV_SCTA
 #define SV_SCTA 3
 #endif
 #ifndef SV_PSTREAM
 #define SV_PSTREAM 8
 #endif
+#ifndef SV_PSTREAM_F32
+#define SV_PSTREAM_F32 6
+#endif
 #ifndef SV_SPLIT_PARTS
 #define SV_SPLIT_PARTS 4              // parts the last wave of rows is split into (1: no split)
 #endif
 constexpr int SCTA = SV_SCTA;
-constexpr int PSTREAM = SV_PSTREAM;
 constexpr int SPLIT_PARTS = SV_SPLIT_PARTS;
+template <typename E>
+__host__ __device__ constexpr int pstream() { return sizeof(E) == 2 ? SV_PSTREAM : SV_PSTREAM_F32; }
+template <typename E>
+__host__ __device__ constexpr int stream_threads() { return 32 * (2 + pstream<E>()); }
 #ifndef SV_SPLIT_WAVES
 #define SV_SPLIT_WAVES 2
 #endif
 constexpr int SPLIT_WAVES = SV_SPLIT_WAVES;   // waves of rows (one row per CTA each) that are split
-constexpr int ST = 32 * (2 + PSTREAM);
 #ifndef SV_SELT
 #define SV_SELT 128
 #endif
 constexpr int SELT = SV_SELT;         // threads per select CTA (one row each)
+// select CTAs resident per SM (the select kernel's launch bound: 56 registers a thread)
+constexpr int SEL_PER_SM = SELT >= 128 ? 9 : 1152 / SELT;
 #ifndef SV_PNS_MAX
 #define SV_PNS_MAX 16
 #endif
@@ -100,7 +107,8 @@ struct __align__(16) RowStat {
 };
 
 struct WsLayout {
-    size_t counters, jobcnt, rowarg, stats, pq, prep, gstats, hdir, hmask, hstat, listb, jobs, jobsum, timing, total;
+    size_t counters, jobcnt, partcnt, rowarg, stats, pq, prep, gstats, hdir, hmask, hstat, listb, jobs, jobsum,
+        ready, order, timing, total;
 };
 
 // Phase timestamps (globaltimer ns) per work unit, recorded only in builds with SV_TIMING.
@@ -113,13 +121,16 @@ __host__ __device__ inline int nseg_pad(int nseg) { return (nseg + 31) & ~31; }
 
 // Workspace: [header 256 B: error word, first bad request, work claim counter, stream failure
 // flag, lazy scheme: queued row count, residual job count, second work claim counter]
-// [per-request arrival counters][per-job slice arrival counters][per-row argmax keys of greedy rows]
+// [per-request arrival counters][per-job slice arrival counters][per-row counts of the stream
+// kernel's finished shares][per-row argmax keys of greedy rows]
 // [RowStat per row][(p, q) per draft][prepared row context, 640 B per row]
 // [segment statistics: 3 words per padded segment per row]
 // [history index: np+1 words per request][history segment mask: np/32 words per request]
 // [history status: 1 word per request]
 // [lazy scheme: queued rows, 1 word per row; residual jobs, 2 words per request; the jobs'
 // per-segment residual and target sums, 2 words per padded segment per request]
+// [per-row ready words (the call's epoch once the row's statistics are complete)]
+// [the streaming order: a ready word, then the row at each position (R words)]
 // [timing, SV_TIMING builds only].  The header, the counters and the argmax keys are cleared
 // by every call; the history regions are written by the history prepass of calls that pass a
 // history, the lazy regions only by the lazy scheme.
@@ -130,7 +141,9 @@ __host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     L.counters = o;
     o += size_t(B) * 4;
     L.jobcnt = o;
-    o = (o + size_t(B) * 4 + 7) & ~size_t(7);
+    o += size_t(B) * 4;
+    L.partcnt = o;
+    o = (o + size_t(R) * 4 + 7) & ~size_t(7);
     L.rowarg = o;
     o = up256(o + size_t(R) * 8);
     L.stats = o;
@@ -153,6 +166,10 @@ __host__ __device__ inline WsLayout ws_layout(int B, int R, int V) {
     o = up256(o + size_t(B) * 8);
     L.jobsum = o;
     o = up256(o + size_t(B) * np * 8);
+    L.ready = o;
+    o = up256(o + size_t(R) * 4);
+    L.order = o;
+    o = up256(o + 16 + size_t(R) * 4);
     L.timing = o;
 #ifdef SV_TIMING
     o = up256(o + size_t(R) * PMAX * NTIME * 8);
@@ -206,6 +223,15 @@ struct Args {
     int ctas;                 // stream kernel: CTAs the launch would use for every row
     int32_t *jobcnt;          // per residual job: slices done
     int32_t *listb;           // rows queued for phase 2 (count in hdr[4])
+    // one-pass call: rows are streamed (and selected) in an order of requests -- sampled ones
+    // first, greedy ones last -- and each row is selected as soon as its statistics are complete
+    uint32_t epoch;           // this call's tag for the ready words (distinct per call)
+    int32_t *partcnt;         // per row: finished shares (streamer warps per part, and the preparation)
+    uint32_t *ready;          // per row: epoch once the row's statistics and context are in place
+    unsigned long long *ordflag;  // key << 32 | (2 * epoch + (1: identity order)) once the order is written
+    uint32_t key;             // per-process random tag of ordflag (an old or arbitrary word never matches)
+    int32_t *rowmap;          // the row at each position of that order
+    int perrow;               // one-pass call: select each row once it is streamed (else once all are)
     int32_t *jobs;            // residual jobs (request, row), count in hdr[5]
     float *jobsum;            // per job and segment: sum of max(0, p - q), then sum of p
 };

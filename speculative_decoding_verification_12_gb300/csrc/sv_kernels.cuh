@@ -175,12 +175,13 @@ __device__ __forceinline__ int listed_row(const Args &A, int li) {
 }
 
 // A stream CTA gave up on a bounded wait: record SV_DEV_TIMEOUT and raise the call's stream
-// failure flag (header word 3), from which every select CTA marks its row KIND_FAIL -- rows
-// this CTA had claimed were never reduced, so no request of the call can be trusted.
+// failure flag (header word 3).  Rows this CTA had claimed were never reduced: with whole-grid
+// selection every select CTA then fails its row's request, with per-row selection those whose
+// row never became ready do.
 __device__ __forceinline__ void sfail(const Args &A, SShared &P, int b) {
     P.fail = 1;
     record_error(A, 7, b < 0 ? 0 : b);
-    // every writer stores the same value; the select kernel reads it once the stream grid is done
+    // every writer stores the same value
     *reinterpret_cast<volatile int32_t *>(A.hdr + 3) = 1;
 }
 
@@ -200,11 +201,18 @@ static __device__ __noinline__ void drain_copies(unsigned long long *full, int q
 // fp32 rows hold twice the registers per segment: two CTAs per SM instead of SCTA
 template <typename E>
 __host__ __device__ constexpr int stream_ctas() { return sizeof(E) == 2 ? SCTA : (SCTA < 2 ? SCTA : 2); }
+// How the stream and select kernels of a call work together; each has an instance per scheme,
+// which holds none of the others' code.
+enum : int {
+    SCH_GRID = 0,   // one-pass call: every row selected once the whole stream grid is done
+    SCH_ROWS = 1,   // one-pass call: rows streamed in the order the clearing kernel built, each
+                    // selected as soon as its own units are streamed (per-row ready words)
+    SCH_LAZY = 2    // the lazy scheme's launches (phases 1 and 2)
+};
 
-// LAZY: the instance for the lazy scheme's launches (phases 1 and 2); the one-pass launch uses
-// the other, which holds none of that code.
-template <typename E, bool HIST, bool LAZY>
-__global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args A) {
+template <typename E, bool HIST, int SCH>
+__global__ void __launch_bounds__(stream_threads<E>(), stream_ctas<E>()) stream_kernel(const Args A) {
+    constexpr bool LAZY = SCH == SCH_LAZY, PERROW = SCH == SCH_ROWS;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ SShared P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -219,11 +227,11 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
     if (threadIdx.x == 0) {
         for (int s = 0; s < PNS; s++) {
             mbar_init(&P.full[s], 1);
-            mbar_init(&P.empty[s], PSTREAM);
+            mbar_init(&P.empty[s], pstream<E>());
         }
         for (int s = 0; s < NRB; s++) {
             mbar_init(&P.rb_desc[s], 1);
-            mbar_init(&P.rb_done[s], PSTREAM);
+            mbar_init(&P.rb_done[s], pstream<E>());
         }
         P.fail = 0;
         mbar_fence_init();
@@ -232,6 +240,9 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
     // the workspace words this kernel counts on were cleared by the kernel before it (this one
     // may start early, as its programmatic dependent): wait for them
     asm volatile("griddepcontrol.wait;" ::: "memory");
+#ifdef SV_TIMING
+    if (threadIdx.x == 0) atomicMin(A.timing + (size_t)5 * A.R * NTIME + 2, global_ns());
+#endif
 
     if (warp == 0) {
         // ---- issuer (one thread): bulk copies of each prepared unit, chunk by chunk
@@ -270,9 +281,12 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
         // this launch streams (listed_row): every row, each request's first row, or the rows
         // the first phase of the lazy scheme queued (counted once the wait above is over).
         int rows = A.R, nsplit = A.nsplit;
+        bool ident = true;   // per-row selection: stream in the order the clearing kernel built
         if constexpr (LAZY) {
             rows = A.phase == 1 ? A.B : __ldcg(A.hdr + 4);
             nsplit = NP > 1 ? min(rows, A.ctas * SPLIT_WAVES) : 0;
+        } else if constexpr (PERROW) {
+            ident = (__ldcg(A.ordflag) & 1ull) != 0;
         }
         const long long whole = (long long)rows - nsplit;
         const long long units = whole + (long long)nsplit * NP;
@@ -285,6 +299,10 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
                 return;
             }
             RowCtx &R = P.rc[slot];
+            // The unit this slot held is streamed (the streamer warps' arrivals release their
+            // writes to this warp): publish it as one share of its row.  The scheduler, not each
+            // streamer warp, pays the fence, and it waits on exactly this unit anyway.
+            if (PERROW && j >= NRB && lane == 0) row_share_done(A, R.r, R.nparts);
             int u = 0;
             // (the lazy scheme's second phase claims from a counter of its own)
             if (lane == 0) u = atomicAdd(A.hdr + (LAZY && A.phase == 2 ? 6 : 2), 1);
@@ -293,6 +311,17 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
                 if (lane == 0) {
                     R.r = -1;
                     mbar_arrive(&P.rb_desc[slot]);
+                }
+                if constexpr (PERROW) {
+                    // the units still in flight, oldest first, published as they finish
+                    for (int jj = j - NRB + 1 < 0 ? 0 : j - NRB + 1; jj < j; jj++) {
+                        const int sl = jj % NRB;
+                        if (!__all_sync(0xffffffffu, mbar_wait(&P.rb_done[sl], (uint32_t)(jj / NRB) & 1u))) {
+                            if (lane == 0) sfail(A, P, -1);
+                            return;
+                        }
+                        if (lane == 0) row_share_done(A, P.rc[sl].r, P.rc[sl].nparts);
+                    }
                 }
                 return;
             }
@@ -314,7 +343,7 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
                 part = t - (t / NP) * NP;
                 npu = NP;
             }
-            const int r = LAZY ? listed_row(A, li) : li;
+            const int r = LAZY ? listed_row(A, li) : (PERROW && !ident ? order_row(A, li) : li);
             if (!LAZY || r >= 0) {
                 locate_row(A, R, r);
                 if (R.active) build_penalties(A, R, R.i);
@@ -358,6 +387,8 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
                 const int4 *src = reinterpret_cast<const int4 *>(&R);
                 int4 *dst = A.prep + (size_t)r * (PREP_BYTES / 16);
                 for (int t = lane; t < PREP_BYTES / 16; t += 32) dst[t] = src[t];
+                // (published with the unit's completion, by this warp: its lanes' writes are
+                // ordered before that by the warp barriers in between)
             }
             __syncwarp();
         }
@@ -392,36 +423,118 @@ __global__ void __launch_bounds__(ST, stream_ctas<E>()) stream_kernel(const Args
     }
 }
 
+// A row the select kernel cannot trust (it was not streamed in full): its request's outputs
+// become -1, its draft's (p, q) NaN, and SV_DEV_TIMEOUT is recorded.  The request is not
+// finalised, since this row never arrives.  One warp.
+__device__ __forceinline__ void fail_unstreamed_row(const Args &A, int r) {
+    const int lane = lane_id();
+    const int b = A.row_off ? find_request(A.row_off, A.B, r) : r / (A.k_max + 1);
+    if (b < 0 || b >= A.B) {
+        if (lane == 0) record_error(A, 7, 0);
+        return;
+    }
+    const int r0 = A.row_off ? __ldg(A.row_off + b) : b * (A.k_max + 1);
+    const int kw = A.k_max + 1;
+    for (int j = lane; j < kw; j += 32) A.out_tok[(size_t)b * kw + j] = -1;
+    if (lane == 0) {
+        A.acc[b] = -1;
+        record_error(A, 7, b);
+        const int i = r - r0, k = min(__ldg(A.nd + b), A.k_max);
+        if (i >= 0 && i < k) {
+            const size_t d = (size_t)(r0 - b + i);
+            A.pq[d * 2] = NAN;
+            A.pq[d * 2 + 1] = NAN;
+            if (A.out_pq) {
+                A.out_pq[d * 2] = NAN;
+                A.out_pq[d * 2 + 1] = NAN;
+            }
+        }
+    }
+}
+
 // One CTA per row: the row's kept set, draws and draft probabilities from the statistics the
 // stream kernel wrote; the request's last row finalises the request.
-template <typename E, bool QVEC, bool LAZY>
-__global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_kernel(const Args A) {
+template <typename E, bool QVEC, int SCH>
+__global__ void __launch_bounds__(SELT, SEL_PER_SM) select_kernel(const Args A) {
+    constexpr bool LAZY = SCH == SCH_LAZY, PERROW = SCH == SCH_ROWS;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ RowCtx S;
     const Grp<SELT, 0> g(threadIdx.x);
     const int np = nseg_pad(A.nseg);
     float *sb = reinterpret_cast<float *>(dsm);
     const Scratch X = carve_scratch(dsm + up128((size_t)3 * np * 4), np, dsm, select_smem(A.nseg));
-    // a later launch of the lazy scheme may be scheduled as soon as SMs free up
-    if constexpr (LAZY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // the stream kernel's results (and every earlier write on the stream) are visible past here
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // this CTA's row: every row in turn, each request's first row, or a row the first phase of
-    // the lazy scheme queued
+    // this CTA's row: the row at its streaming position (one-pass call), each request's first
+    // row, or a row the first phase of the lazy scheme queued
     int r = blockIdx.x;
-    if constexpr (LAZY) {
-        if (A.phase == 1) {
-            r = first_row(A, blockIdx.x);
-            if (r < 0) {   // a request that owns no rows
-                fail_request(g, A, blockIdx.x);
-                return;
+    bool ready = true;
+#ifdef SV_TIMING
+    const unsigned long long tent = global_ns();
+#endif
+    if constexpr (PERROW) {
+        // Not a wait for the whole stream grid: the order, then this row alone.  The row is
+        // selected as soon as every unit of it is streamed, while later rows still stream.  Both
+        // waits are bounded, and the second ends early once a stream CTA has given up.
+        __shared__ int s_r, s_ok;
+        if (g.warp() == 0) {
+            unsigned long long of = 0;
+            int ok = 1;
+            const unsigned long long tag = ((unsigned long long)A.key << 32) | (2ull * A.epoch);
+            if (g.lane() == 0)
+                ok = wait_word(A.ordflag, ld_acquire_u64, [&](unsigned long long v) { return (v & ~1ull) == tag; }, &of);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            of = __shfl_sync(0xffffffffu, of, 0);
+            const int rr = (ok && !(of & 1ull)) ? order_row(A, (int)blockIdx.x) : (int)blockIdx.x;
+            if (g.lane() == 0) {
+                uint32_t v = 0;
+                if (ok) {
+                    wait_word(A.ready + rr, ld_acquire_u32,
+                              [&](uint32_t x) { return x == A.epoch || *(volatile const int32_t *)(A.hdr + 3) != 0; }, &v);
+                }
+                s_ok = ok && v == A.epoch;
+                s_r = rr;
             }
-        } else {
-            if ((int)blockIdx.x >= __ldcg(A.hdr + 4)) return;
-            r = __ldcg(A.listb + blockIdx.x);
         }
+        g.sync();
+        r = s_r;
+        ready = s_ok != 0;
+    } else {
+        // a later launch of the lazy scheme may be scheduled as soon as SMs free up
+        if constexpr (LAZY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        // the stream kernel's results (and every earlier write on the stream) are visible past here
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if constexpr (LAZY) {
+            if (A.phase == 1) {
+                r = first_row(A, blockIdx.x);
+                if (r < 0) {   // a request that owns no rows
+                    fail_request(g, A, blockIdx.x);
+                    return;
+                }
+            } else {
+                if ((int)blockIdx.x >= __ldcg(A.hdr + 4)) return;
+                r = __ldcg(A.listb + blockIdx.x);
+            }
+        }
+        // a stream CTA gave up on a wait: no row of this launch can be trusted
+        ready = __ldcg(A.hdr + 3) == 0;
     }
     SV_MARK(A, 4 * A.R + r, 1);
+#ifdef SV_TIMING
+    if (g.t == 0) {
+        A.timing[(size_t)(4 * A.R + r) * NTIME + 0] = tent;
+        atomicMin(A.timing + (size_t)5 * A.R * NTIME + 3, tent);
+    }
+#endif
+    // The CTA of the last position joins the stream grid before it ends, so that this grid
+    // (and whatever the stream runs after it) completes after the stream kernel.  That row is
+    // streamed last: the join costs the stream kernel's exit, not a wait for the whole stream.
+    const bool join = PERROW && blockIdx.x == gridDim.x - 1;
+    if (!ready) {
+        // The row was not (or not surely) streamed: a stream CTA gave up on a wait.  Its request
+        // gets -1 outputs and SV_DEV_TIMEOUT, and is never finalised (this row does not arrive).
+        if (g.warp() == 0) fail_unstreamed_row(A, r);
+        if (join) asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     // the row's prepared context and segment statistics, in one round of loads
     {
         const int4 *src = A.prep + (size_t)r * (PREP_BYTES / 16);
@@ -435,16 +548,10 @@ __global__ void __launch_bounds__(SELT, SELT >= 128 ? 9 : 1152 / SELT) select_ke
     g.sync();
 #endif
     SV_MARK(A, 4 * A.R + r, 2);
+    if (join) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (S.b < 0) return;   // a row outside every request: nothing to count
     if (!LAZY) fail_empty_requests(g, A, S);
-    if (S.active) {
-        if (__ldcg(A.hdr + 3) == 0) {
-            select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
-        } else if (g.t == 0) {
-            // a stream CTA gave up on a wait: this row's statistics cannot be trusted
-            fail_row(A, S);
-        }
-    }
+    if (S.active) select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
     SV_MARK(A, 4 * A.R + r, 4);
     if (LAZY && A.phase == 1) first_row_decision<E, true, QVEC>(g, A, S, X);
     else arrive_and_finalize<E, true, QVEC, LAZY>(g, A, S, X);
@@ -594,16 +701,16 @@ static unsigned stream_grid(const Args &B, long long ctas, long long rows) {
 }
 
 // Launches the stream kernel (SCTA CTAs per SM) and the select kernel as its programmatic
-// dependent; returns cudaErrorNotSupported (nothing launched) when the kernels cannot be
-// resident for this vocabulary.
-template <typename E, bool QVEC>
+// dependent, in scheme SCH (SCH_GRID or SCH_ROWS); returns cudaErrorNotSupported (nothing
+// launched) when the kernels cannot be resident for this vocabulary.
+template <typename E, bool QVEC, int SCH>
 static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream, const LaunchOpts &o) {
     Args B = A;
     StreamPlan pl;
     if (!plan_stream<E>(B, o, pl)) return cudaErrorNotSupported;
     // the stream kernel with the history variants only when the call passes a history
-    auto k1 = A.hoff ? stream_kernel<E, true, false> : stream_kernel<E, false, false>;
-    auto k2 = select_kernel<E, QVEC, false>;
+    auto k1 = A.hoff ? stream_kernel<E, true, SCH> : stream_kernel<E, false, SCH>;
+    auto k2 = select_kernel<E, QVEC, SCH>;
     cudaError_t e;
     if ((e = ensure_smem(k1, pl.smem1)) != cudaSuccess) return e;
     if ((e = ensure_smem(k2, pl.smem2)) != cudaSuccess) return e;
@@ -611,7 +718,7 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream, const 
     B.nsplit = B.nparts > 1 ? (int)(pl.ctas * SPLIT_WAVES < A.R ? pl.ctas * SPLIT_WAVES : A.R) : 0;
     if (o.ph0 && (e = cudaEventRecord(o.ph0, stream)) != cudaSuccess) return e;
     // a programmatic dependent of the clearing kernel (or of the history prepass)
-    if ((e = launch_dependent(k1, stream_grid(B, pl.ctas, A.R), ST, pl.smem1, stream, B)) != cudaSuccess) return e;
+    if ((e = launch_dependent(k1, stream_grid(B, pl.ctas, A.R), stream_threads<E>(), pl.smem1, stream, B)) != cudaSuccess) return e;
     if (o.ph1 && (e = cudaEventRecord(o.ph1, stream)) != cudaSuccess) return e;
     return launch_dependent(k2, (unsigned)A.R, SELT, pl.smem2, stream, B);
 }
@@ -623,29 +730,29 @@ static cudaError_t launch_lazy_kernels(const Args &A, cudaStream_t stream, const
     Args B = A;
     StreamPlan pl;
     if (!plan_stream<E>(B, o, pl)) return cudaErrorNotSupported;
-    auto k1 = A.hoff ? stream_kernel<E, true, true> : stream_kernel<E, false, true>;
-    auto k2 = select_kernel<E, QVEC, true>;
+    auto k1 = A.hoff ? stream_kernel<E, true, SCH_LAZY> : stream_kernel<E, false, SCH_LAZY>;
+    auto k2 = select_kernel<E, QVEC, SCH_LAZY>;
     auto k3 = resid_kernel<E, QVEC>;
     cudaError_t e;
     if ((e = ensure_smem(k1, pl.smem1)) != cudaSuccess) return e;
     if ((e = ensure_smem(k2, pl.smem2)) != cudaSuccess) return e;
     if ((e = ensure_smem(k3, pl.smem3)) != cudaSuccess) return e;
     B.phase = 1;
-    if ((e = launch_dependent(k1, stream_grid(B, pl.ctas, A.B), ST, pl.smem1, stream, B)) != cudaSuccess) return e;
+    if ((e = launch_dependent(k1, stream_grid(B, pl.ctas, A.B), stream_threads<E>(), pl.smem1, stream, B)) != cudaSuccess) return e;
     if ((e = launch_dependent(k2, (unsigned)A.B, SELT, pl.smem2, stream, B)) != cudaSuccess) return e;
     if (A.R == A.B) return cudaSuccess;   // no drafts: nothing is queued
     B.phase = 2;
-    if ((e = launch_dependent(k1, (unsigned)pl.ctas, ST, pl.smem1, stream, B)) != cudaSuccess) return e;
+    if ((e = launch_dependent(k1, (unsigned)pl.ctas, stream_threads<E>(), pl.smem1, stream, B)) != cudaSuccess) return e;
     if ((e = launch_dependent(k2, (unsigned)(A.R - A.B), SELT, pl.smem2, stream, B)) != cudaSuccess) return e;
     return launch_dependent(k3, (unsigned)A.B * RSL, RST, pl.smem3, stream, B);
 }
 
-// The one-pass call for logits of type E: the two kernels for aligned rows they can hold, else
-// the row kernel (any alignment).
+// The one-pass call for logits of type E with whole-grid selection: the two kernels for aligned
+// rows they can hold, else the row kernel (any alignment).
 template <typename E>
 static cudaError_t launch_onepass_dtype(const Args &A, cudaStream_t st, const LaunchOpts &o, bool vec, bool qvec) {
     cudaError_t e = cudaErrorNotSupported;
-    if (vec) e = qvec ? launch_two_kernels<E, true>(A, st, o) : launch_two_kernels<E, false>(A, st, o);
+    if (vec) e = qvec ? launch_two_kernels<E, true, SCH_GRID>(A, st, o) : launch_two_kernels<E, false, SCH_GRID>(A, st, o);
     if (e == cudaErrorNotSupported) {
         cudaGetLastError();   // clear a sticky "not supported" from the probe, if any
         if (vec) e = qvec ? launch_rows<E, true, true>(A, st) : launch_rows<E, true, false>(A, st);

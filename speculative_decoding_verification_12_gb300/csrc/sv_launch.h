@@ -21,6 +21,11 @@ struct LaunchOpts {
 cudaError_t launch_onepass_bf16(const Args &A, cudaStream_t stream, const LaunchOpts &o, bool vec, bool qvec);
 cudaError_t launch_onepass_f32(const Args &A, cudaStream_t stream, const LaunchOpts &o, bool vec, bool qvec);
 
+// The one-pass call with per-row selection (Args::perrow) for 16-byte aligned rows;
+// cudaErrorNotSupported (nothing launched) when the kernels cannot hold the vocabulary.
+cudaError_t launch_rows_bf16(const Args &A, cudaStream_t stream, const LaunchOpts &o, bool qvec);
+cudaError_t launch_rows_f32(const Args &A, cudaStream_t stream, const LaunchOpts &o, bool qvec);
+
 // The lazy scheme for 16-byte aligned rows; cudaErrorNotSupported (nothing launched) when the
 // kernels cannot hold the vocabulary.
 cudaError_t launch_lazy_bf16(const Args &A, cudaStream_t stream, const LaunchOpts &o, bool qvec);

@@ -94,6 +94,149 @@ __device__ __forceinline__ int find_request(const int32_t *off, int B, int r) {
     return ans;
 }
 
+// ------------------------------------------------------------------------------------------
+// streaming order and per-row readiness (one-pass call)
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Waits (one thread, bounded, sleeping between polls) until pred(*p) holds; the word's last
+// value goes to *last.  False once WAIT_NS has passed.
+template <typename T, typename LD, typename PRED>
+__device__ __forceinline__ bool wait_word(const T *p, LD ld, PRED pred, T *last) {
+    T v = ld(p);
+    if (pred(v)) {
+        *last = v;
+        return true;
+    }
+    const unsigned long long t0 = global_ns();
+    unsigned ns = 32;
+    while (!pred(v = ld(p))) {
+        __nanosleep(ns);
+        ns = ns < 256 ? ns * 2 : 256;
+        if (global_ns() - t0 > WAIT_NS) {
+            *last = v;
+            return false;
+        }
+    }
+    *last = v;
+    return true;
+}
+
+// Row at streaming position li (written by the clearing kernel, read through L2).
+__device__ __forceinline__ int order_row(const Args &A, int li) { return __ldcg(A.rowmap + li); }
+
+// The streaming order of a one-pass call: requests with sampled rows first, greedy ones last
+// (each group in request order), as the row at each position.  A greedy row's selection is
+// short, so rows streamed last finish soon after the stream; the sampled rows' longer
+// selections overlap the greedy rows' streaming.  Run by one block of NT threads, which also
+// zeroes every row's ready word; the stream kernel waits for this block.  A request's first
+// position is the rows of the requests before it in its own group (one block-wide scan per
+// group), after every sampled row when it is greedy.  Publishes key << 32 | 2 * epoch in
+// *ordflag once written, or with + 1 (the identity order) when row_offsets are inconsistent --
+// then every row keeps its place and the kernels' own checks report the layout.
+template <int NT>
+__device__ void build_order(const Args &A) {
+    constexpr int NW = NT / 32;
+    __shared__ int s_red[2][NW];
+    __shared__ int s_carry[2];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int B = A.B;
+    const unsigned long long tag = (unsigned long long)A.key << 32;
+    for (int r = t; r < A.R; r += NT) A.ready[r] = 0u;
+    // the layout's consistency, and the rows of the sampled group
+    bool ok = true;
+    int samp = 0;
+    for (int b = t; b < B; b += NT) {
+        const int r0 = A.row_off ? __ldg(A.row_off + b) : b * (A.k_max + 1);
+        const int r1 = A.row_off ? __ldg(A.row_off + b + 1) : r0 + A.k_max + 1;
+        if (r1 < r0 || (b == 0 && r0 != 0) || (b == B - 1 && r1 != A.R)) ok = false;
+        if (!__ldg(A.greedy + b)) samp += r1 - r0;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (t == 0) st_release_u64(A.ordflag, tag | (2u * A.epoch + 1u));
+        return;
+    }
+    // (consistent offsets: every count is >= 0 and they sum to R, so positions stay below R)
+    for (int o = 16; o > 0; o >>= 1) samp += __shfl_xor_sync(0xffffffffu, samp, o);
+    if (lane == 0) s_red[0][warp] = samp;
+    __syncthreads();
+    if (t == 0) {
+        int tot = 0;
+        for (int w = 0; w < NW; w++) tot += s_red[0][w];
+        s_carry[0] = 0;     // next position of the sampled group
+        s_carry[1] = tot;   // next position of the greedy group
+    }
+    __syncthreads();
+    for (int b0 = 0; b0 < B; b0 += NT) {
+        const int b = b0 + t;
+        int r0 = 0, n = 0;
+        bool gr = false;
+        if (b < B) {
+            r0 = A.row_off ? __ldg(A.row_off + b) : b * (A.k_max + 1);
+            n = (A.row_off ? __ldg(A.row_off + b + 1) : r0 + A.k_max + 1) - r0;
+            gr = __ldg(A.greedy + b) != 0;
+        }
+        // inclusive warp scans of the two groups' row counts
+        int is = gr ? 0 : n, ig = gr ? n : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ys = __shfl_up_sync(0xffffffffu, is, o), yg = __shfl_up_sync(0xffffffffu, ig, o);
+            if (lane >= o) {
+                is += ys;
+                ig += yg;
+            }
+        }
+        if (lane == 31) {
+            s_red[0][warp] = is;
+            s_red[1][warp] = ig;
+        }
+        __syncthreads();
+        int cs = s_carry[0], cg = s_carry[1];
+        for (int w = 0; w < warp; w++) {
+            cs += s_red[0][w];
+            cg += s_red[1][w];
+        }
+        const int pos = gr ? cg + ig - n : cs + is - n;
+        for (int j = 0; j < n; j++) A.rowmap[pos + j] = r0 + j;
+        __syncthreads();
+        if (t == 0) {
+            for (int w = 0; w < NW; w++) {
+                s_carry[0] += s_red[0][w];
+                s_carry[1] += s_red[1][w];
+            }
+        }
+        __syncthreads();
+    }
+    // (the barrier above orders every thread's writes before this release)
+    if (t == 0) st_release_u64(A.ordflag, tag | (2u * A.epoch));
+}
+
+// One finished share of row r (a streamed unit: the whole row, or one of its parts): the share
+// that completes the row publishes it ready for this call.  One thread, whose release covers
+// the writes it has synchronised with (the unit's streamer warps, through the unit barrier).
+__device__ __forceinline__ void row_share_done(const Args &A, int r, int shares) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(A.partcnt + r) : "memory");
+    if (old == shares - 1) st_release_u32(A.ready + r, A.epoch);
+}
+
 // Request-level checks shared by every row of the request (one thread).
 __device__ __forceinline__ void load_request(const Args &A, RowCtx &S, int b) {
     S.b = b;

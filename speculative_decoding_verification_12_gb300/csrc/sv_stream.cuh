@@ -189,8 +189,9 @@ __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned lo
                                            int V, int sw, const RowCtx &R, const SegStats &o, const uint32_t *dmask,
                                            unsigned long long *argslot, unsigned long long *tslot) {
     constexpr int SPC = SB / (SEG * (int)sizeof(E));   // segments per chunk
-    constexpr int PER = (SPC + PSTREAM - 1) / PSTREAM;
-    constexpr bool EVEN = SPC % PSTREAM == 0;
+    constexpr int NSW = pstream<E>();
+    constexpr int PER = (SPC + NSW - 1) / NSW;
+    constexpr bool EVEN = SPC % NSW == 0;
     const int nfull = V / SEG;                          // segments wholly inside the row
     const float s = R.s;
     (void)tslot;
@@ -213,7 +214,7 @@ __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned lo
         Raw8<E> raw[PER];
 #pragma unroll
         for (int u = 0; u < PER; u++) {
-            const int jj = sw + u * PSTREAM;
+            const int jj = sw + u * NSW;
             if (EVEN || jj < SPC) raw[u] = ring_raw<E>(buf, jj);
         }
         __syncwarp();
@@ -221,7 +222,7 @@ __device__ __forceinline__ bool stream_row(unsigned long long *full, unsigned lo
         rp.next(pns);
 #pragma unroll
         for (int u = 0; u < PER; u++) {
-            const int jj = sw + u * PSTREAM;
+            const int jj = sw + u * NSW;
             const int seg = c * SPC + jj;
             if ((!EVEN && jj >= SPC) || seg >= nseg) continue;
             bool clean = seg < nfull;

@@ -5,6 +5,12 @@
 namespace sv {
 
 cudaError_t launch_onepass_bf16(const Args &A, cudaStream_t stream, const LaunchOpts &o, bool vec, bool qvec) {
+    if (vec && A.perrow) {
+        // per-row selection (its instances compile in a unit of their own)
+        const cudaError_t e = launch_rows_bf16(A, stream, o, qvec);
+        if (e != cudaErrorNotSupported) return e;
+        cudaGetLastError();   // the vocabulary does not fit the two kernels: the row kernel below
+    }
     return launch_onepass_dtype<uint16_t>(A, stream, o, vec, qvec);
 }
 

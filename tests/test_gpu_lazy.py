@@ -97,6 +97,10 @@ def test_lazy_empty_requests_in_ragged_layout(sv, oracle_lib):
     ro[6] = ro[5]
     w.row_offsets = ro
     w.num_drafts[6] = min(w.k_max, int(ro[7] - ro[6]) - 1)
+    # request 6's draft rows now start one slot early, on the last draft slot of the requests
+    # before it: those leave that slot unused
+    for b in range(5):
+        w.num_drafts[b] = min(int(w.num_drafts[b]), max(0, int(ro[6]) - 6 - (int(ro[b]) - b)))
     s, g, o, db = lazy_compare(oracle_lib, w)
     assert g["accept_len"][5] == -1 and (g["out_tokens"][5] == -1).all() and o["error"][5] == 1
     assert sv.sv_read_device_error(db.workspace)[0] == 1

@@ -101,6 +101,38 @@ def test_zero_drafts_and_padding_rows(sv, oracle_lib):
     full_compare(oracle_lib, w)
 
 
+def test_empty_requests_in_ragged_layout(sv, oracle_lib):
+    """Requests that own no rows in row_offsets get -1 and a layout error, the others verify."""
+    w = W.random_batch(71, B=12, k_max=4, V=3000, dtype="bf16", varlen=True, greedy_frac=0.3)
+    ro = w.row_offsets.copy()
+    ro[6] = ro[5]                  # request 5 owns no rows: its rows go to the front of request 6
+    w.row_offsets = ro
+    w.num_drafts[6] = min(w.k_max, int(ro[7] - ro[6]) - 1)
+    # request 6's draft rows now start one slot early, on the last draft slot of the requests
+    # before it: those leave that slot unused
+    for b in range(5):
+        w.num_drafts[b] = min(int(w.num_drafts[b]), max(0, int(ro[6]) - 6 - (int(ro[b]) - b)))
+    s, g, o, db = full_compare(oracle_lib, w)
+    assert g["accept_len"][5] == -1 and (g["out_tokens"][5] == -1).all() and o["error"][5] == 1
+    assert sv.sv_read_device_error(db.workspace)[0] == 1
+
+
+@pytest.mark.parametrize("pattern", ["all_sampled", "all_greedy", "alternate", "greedy_first_half"])
+def test_streaming_order_mixes(sv, oracle_lib, pattern):
+    """With more rows than the select kernel holds at once (about 1600 here, against 9 per SM on
+    152 SMs), sampled requests stream first and greedy ones last, and each row is selected once its
+    own statistics are complete: every mix of the two (none, all, interleaved, in blocks), over
+    more requests than one block of the order builder takes at a time, ragged and uniform."""
+    for varlen in (True, False):
+        w = W.random_batch(80, B=700 if varlen else 400, k_max=3, V=2048, dtype="bf16", varlen=varlen,
+                           greedy_frac=0.0)
+        assert w.total_rows > 1368
+        idx = np.arange(w.B)
+        w.greedy[:] = {"all_sampled": 0 * idx, "all_greedy": 0 * idx + 1, "alternate": idx % 2,
+                       "greedy_first_half": (idx < w.B // 2)}[pattern].astype(np.uint8)
+        full_compare(oracle_lib, w)
+
+
 def test_q_equals_p_and_disjoint_supports(sv, oracle_lib):
     V, k, B = 64, 4, 40
     g = np.random.default_rng(5)
