@@ -122,7 +122,7 @@ size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V);
  *   draft_tokens   device int32 [total_rows - B]: x_i, the drafted token ids.
  *   num_drafts     device int32 [B]: k_b, 0 <= k_b <= k_max.
  *   row_offsets    device int32 [B+1] (row_offsets[0] = 0, row_offsets[B] = total_rows), or NULL.
- *   B, k_max, V, total_rows: host sizes; 1 <= V <= 2^21, 0 <= k_max <= 64, B >= 1.
+ *   B, k_max, V, total_rows: host sizes; 1 <= V <= 2^21, 0 <= k_max <= 64, 1 <= B < 2^25.
  *   params         per-request sampling parameters (device arrays of length B).
  *   uniforms       device fp32 [total_rows, 2] in [0, 1): slot 0 of row i is the accept test of
  *                  draft i; slot 1 of the row where the request stops is the residual draw (at a

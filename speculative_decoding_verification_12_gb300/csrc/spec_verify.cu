@@ -91,6 +91,9 @@ static cudaError_t current_device(int &dev) {
 // programmatic dependent (the stream kernel) start at once; that kernel waits before use.
 __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const Args A, int order) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#ifdef SV_TIMING
+    if (threadIdx.x == 0) atomicMin(A.timing + (size_t)5 * A.R * NTIME + 4, global_ns());
+#endif
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);
 #ifdef SV_TIMING
@@ -99,6 +102,8 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const 
     if (order && blockIdx.x == 0) build_order<256>(A);
 #ifdef SV_TIMING
     if (order && blockIdx.x == 0 && threadIdx.x == 0) A.timing[(size_t)5 * A.R * NTIME + 1] = global_ns();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(A.timing + (size_t)5 * A.R * NTIME + 5, global_ns());
 #endif
 }
 
@@ -154,7 +159,7 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
                              void *workspace, size_t workspace_bytes, void *stream, bool onehot, bool lazy) {
     if (onehot) draft_probs = nullptr;
     if (B < 1 || k_max < 0 || V < 1 || total_rows < B) return SV_ERR_INVALID_ARG;
-    if (k_max > MAXK || V > MAXV) return SV_ERR_UNSUPPORTED;
+    if (k_max > MAXK || V > MAXV || B >= (1 << 25)) return SV_ERR_UNSUPPORTED;
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (!row_offsets && (long long)total_rows != (long long)B * (k_max + 1)) return SV_ERR_INVALID_ARG;
     const int D = total_rows - B;
@@ -190,7 +195,7 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     A.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     A.jobcnt = reinterpret_cast<int32_t *>(ws + L.jobcnt);
     A.listb = reinterpret_cast<int32_t *>(ws + L.listb);
-    A.jobs = reinterpret_cast<int32_t *>(ws + L.jobs);
+    A.jobs = reinterpret_cast<unsigned long long *>(ws + L.jobs);
     A.jobsum = reinterpret_cast<float *>(ws + L.jobsum);
     A.rowarg = reinterpret_cast<unsigned long long *>(ws + L.rowarg);
     A.prep = reinterpret_cast<int4 *>(ws + L.prep);
@@ -213,6 +218,7 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     A.withhold = g_withhold.load() ? 1 : 0;
     A.phase = 0;
     A.ctas = 0;
+    A.nworkers = 0;
     A.partcnt = reinterpret_cast<int32_t *>(ws + L.partcnt);
     A.ready = reinterpret_cast<uint32_t *>(ws + L.ready);
     A.ordflag = reinterpret_cast<unsigned long long *>(ws + L.order);
@@ -240,6 +246,7 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
     // ends.  With one wave, early select CTAs would only share the SMs with the stream's last
     // units, so every row is selected once the whole stream is done.
     A.perrow = (vec && !lazy && (long long)total_rows > (long long)SEL_PER_SM * nsm) ? 1 : 0;
+
     // clear the error word, the work claim counter, the per-request arrival counters, the
     // per-row part counters and the greedy rows' argmax keys
     {

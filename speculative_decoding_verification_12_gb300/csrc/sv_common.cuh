@@ -62,7 +62,7 @@ constexpr int SELT = SV_SELT;         // threads per select CTA (one row each)
 // select CTAs resident per SM (the select kernel's launch bound: 56 registers a thread)
 constexpr int SEL_PER_SM = SELT >= 128 ? 9 : 1152 / SELT;
 #ifndef SV_PNS_MAX
-#define SV_PNS_MAX 16
+#define SV_PNS_MAX 3
 #endif
 constexpr int PNS_MAX = SV_PNS_MAX;   // ring stages at most (the launch picks what fits)
 #ifndef SV_NRB
@@ -200,7 +200,9 @@ struct Args {
     int32_t *hdr;             // [0] error code, [1] INT_MAX - first bad request, [2] work claim counter,
                               // [3] stream failure flag (a stream CTA gave up on a bounded wait),
                               // [4] lazy scheme: rows queued for phase 2, [5] residual jobs queued,
-                              // [6] phase 2's work claim counter
+                              // [6] phase 2's work claim counter, [7] one-pass select: row CTAs
+                              // done, [8] residual slices claimed by its worker CTAs, [9] rows
+                              // whose kept set is not a candidate list (may need a residual job)
     int32_t *counters;
     unsigned long long *rowarg;   // greedy rows' (max key, ~lowest position), from the stream kernel
     float *gstats;            // per-row segment statistics [R][3][npad] (stream -> select kernel)
@@ -232,7 +234,8 @@ struct Args {
     uint32_t key;             // per-process random tag of ordflag (an old or arbitrary word never matches)
     int32_t *rowmap;          // the row at each position of that order
     int perrow;               // one-pass call: select each row once it is streamed (else once all are)
-    int32_t *jobs;            // residual jobs (request, row), count in hdr[5]
+    int nworkers;             // one-pass call: residual worker CTAs after the select grid's row CTAs
+    unsigned long long *jobs; // residual jobs, count in hdr[5]: epoch << 32 | request << 7 | row
     float *jobsum;            // per job and segment: sum of max(0, p - q), then sum of p
 };
 

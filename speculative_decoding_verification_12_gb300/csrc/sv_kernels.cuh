@@ -201,6 +201,14 @@ static __device__ __noinline__ void drain_copies(unsigned long long *full, int q
 // fp32 rows hold twice the registers per segment: two CTAs per SM instead of SCTA
 template <typename E>
 __host__ __device__ constexpr int stream_ctas() { return sizeof(E) == 2 ? SCTA : (SCTA < 2 ? SCTA : 2); }
+// One-pass calls: finalisers queue their whole-row residual draws, and A.nworkers worker CTAs
+// that follow the row CTAs in the select grid take them slice by slice, instead of the
+// finalising CTA drawing them alone.
+#ifndef SV_RESIDQ
+#define SV_RESIDQ 1
+#endif
+constexpr bool RESIDQ = SV_RESIDQ != 0;
+
 // How the stream and select kernels of a call work together; each has an instance per scheme,
 // which holds none of the others' code.
 enum : int {
@@ -224,6 +232,9 @@ __global__ void __launch_bounds__(stream_threads<E>(), stream_ctas<E>()) stream_
 
     // the select kernel's CTAs may be scheduled as soon as SMs free up
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#ifdef SV_TIMING
+    if (threadIdx.x == 0) atomicMin(A.timing + (size_t)5 * A.R * NTIME + 6, global_ns());
+#endif
     if (threadIdx.x == 0) {
         for (int s = 0; s < PNS; s++) {
             mbar_init(&P.full[s], 1);
@@ -347,6 +358,10 @@ __global__ void __launch_bounds__(stream_threads<E>(), stream_ctas<E>()) stream_
             if (!LAZY || r >= 0) {
                 locate_row(A, R, r);
                 if (R.active) build_penalties(A, R, R.i);
+                // a sampled row whose kept set is not built as a candidate list may end in a
+                // whole-row residual draw: counted once per row for the select grid's workers
+                if (!LAZY && RESIDQ && part == 0 && lane == 0 && R.active && !R.greedy && !A.onehot && R.mode != MODE_TOP2)
+                    atomicAdd(A.hdr + 9, 1);
             } else if (lane == 0) {
                 R.active = 0;   // a first row the request does not have: nothing to stream
             }
@@ -452,14 +467,144 @@ __device__ __forceinline__ void fail_unstreamed_row(const Args &A, int r) {
     }
 }
 
+// Whole-row residual draws that finalisers queued ("Speculative Decoding in Custom LLM
+// Servicing: Implementing Draft Models in Rust", "The Memory Bandwidth Wall and Speculative
+// Math": the residual max(0, p - q), normalised; an empty residual draws from p).  A job is
+// split into RSL slices of the rejected row; a slice is the per-segment sums of max(0, p - q)
+// and of p over its segments, read with many loads in flight, and the job's last slice to
+// finish draws the final token from every slice's sums.
+constexpr int RSL = 8;     // slices per residual job
+constexpr int RST = 256;   // threads per residual kernel CTA
+#ifndef SV_RESID_PER_SM
+#define SV_RESID_PER_SM 8
+#endif
+constexpr int RESID_PER_SM = SV_RESID_PER_SM;   // residual kernel CTAs per SM at most
+
+// Slice p of job j, by the whole group; S (the row context) and rsm (2 np floats) are the
+// group's shared scratch, `last` a shared word.
+template <typename E, bool QVEC, int U, class G>
+__device__ void resid_slice(const G &g, const Args &A, RowCtx &S, float *rsm, int *last, int j, int p) {
+    const unsigned long long w = __ldcg(A.jobs + j);
+    const int b = (int)((w >> 7) & 0x1FFFFFFu), a = (int)(w & 127u);
+    const int V = A.V, nseg = A.nseg, np = nseg_pad(nseg);
+    const int lane = g.lane();
+    const int r = first_row(A, b) + a;   // (a job comes from a finalised request, so b owns rows)
+    g.sync();   // (S and rsm of the group's previous slice are no longer read)
+    if (g.warp() == 0) {
+        locate_row(A, S, r);
+        build_penalties(A, S, a);
+    }
+    g.sync();
+    const RowStat st = load_stat(A.stats + r);
+    const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)r * V;
+    const float *qrow = A.q + (size_t)(S.d0 + a) * V;
+    const WResid wr{st.m, st.s, st.invZ, st.taukey};
+    const WProb wp{st.m, st.s, st.invZ, st.taukey};
+    float *sumr = A.jobsum + (size_t)j * 2 * np, *sump = sumr + np;
+    const int s_lo = (int)((long long)nseg * p / RSL), s_hi = (int)((long long)nseg * (p + 1) / RSL);
+    pass_segment_range<E, true, QVEC, true, U>(
+        g, S, row, qrow, V, s_lo, s_hi, [&](int seg, const float *v, const float *qv) {
+            float x = 0.f, y = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; t++) {
+                if (seg * SEG + lane * 8 + t < V) {
+                    x += wr(v[t], qv[t]);
+                    y += wp(v[t], qv[t]);
+                }
+            }
+            x = warp_sum(x);
+            y = warp_sum(y);
+            if (lane == 0) {
+                sumr[seg] = x;
+                sump[seg] = y;
+            }
+        });
+    g.sync();
+    if (g.t == 0) {
+        __threadfence();
+        *last = atomicAdd(A.jobcnt + j, 1) == RSL - 1;
+    }
+    g.sync();
+    if (!*last) return;
+    __threadfence();
+    for (int t = g.t; t < nseg; t += G::kThreads) {
+        rsm[t] = __ldcg(sumr + t);
+        rsm[np + t] = __ldcg(sump + t);
+    }
+    g.sync();
+    const float u = __ldg(A.uni + (size_t)r * 2 + 1);
+    int tok = draw_by_segments<E, true, QVEC>(g, S, row, qrow, V, nseg, rsm, u, wr);
+    if (tok < 0) tok = draw_by_segments<E, true, QVEC>(g, S, row, nullptr, V, nseg, rsm + np, u, wp);
+    if (g.t == 0) A.out_tok[(size_t)b * (A.k_max + 1) + a] = tok;
+}
+
+#ifndef SV_WORKERS_PER_SM
+#define SV_WORKERS_PER_SM 4
+#endif
+#ifndef SV_WORKER_U
+#define SV_WORKER_U 1
+#endif
+constexpr int WORKERS_PER_SM = SV_WORKERS_PER_SM;
+
+// A worker CTA of the one-pass select grid: claims residual slices in turn, waits (bounded) for
+// the claimed slice's job to be queued, and leaves once every row CTA is done and no slice is
+// left.  Worker CTAs come after every row CTA in the grid and are fewer than the select CTAs an
+// SM holds, so they never keep a row CTA from its slot.
+template <typename E, bool QVEC>
+__device__ void resid_worker(const Grp<SELT, 0> &g, const Args &A, unsigned char *dsm, RowCtx &S) {
+    __shared__ int s_sl, s_go, last;
+    float *rsm = reinterpret_cast<float *>(dsm);
+    const uint32_t *njobs = reinterpret_cast<const uint32_t *>(A.hdr + 5);
+    const uint32_t *rowsdone = reinterpret_cast<const uint32_t *>(A.hdr + 7);
+    // the header counters were cleared before the stream kernel ran, which is done past here
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // With no row that builds its kept set otherwise than as a candidate list, a job can only
+    // come from a candidate overflow: the first worker stays for that, the others leave.
+    if ((int)blockIdx.x != A.R && __ldcg(A.hdr + 9) == 0) return;
+    for (;;) {
+        if (g.t == 0) {
+            const int sl = atomicAdd(A.hdr + 8, 1);
+            int go = 0;
+            const unsigned long long t0 = global_ns();
+            unsigned ns = 64;
+            for (;;) {
+                // (volatile polls; the acquiring loads only once a condition holds)
+                if (sl < (int)*reinterpret_cast<const volatile uint32_t *>(njobs) * RSL) {
+                    go = 1;
+                    break;
+                }
+                if ((int)*reinterpret_cast<const volatile uint32_t *>(rowsdone) >= A.R) {
+                    go = (int)ld_acquire_u32(rowsdone) >= A.R && sl < (int)ld_acquire_u32(njobs) * RSL;
+                    break;
+                }
+                if (global_ns() - t0 > WAIT_NS) {
+                    record_error(A, 7, 0);
+                    break;
+                }
+                __nanosleep(ns);
+                ns = ns < 256 ? ns * 2 : 256;
+            }
+            if (go) {
+                // the job's record follows the reservation of its slot
+                unsigned long long w = 0;
+                go = wait_word(A.jobs + sl / RSL, ld_acquire_u64,
+                               [&](unsigned long long v) { return (uint32_t)(v >> 32) == A.epoch; }, &w);
+                if (!go) record_error(A, 7, 0);
+            }
+            s_sl = sl;
+            s_go = go;
+        }
+        g.sync();
+        if (!s_go) return;
+        resid_slice<E, QVEC, SV_WORKER_U>(g, A, S, rsm, &last, s_sl / RSL, s_sl % RSL);
+    }
+}
+
 // One CTA per row: the row's kept set, draws and draft probabilities from the statistics the
 // stream kernel wrote; the request's last row finalises the request.
 template <typename E, bool QVEC, int SCH>
-__global__ void __launch_bounds__(SELT, SEL_PER_SM) select_kernel(const Args A) {
+__device__ __forceinline__ void select_row_cta(const Grp<SELT, 0> &g, const Args &A, unsigned char *dsm, RowCtx &S) {
     constexpr bool LAZY = SCH == SCH_LAZY, PERROW = SCH == SCH_ROWS;
-    extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ RowCtx S;
-    const Grp<SELT, 0> g(threadIdx.x);
     const int np = nseg_pad(A.nseg);
     float *sb = reinterpret_cast<float *>(dsm);
     const Scratch X = carve_scratch(dsm + up128((size_t)3 * np * 4), np, dsm, select_smem(A.nseg));
@@ -527,7 +672,7 @@ __global__ void __launch_bounds__(SELT, SEL_PER_SM) select_kernel(const Args A) 
     // The CTA of the last position joins the stream grid before it ends, so that this grid
     // (and whatever the stream runs after it) completes after the stream kernel.  That row is
     // streamed last: the join costs the stream kernel's exit, not a wait for the whole stream.
-    const bool join = PERROW && blockIdx.x == gridDim.x - 1;
+    const bool join = PERROW && (int)blockIdx.x == A.R - 1;
     if (!ready) {
         // The row was not (or not surely) streamed: a stream CTA gave up on a wait.  Its request
         // gets -1 outputs and SV_DEV_TIMEOUT, and is never finalised (this row does not arrive).
@@ -554,19 +699,39 @@ __global__ void __launch_bounds__(SELT, SEL_PER_SM) select_kernel(const Args A) 
     if (S.active) select_row<E, true>(g, A, S, X, stats_at(sb, np), A.rowarg + r);
     SV_MARK(A, 4 * A.R + r, 4);
     if (LAZY && A.phase == 1) first_row_decision<E, true, QVEC>(g, A, S, X);
-    else arrive_and_finalize<E, true, QVEC, LAZY>(g, A, S, X);
+    else arrive_and_finalize<E, true, QVEC, LAZY, LAZY || RESIDQ>(g, A, S, X);
     SV_MARK(A, 4 * A.R + r, 5);
 }
 
-// Lazy scheme, last launch: the whole-row residual draws its finalisers queued.  RSL CTAs take
-// a slice of the rejected row each -- the per-segment sums of max(0, p - q) and of p, read
-// with many loads in flight -- and the last slice to finish draws the final token from them
-// ("Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust", "The
-// Memory Bandwidth Wall and Speculative Math": the residual max(0, p - q), normalised; an
-// empty residual draws from p).
-constexpr int RSL = 8;     // CTAs per residual job
-constexpr int RST = 256;   // threads per residual CTA
+template <typename E, bool QVEC, int SCH>
+__global__ void __launch_bounds__(SELT, SEL_PER_SM) select_kernel(const Args A) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ RowCtx S;
+    const Grp<SELT, 0> g(threadIdx.x);
+    if constexpr (SCH != SCH_LAZY && RESIDQ) {
+        if ((int)blockIdx.x >= A.R) {
+            resid_worker<E, QVEC>(g, A, dsm, S);
+            return;
+        }
+    }
+    select_row_cta<E, QVEC, SCH>(g, A, dsm, S);
+    if constexpr (SCH != SCH_LAZY && RESIDQ) {
+        // this row CTA is done; a CTA that queued a residual job releases its reservation with
+        // the count (the only ordering the workers rely on: the job's record is released on its
+        // own), the others count without a fence
+        g.sync();
+        if (g.t == 0) {
+            if (S.last && S.need_resid) {
+                int old;
+                asm volatile("atom.release.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(A.hdr + 7) : "memory");
+            } else {
+                atomicAdd(A.hdr + 7, 1);
+            }
+        }
+    }
+}
 
+// Lazy scheme, last launch: every slice of every queued job, taken in turn by the grid's CTAs.
 template <typename E, bool QVEC>
 __global__ void __launch_bounds__(RST) resid_kernel(const Args A) {
     extern __shared__ __align__(16) float rsm[];   // the job's residual sums, then p sums (np each)
@@ -574,58 +739,15 @@ __global__ void __launch_bounds__(RST) resid_kernel(const Args A) {
     __shared__ int last;
     const Grp<RST, 0> g(threadIdx.x);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int j = blockIdx.x / RSL, p = blockIdx.x % RSL;
-    if (j >= __ldcg(A.hdr + 5)) return;
-    const int b = __ldcg(A.jobs + 2 * j), a = __ldcg(A.jobs + 2 * j + 1);
-    const int V = A.V, nseg = A.nseg, np = nseg_pad(nseg);
-    const int r = first_row(A, b) + a;   // (a job comes from a finalised request, so b owns rows)
-    if (g.warp() == 0) {
-        locate_row(A, S, r);
-        build_penalties(A, S, a);
-    }
-    g.sync();
-    const RowStat st = load_stat(A.stats + r);
-    const E *row = reinterpret_cast<const E *>(A.logits) + (size_t)r * V;
-    const float *qrow = A.q + (size_t)(S.d0 + a) * V;
-    const WResid wr{st.m, st.s, st.invZ, st.taukey};
-    const WProb wp{st.m, st.s, st.invZ, st.taukey};
-    float *sumr = A.jobsum + (size_t)j * 2 * np, *sump = sumr + np;
-    const int lane = g.lane();
-    const int s_lo = (int)((long long)nseg * p / RSL), s_hi = (int)((long long)nseg * (p + 1) / RSL);
-    pass_segment_range<E, true, QVEC, true, sizeof(E) == 2 ? 2 : 1>(
-        g, S, row, qrow, V, s_lo, s_hi, [&](int seg, const float *v, const float *qv) {
-            float x = 0.f, y = 0.f;
-#pragma unroll
-            for (int t = 0; t < 8; t++) {
-                if (seg * SEG + lane * 8 + t < V) {
-                    x += wr(v[t], qv[t]);
-                    y += wp(v[t], qv[t]);
-                }
-            }
-            x = warp_sum(x);
-            y = warp_sum(y);
-            if (lane == 0) {
-                sumr[seg] = x;
-                sump[seg] = y;
-            }
-        });
-    g.sync();
-    if (g.t == 0) {
-        __threadfence();
-        last = atomicAdd(A.jobcnt + j, 1) == RSL - 1;
-    }
-    g.sync();
-    if (!last) return;
-    __threadfence();
-    for (int t = g.t; t < nseg; t += RST) {
-        rsm[t] = __ldcg(sumr + t);
-        rsm[np + t] = __ldcg(sump + t);
-    }
-    g.sync();
-    const float u = __ldg(A.uni + (size_t)r * 2 + 1);
-    int tok = draw_by_segments<E, true, QVEC>(g, S, row, qrow, V, nseg, rsm, u, wr);
-    if (tok < 0) tok = draw_by_segments<E, true, QVEC>(g, S, row, nullptr, V, nseg, rsm + np, u, wp);
-    if (g.t == 0) A.out_tok[(size_t)b * (A.k_max + 1) + a] = tok;
+    const int nslices = __ldcg(A.hdr + 5) * RSL;
+    for (int sl = blockIdx.x; sl < nslices; sl += gridDim.x)
+        resid_slice<E, QVEC, sizeof(E) == 2 ? 2 : 1>(g, A, S, rsm, &last, sl / RSL, sl % RSL);
+}
+
+// CTAs of a residual launch: every slice of every job at most, and a few per SM.
+static unsigned resid_grid(const Args &A, const LaunchOpts &o) {
+    const long long most = (long long)A.B * RSL, few = (long long)o.nsm * RESID_PER_SM;
+    return (unsigned)(most < few ? most : few);
 }
 
 // Opts the kernel into `smem` bytes of dynamic shared memory where it needs more than the
@@ -679,8 +801,11 @@ static bool plan_stream(Args &B, const LaunchOpts &o, StreamPlan &pl) {
     pl.ctas = (long long)o.nsm * stream_ctas<E>();
     B.ctas = (int)pl.ctas;
     // the last wave of rows (one per CTA) is split into parts of at least 2 chunks
+#ifndef SV_PART_MIN
+#define SV_PART_MIN 6
+#endif
     const long long nc = ((long long)B.V * sizeof(E) + SB - 1) / SB;
-    B.nparts = (int)(nc / 2 < SPLIT_PARTS ? nc / 2 : SPLIT_PARTS);
+    B.nparts = (int)(nc / SV_PART_MIN < SPLIT_PARTS ? nc / SV_PART_MIN : SPLIT_PARTS);
     if (B.nparts < 2 || B.R < 2) B.nparts = 1;
     // shared memory of one stream CTA when SCTA share an SM (228 KB, 1 KB reserved per CTA)
     const size_t budget = (stream_ctas<E>() == 1 ? (size_t)232448 : (size_t)233472 / stream_ctas<E>() - 1024) - sizeof(SShared);
@@ -720,7 +845,17 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream, const 
     // a programmatic dependent of the clearing kernel (or of the history prepass)
     if ((e = launch_dependent(k1, stream_grid(B, pl.ctas, A.R), stream_threads<E>(), pl.smem1, stream, B)) != cudaSuccess) return e;
     if (o.ph1 && (e = cudaEventRecord(o.ph1, stream)) != cudaSuccess) return e;
-    return launch_dependent(k2, (unsigned)A.R, SELT, pl.smem2, stream, B);
+    // With queued residuals, the worker CTAs follow the row CTAs: when the rows take one wave
+    // of select CTAs, as many workers as the wave leaves slots for (at least half an SM's
+    // worth), so that no second wave of CTAs ends the kernel; otherwise WORKERS_PER_SM per SM.
+    // Never more than every job's slices.
+    if (RESIDQ && A.R > A.B) {
+        const long long slots = (long long)o.nsm * SEL_PER_SM, most = (long long)A.B * RSL;
+        long long w = A.R <= slots ? slots - A.R : (long long)o.nsm * WORKERS_PER_SM;
+        if (w < o.nsm / 2) w = o.nsm / 2;
+        B.nworkers = (int)(w < most ? w : most);
+    }
+    return launch_dependent(k2, (unsigned)(A.R + B.nworkers), SELT, pl.smem2, stream, B);
 }
 
 // The lazy scheme: both kernels over each request's row 0, both over the rows the first phase
@@ -744,7 +879,7 @@ static cudaError_t launch_lazy_kernels(const Args &A, cudaStream_t stream, const
     B.phase = 2;
     if ((e = launch_dependent(k1, (unsigned)pl.ctas, stream_threads<E>(), pl.smem1, stream, B)) != cudaSuccess) return e;
     if ((e = launch_dependent(k2, (unsigned)(A.R - A.B), SELT, pl.smem2, stream, B)) != cudaSuccess) return e;
-    return launch_dependent(k3, (unsigned)A.B * RSL, RST, pl.smem3, stream, B);
+    return launch_dependent(k3, resid_grid(A, o), RST, pl.smem3, stream, B);
 }
 
 // The one-pass call for logits of type E with whole-grid selection: the two kernels for aligned

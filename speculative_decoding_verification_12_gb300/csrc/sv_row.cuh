@@ -117,7 +117,8 @@ __device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned l
 }
 
 // Waits (one thread, bounded, sleeping between polls) until pred(*p) holds; the word's last
-// value goes to *last.  False once WAIT_NS has passed.
+// value goes to *last.  False once WAIT_NS has passed.  `ld` is an acquiring load; the polls
+// in between are plain volatile reads, so that many waiters do not fence the memory system.
 template <typename T, typename LD, typename PRED>
 __device__ __forceinline__ bool wait_word(const T *p, LD ld, PRED pred, T *last) {
     T v = ld(p);
@@ -127,16 +128,18 @@ __device__ __forceinline__ bool wait_word(const T *p, LD ld, PRED pred, T *last)
     }
     const unsigned long long t0 = global_ns();
     unsigned ns = 32;
-    while (!pred(v = ld(p))) {
+    for (;;) {
         __nanosleep(ns);
         ns = ns < 256 ? ns * 2 : 256;
+        if (pred(*reinterpret_cast<const volatile T *>(p))) {
+            *last = v = ld(p);   // (the condition is monotone: it still holds)
+            return true;
+        }
         if (global_ns() - t0 > WAIT_NS) {
-            *last = v;
+            *last = *reinterpret_cast<const volatile T *>(p);
             return false;
         }
     }
-    *last = v;
-    return true;
 }
 
 // Row at streaming position li (written by the clearing kernel, read through L2).

@@ -946,8 +946,8 @@ __device__ __forceinline__ bool accept_test(float p, float q, float u) {
 // the final token is the stopping row's sample.
 // `lim`: the last row whose statistics exist (the lazy scheme finalises a request that stops at
 // row 0 before its other rows are read); rows past it are never the stopping row.
-// LAZY: the lazy scheme's finaliser, which queues a whole-row residual instead of drawing it.
-template <typename E, bool VEC, bool QVEC, bool LAZY = false, class G>
+// QUEUE: a whole-row residual is queued for the residual kernel instead of drawn here.
+template <typename E, bool VEC, bool QVEC, bool QUEUE = false, class G>
 __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X, int lim = 0x7fffffff) {
     const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
     int *xs = reinterpret_cast<int *>(X.cand);   // the request's draft tokens, for the outputs
@@ -1031,13 +1031,12 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X,
         }
     }
     g.sync();
-    if (LAZY && S.need_resid) {
-        // the lazy scheme queues the whole-row residual for its residual kernel, which draws
-        // the final token (out_tokens[b][a] holds -1 until then)
+    if (QUEUE && S.need_resid) {
+        // the whole-row residual goes to the residual kernel, which draws the final token
+        // (out_tokens[b][a] holds -1 until then)
         if (g.t == 0) {
             const int jj = atomicAdd(A.hdr + 5, 1);
-            A.jobs[2 * jj] = b;
-            A.jobs[2 * jj + 1] = S.a;
+            st_release_u64(A.jobs + jj, ((unsigned long long)A.epoch << 32) | ((uint32_t)b << 7) | (uint32_t)S.a);
         }
     } else if (S.need_resid) {
         // residual max(0, p - q) over a whole row (rows that keep too many tokens for a list)
@@ -1128,7 +1127,7 @@ __device__ __forceinline__ void fail_empty_requests(const G &g, const Args &A, c
 
 // After a row: count it towards its request; the group that brings the count to the
 // request's row count finalises it.  Every thread of the group must call this.
-template <typename E, bool VEC, bool QVEC, bool LAZY = false, class G>
+template <typename E, bool VEC, bool QVEC, bool LAZY = false, bool QUEUE = false, class G>
 __device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X) {
     g.sync();
     if (g.t == 0) {
@@ -1142,7 +1141,7 @@ __device__ __forceinline__ void arrive_and_finalize(const G &g, const Args &A, R
     }
     g.sync();
     if (S.last) {
-        finalize<E, VEC, QVEC, LAZY>(g, A, S, X);
+        finalize<E, VEC, QVEC, QUEUE>(g, A, S, X);
 #ifdef SV_TIMING
         if (g.t == 0) A.timing[(size_t)S.tix * NTIME + 7] = 1;
 #endif
