@@ -351,6 +351,11 @@ __device__ __forceinline__ unsigned long long l2_stream_policy() {
 }
 // One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16) that
 // completes `bytes` of transaction count on `bar`, with an L2 cache policy.
+// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, unsigned long long *bar,
                                          unsigned long long pol) {
     asm volatile(

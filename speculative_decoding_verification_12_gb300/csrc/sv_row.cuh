@@ -532,11 +532,38 @@ __device__ __forceinline__ void seg_values(const RowCtx &S, const E *row, int V,
 // the lane's 8 penalised values; qv: the draft row's 8 values when WITHQ, else zeros).  Each
 // warp takes segments s_lo + warp, s_lo + warp + kWarps, ... and has U of them in flight
 // before it uses any, so a full pass is not one memory latency per segment.
+// With aligned rows, one thread also keeps an L2 prefetch PF_SEGS segments ahead of the
+// warps (of q too when it is read and aligned), so that their loads find the data in L2: a
+// CTA's own loads in flight are far too few to cover the memory latency.
+#ifndef SV_PF_SEGS
+#define SV_PF_SEGS 32
+#endif
+constexpr int PF_SEGS = SV_PF_SEGS;
+
+// Prefetches segments [a, b) of the row (and of q) into L2.  One thread.
+template <typename E, bool QVEC, bool WITHQ>
+__device__ __forceinline__ void prefetch_segs(const E *row, const float *qrow, int V, int a, int b) {
+    const int e0 = a * SEG, e1 = min(b * SEG, V);
+    if (e0 >= e1) return;
+    bulk_prefetch_l2(row + e0, (uint32_t)((e1 - e0) * (int)sizeof(E)));
+    if constexpr (WITHQ && QVEC) {
+        if (qrow) bulk_prefetch_l2(qrow + e0, (uint32_t)((e1 - e0) * 4));
+    }
+}
+
 template <typename E, bool VEC, bool QVEC, bool WITHQ, int U, class G, class F>
 __device__ __forceinline__ void pass_segment_range(const G &g, const RowCtx &S, const E *row, const float *qrow,
                                                    int V, int s_lo, int nseg, F &&f) {
     const int lane = g.lane();
-    for (int s0 = s_lo + g.warp(); s0 < nseg; s0 += G::kWarps * U) {
+    constexpr int STEP = G::kWarps * U;
+    if constexpr (VEC && PF_SEGS > 0) {
+        if (g.t == 0) prefetch_segs<E, QVEC, WITHQ>(row, qrow, V, s_lo, min(s_lo + PF_SEGS, nseg));
+    }
+    for (int s0 = s_lo + g.warp(); s0 < nseg; s0 += STEP) {
+        if constexpr (VEC && PF_SEGS > 0) {
+            // (thread 0 is in warp 0, whose s0 is the step's first segment)
+            if (g.t == 0) prefetch_segs<E, QVEC, WITHQ>(row, qrow, V, s0 + PF_SEGS, min(s0 + PF_SEGS + STEP, nseg));
+        }
         Raw8<E> raw[U];
         float qv[U][8];
 #pragma unroll
