@@ -87,8 +87,9 @@ static cudaError_t current_device(int &dev) {
     return (dev < 0 || dev >= MAX_DEVICES) ? cudaErrorNotSupported : cudaSuccess;
 }
 // Clears n16 16-byte words at p (the workspace header, counters and argmax keys); with
-// `order`, block 0 also builds the one-pass call's streaming order (build_order).  Lets its
-// programmatic dependent (the stream kernel) start at once; that kernel waits before use.
+// `order` (per-row selection) it also zeroes the rows' ready words, and block 0 builds the
+// streaming order (build_order).  Lets its programmatic dependent (the stream kernel) start at
+// once; that kernel waits before use.
 __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const Args A, int order) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #ifdef SV_TIMING
@@ -96,6 +97,10 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const 
 #endif
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);
+    // per-row selection: every row's ready word (a stale word holds an older epoch, never this
+    // call's, and the stream kernel sets none before this grid is done)
+    if (order)
+        for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < A.R; r += gridDim.x * blockDim.x) A.ready[r] = 0u;
 #ifdef SV_TIMING
     if (order && blockIdx.x == 0 && threadIdx.x == 0) A.timing[(size_t)5 * A.R * NTIME + 0] = global_ns();
 #endif

@@ -473,7 +473,10 @@ __device__ __forceinline__ void fail_unstreamed_row(const Args &A, int r) {
 // split into RSL slices of the rejected row; a slice is the per-segment sums of max(0, p - q)
 // and of p over its segments, read with many loads in flight, and the job's last slice to
 // finish draws the final token from every slice's sums.
-constexpr int RSL = 8;     // slices per residual job
+#ifndef SV_RSL
+#define SV_RSL 8
+#endif
+constexpr int RSL = SV_RSL;   // slices per residual job
 constexpr int RST = 256;   // threads per residual kernel CTA
 #ifndef SV_RESID_PER_SM
 #define SV_RESID_PER_SM 8
@@ -539,12 +542,13 @@ __device__ void resid_slice(const G &g, const Args &A, RowCtx &S, float *rsm, in
 }
 
 #ifndef SV_WORKERS_PER_SM
-#define SV_WORKERS_PER_SM 4
+#define SV_WORKERS_PER_SM 8
 #endif
 #ifndef SV_WORKER_U
 #define SV_WORKER_U 1
 #endif
 constexpr int WORKERS_PER_SM = SV_WORKERS_PER_SM;
+static_assert(WORKERS_PER_SM < SEL_PER_SM, "residual workers leave every SM a slot for row CTAs");
 
 // A worker CTA of the one-pass select grid: claims residual slices in turn, waits (bounded) for
 // the claimed slice's job to be queued, and leaves once every row CTA is done and no slice is
@@ -596,7 +600,16 @@ __device__ void resid_worker(const Grp<SELT, 0> &g, const Args &A, unsigned char
         }
         g.sync();
         if (!s_go) return;
+#ifdef SV_TIMING
+        if (g.t == 0) atomicMin(A.timing + (size_t)5 * A.R * NTIME + 8, global_ns());
+#endif
         resid_slice<E, QVEC, SV_WORKER_U>(g, A, S, rsm, &last, s_sl / RSL, s_sl % RSL);
+#ifdef SV_TIMING
+        if (g.t == 0) {
+            atomicMax(A.timing + (size_t)5 * A.R * NTIME + 9, global_ns());
+            atomicAdd(A.timing + (size_t)5 * A.R * NTIME + 10, 1ull);
+        }
+#endif
     }
 }
 
@@ -847,8 +860,9 @@ static cudaError_t launch_two_kernels(const Args &A, cudaStream_t stream, const 
     if (o.ph1 && (e = cudaEventRecord(o.ph1, stream)) != cudaSuccess) return e;
     // With queued residuals, the worker CTAs follow the row CTAs: when the rows take one wave
     // of select CTAs, as many workers as the wave leaves slots for (at least half an SM's
-    // worth), so that no second wave of CTAs ends the kernel; otherwise WORKERS_PER_SM per SM.
-    // Never more than every job's slices.
+    // worth), so that no second wave of CTAs ends the kernel; otherwise WORKERS_PER_SM per SM,
+    // one slot per SM short of the select CTAs an SM holds, so that row CTAs always find slots
+    // whatever order the CTAs are dispatched in.  Never more than every job's slices.
     if (RESIDQ && A.R > A.B) {
         const long long slots = (long long)o.nsm * SEL_PER_SM, most = (long long)A.B * RSL;
         long long w = A.R <= slots ? slots - A.R : (long long)o.nsm * WORKERS_PER_SM;
