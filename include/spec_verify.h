@@ -139,7 +139,13 @@ size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V);
  *                  whenever prior_offsets is (SV_ERR_INVALID_ARG otherwise); a short prepass
  *                  kernel then checks each request's history and indexes it by 256-token
  *                  segment in the workspace.
- *   stream         cudaStream_t.
+ *   stream         cudaStream_t.  The call enqueues its kernels in stream order.  Its first
+ *                  kernel is a programmatic dependent of the work before it on the stream and
+ *                  waits for that work to complete; its last kernel lets the next launch on
+ *                  the stream be scheduled early, so a kernel launched after it with
+ *                  programmatic stream serialization must wait for its prerequisite grid
+ *                  (cudaGridDependencySynchronize) before reading the outputs, as such a kernel
+ *                  always must.  Ordinary launches, copies and events are unaffected.
  *
  * Per row the target distribution is p = softmax(z / T) over the tokens kept by top-k (every
  * token >= the k-th largest, ties kept) and then top-p (tokens whose renormalised mass strictly
@@ -235,8 +241,9 @@ sv_status spec_rollback(int32_t *kv_seq_len, const int32_t *accept_len, const in
 /*
  * spec_verify_static -- spec_verify with a workspace that the library owns.
  *
- * Not part of the method: the sources verify drafts with whatever memory the serving process
- * provides; this entry point exists for callers that cannot provide device memory for a
+ * The paper has no counterpart for this entry point (in place of a citation): its sources
+ * verify drafts with whatever memory the serving process provides.  It exists for callers that
+ * cannot provide device memory for a
  * workspace -- a host program with no device allocator of its own, or code that must not
  * allocate on the verification path.  It allocates nothing: the workspace is a device array of
  * SV_STATIC_WORKSPACE_BYTES (32 MiB) compiled into the library, present once per device.

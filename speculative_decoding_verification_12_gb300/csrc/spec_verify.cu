@@ -91,6 +91,10 @@ static cudaError_t current_device(int &dev) {
 // streaming order (build_order).  Lets its programmatic dependent (the stream kernel) start at
 // once; that kernel waits before use.
 __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const Args A, int order) {
+    // Launched as a programmatic dependent of whatever ran before it on the stream, so that its
+    // CTAs can be resident before that work ends: that work is complete past this wait, and
+    // only then may the stream kernel's CTAs be scheduled.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #ifdef SV_TIMING
     if (threadIdx.x == 0) atomicMin(A.timing + (size_t)5 * A.R * NTIME + 4, global_ns());
@@ -258,9 +262,19 @@ static sv_status verify_call(const void *target_logits, sv_dtype logits_dtype, c
         // (the clear ends below the statistics region, which starts at a 256-byte boundary)
         const size_t n16 = (L.rowarg + (size_t)total_rows * 8 + 15) / 16;
         const unsigned blocks = (unsigned)((n16 + 255) / 256 < 304 ? (n16 + 255) / 256 : 304);
-        // (with per-row selection, block 0 also builds the streaming order)
-        clear_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4 *>(ws), n16, A, A.perrow);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+        // (with per-row selection, block 0 also builds the streaming order).  A programmatic
+        // dependent of the work before it on the stream, which it waits for.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, clear_kernel, reinterpret_cast<uint4 *>(ws), n16, A, A.perrow) != cudaSuccess)
+            return SV_ERR_CUDA;
     }
     if (A.hoff) {
         history_kernel<<<B, 256, 0, st>>>(A, params.prior_len);

@@ -721,6 +721,10 @@ __global__ void __launch_bounds__(SELT, SEL_PER_SM) select_kernel(const Args A) 
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ RowCtx S;
     const Grp<SELT, 0> g(threadIdx.x);
+    // The next launch on the stream may be scheduled now: the next call's clearing kernel
+    // waits for this grid to complete (as any programmatic dependent must before it reads
+    // this call's results), so its launch overlaps this kernel's tail.
+    if constexpr (SCH != SCH_LAZY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if constexpr (SCH != SCH_LAZY && RESIDQ) {
         if ((int)blockIdx.x >= A.R) {
             resid_worker<E, QVEC>(g, A, dsm, S);

@@ -94,6 +94,23 @@ def test_candidate_overflow_falls_back(sv, oracle_lib):
     full_compare(oracle_lib, w)
 
 
+@pytest.mark.parametrize("B", [6, 400])
+def test_overflow_residuals_with_list_rows_only(sv, oracle_lib, B):
+    """Every sampled row asks for a small top-k, so the stream kernel counts no row whose kept
+    set is built otherwise than as a candidate list, and all residual workers but the first
+    leave at once; all-equal rows overflow the candidate buffer all the same, and their
+    rejections queue whole-row residual jobs that the one remaining worker must draw.  B=400
+    (1600 rows) takes per-row selection, B=6 whole-grid selection."""
+    w = W.random_batch(24, B=B, k_max=3, V=2048, dtype="bf16", greedy_frac=0.25)
+    w.target_logits[:] = W.f32_to_bf16_bits(np.full((w.total_rows, w.V), 0.25, np.float32))
+    w.top_k[:] = 12
+    w.top_p[:] = 1.0
+    s, g, o, _ = full_compare(oracle_lib, w)
+    sampled = ~w.greedy.astype(bool)
+    # rejections happened among sampled requests (so residual jobs were drawn)
+    assert ((g["accept_len"] < w.num_drafts) & sampled).any()
+
+
 def test_zero_drafts_and_padding_rows(sv, oracle_lib):
     w = W.random_batch(23, B=30, k_max=5, V=2000, dtype="bf16", greedy_frac=0.3)
     w.num_drafts[::3] = 0          # uniform layout with unused (padding) rows
