@@ -86,9 +86,9 @@ static cudaError_t current_device(int &dev) {
     if (e != cudaSuccess) return e;
     return (dev < 0 || dev >= MAX_DEVICES) ? cudaErrorNotSupported : cudaSuccess;
 }
-// Clears n16 16-byte words at p (the workspace header, counters and argmax keys); with
-// `order` (per-row selection) it also zeroes the rows' ready words, and block 0 builds the
-// streaming order (build_order).  Lets its programmatic dependent (the stream kernel) start at
+// Clears n16 16-byte words at p (the workspace header, counters and argmax keys) and the
+// residual job records; with `order` (per-row selection) block 0 also zeroes the rows' ready
+// words and builds the streaming order (build_order).  Lets its programmatic dependent (the stream kernel) start at
 // once; that kernel waits before use.
 __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const Args A, int order) {
     // Launched as a programmatic dependent of whatever ran before it on the stream, so that its
@@ -101,10 +101,9 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const 
 #endif
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);
-    // per-row selection: every row's ready word (a stale word holds an older epoch, never this
-    // call's, and the stream kernel sets none before this grid is done)
-    if (order)
-        for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < A.R; r += gridDim.x * blockDim.x) A.ready[r] = 0u;
+    // the residual job records: a worker reads a slot only after this grid is done, and then
+    // finds it zero until its job is written (no stale word can pass for one of this call's)
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < A.B; j += gridDim.x * blockDim.x) A.jobs[j] = 0ull;
 #ifdef SV_TIMING
     if (order && blockIdx.x == 0 && threadIdx.x == 0) A.timing[(size_t)5 * A.R * NTIME + 0] = global_ns();
 #endif

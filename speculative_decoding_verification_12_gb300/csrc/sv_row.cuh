@@ -148,8 +148,8 @@ __device__ __forceinline__ int order_row(const Args &A, int li) { return __ldcg(
 // The streaming order of a one-pass call: requests with sampled rows first, greedy ones last
 // (each group in request order), as the row at each position.  A greedy row's selection is
 // short, so rows streamed last finish soon after the stream; the sampled rows' longer
-// selections overlap the greedy rows' streaming.  Run by one block of NT threads; the stream
-// kernel waits for this block.  A request's first
+// selections overlap the greedy rows' streaming.  Run by one block of NT threads, which first
+// zeroes every row's ready word; the stream kernel waits for this block.  A request's first
 // position is the rows of the requests before it in its own group (one block-wide scan per
 // group), after every sampled row when it is greedy.  Publishes key << 32 | 2 * epoch in
 // *ordflag once written, or with + 1 (the identity order) when row_offsets are inconsistent --
@@ -162,6 +162,10 @@ __device__ void build_order(const Args &A) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int B = A.B;
     const unsigned long long tag = (unsigned long long)A.key << 32;
+    // Every row's ready word, zeroed before the flag below publishes the order: a select CTA
+    // reads its row's word only after that flag, so it never sees a stale word, which could
+    // hold any value (the workspace is the caller's memory).
+    for (int r = t; r < A.R; r += NT) A.ready[r] = 0u;
     // the layout's consistency, and the rows of the sampled group
     bool ok = true;
     int samp = 0;

@@ -950,6 +950,9 @@ __device__ __forceinline__ bool accept_test(float p, float q, float u) {
 template <typename E, bool VEC, bool QVEC, bool QUEUE = false, class G>
 __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X, int lim = 0x7fffffff) {
     const int b = S.b, k = S.k, r0 = S.r0, d0 = S.d0, V = A.V;
+#ifdef SV_TIMING
+    if (g.t == 0 && b >= 0 && b < A.B) atomicAdd(A.timing + (size_t)(6 * A.R + b) * NTIME, 1ull);
+#endif
     int *xs = reinterpret_cast<int *>(X.cand);   // the request's draft tokens, for the outputs
     if (g.warp() == 0) {
         // one round of loads: every row's statistics, draft, (p, q) and uniforms at once; the
@@ -1032,12 +1035,7 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X,
     }
     g.sync();
     if (QUEUE && S.need_resid) {
-        // the whole-row residual goes to the residual kernel, which draws the final token
-        // (out_tokens[b][a] holds -1 until then)
-        if (g.t == 0) {
-            const int jj = atomicAdd(A.hdr + 5, 1);
-            st_release_u64(A.jobs + jj, ((unsigned long long)A.epoch << 32) | ((uint32_t)b << 7) | (uint32_t)S.a);
-        }
+        // the whole-row residual is queued below, once the outputs are written
     } else if (S.need_resid) {
         // residual max(0, p - q) over a whole row (rows that keep too many tokens for a list)
         const int a = S.a;
@@ -1062,9 +1060,16 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X,
         if (a >= 0) v = j < a ? xs[j] : (j == a ? S.tok : -1);
         A.out_tok[(size_t)b * kw + j] = v;
     }
-    if (g.t == 0) {
-        A.acc[b] = a;
-        A.counters[b] = 0;
+    if (g.t == 0) A.acc[b] = a;
+    if (QUEUE && S.need_resid) {
+        // The whole-row residual goes to the residual workers (or kernel), which draw the final
+        // token into out_tokens[b][a] (-1 until then).  Queued after the outputs above, which
+        // the barrier orders before the job's release: a worker's token is never overwritten.
+        g.sync();
+        if (g.t == 0) {
+            const int jj = atomicAdd(A.hdr + 5, 1);
+            st_release_u64(A.jobs + jj, ((unsigned long long)A.epoch << 32) | ((uint32_t)b << 7) | (uint32_t)a);
+        }
     }
 }
 

@@ -182,6 +182,33 @@ def test_device_data_errors(sv, oracle_lib):
     assert (g["accept_len"][:5] == -1).all() and (g["accept_len"][5:] >= 0).all()
 
 
+def test_device_data_errors_per_row_selection(sv, oracle_lib):
+    """The same device-data errors, and a request that owns no rows, in a batch of more rows
+    than the select kernel holds at once (per-row selection, streamed in the built order)."""
+    w = W.random_batch(26, B=700, k_max=3, V=2048, dtype="bf16", varlen=True, greedy_frac=0.3)
+    assert w.total_rows > 1368
+    d1 = w.draft_start(1)
+    if w.num_drafts[1] == 0:
+        w.num_drafts[1] = 1
+    w.draft_tokens[d1] = 2048                 # a draft outside the vocabulary
+    w.temperature[2] = -1.0
+    w.greedy[2] = 0
+    w.top_p[3] = 0.0
+    w.greedy[3] = 0
+    w.num_drafts[4] = 9                       # beyond k_max
+    ro = w.row_offsets.copy()
+    ro[301] = ro[300]                         # request 300 owns no rows: request 301 takes them
+    w.row_offsets = ro
+    w.num_drafts[301] = min(w.k_max, int(ro[302] - ro[301]) - 1)
+    for b in range(300):                      # (the draft slot request 301 now starts on)
+        w.num_drafts[b] = min(int(w.num_drafts[b]), max(0, int(ro[301]) - 301 - (int(ro[b]) - b)))
+    s, g, o, db = full_compare(oracle_lib, w)
+    code, bad = sv.sv_read_device_error(db.workspace)
+    assert code != 0
+    assert g["accept_len"][300] == -1 and o["error"][300] != 0
+    assert (g["accept_len"][[2, 3, 4]] == -1).all()
+
+
 def test_deterministic_repeat(sv):
     w = W.random_batch(25, B=40, k_max=6, V=30000, dtype="bf16", varlen=True)
     g1, db = run_gpu(w)
