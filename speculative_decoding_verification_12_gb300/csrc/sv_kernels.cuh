@@ -478,10 +478,6 @@ __device__ __forceinline__ void fail_unstreamed_row(const Args &A, int r) {
 #endif
 constexpr int RSL = SV_RSL;   // slices per residual job
 constexpr int RST = 256;   // threads per residual kernel CTA
-#ifndef SV_RESID_PER_SM
-#define SV_RESID_PER_SM 8
-#endif
-constexpr int RESID_PER_SM = SV_RESID_PER_SM;   // residual kernel CTAs per SM at most
 
 // Slice p of job j, by the whole group; S (the row context) and rsm (2 np floats) are the
 // group's shared scratch, `last` a shared word.
@@ -761,11 +757,9 @@ __global__ void __launch_bounds__(RST) resid_kernel(const Args A) {
         resid_slice<E, QVEC, sizeof(E) == 2 ? 2 : 1>(g, A, S, rsm, &last, sl / RSL, sl % RSL);
 }
 
-// CTAs of a residual launch: every slice of every job at most, and a few per SM.
-static unsigned resid_grid(const Args &A, const LaunchOpts &o) {
-    const long long most = (long long)A.B * RSL, few = (long long)o.nsm * RESID_PER_SM;
-    return (unsigned)(most < few ? most : few);
-}
+// CTAs of a residual launch: one per slice of every job a call can queue (the kernel's loop
+// covers any grid).
+static unsigned resid_grid(const Args &A) { return (unsigned)((long long)A.B * RSL); }
 
 // Opts the kernel into `smem` bytes of dynamic shared memory where it needs more than the
 // default 48 KB.  The opt-in belongs to the kernel in the current context, so it is looked up
@@ -897,7 +891,7 @@ static cudaError_t launch_lazy_kernels(const Args &A, cudaStream_t stream, const
     B.phase = 2;
     if ((e = launch_dependent(k1, (unsigned)pl.ctas, stream_threads<E>(), pl.smem1, stream, B)) != cudaSuccess) return e;
     if ((e = launch_dependent(k2, (unsigned)(A.R - A.B), SELT, pl.smem2, stream, B)) != cudaSuccess) return e;
-    return launch_dependent(k3, resid_grid(A, o), RST, pl.smem3, stream, B);
+    return launch_dependent(k3, resid_grid(A), RST, pl.smem3, stream, B);
 }
 
 // The one-pass call for logits of type E with whole-grid selection: the two kernels for aligned
