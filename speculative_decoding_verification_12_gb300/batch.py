@@ -114,9 +114,10 @@ def bound_call(db: "DeviceBatch", stream, target_logits=None, draft_probs=None, 
                            db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens,
                            db.accept_len, db.out_pq, db.workspace, stream, db.prior)
     else:
-        spec_verify(tl, dp, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k,
-                    db.top_p, db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens, db.accept_len,
-                    db.out_pq, db.workspace, stream, db.prior)
+        (spec_verify_lazy if lazy else spec_verify)(
+            tl, dp, db.draft_tokens, db.num_drafts, db.row_offsets, db.k_max, db.temperature, db.top_k, db.top_p,
+            db.presence, db.frequency, db.greedy, db.uniforms, db.out_tokens, db.accept_len, db.out_pq,
+            db.workspace, stream, db.prior)
     p = lambda t: None if t is None else t.data_ptr()
     ho, ht, hc = db.prior if db.prior is not None else (None, None, None)
     params = SvParams(p(db.temperature), p(db.top_k), p(db.top_p), p(db.presence), p(db.frequency), p(db.greedy),
