@@ -57,6 +57,19 @@ def test_history_random_batches(sv, oracle_lib, case):
     assert s["requests"] >= B - 1
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_history_per_row_selection(sv, oracle_lib, dtype):
+    """Prior histories in a batch of more rows than the select kernel holds at once (1711 rows
+    against 9 per SM on 152 SMs): the history instance of the stream kernel in the per-row
+    scheme, rows streamed in the built order."""
+    w = W.random_batch(79, B=700, k_max=3, V=2048, dtype=dtype, varlen=True, greedy_frac=0.3)
+    assert w.total_rows > 1368
+    w.presence[::2] = np.maximum(w.presence[::2], 0.4)
+    W.with_history(w, 79, 300)
+    s, g, o, _ = full_compare(oracle_lib, w)
+    assert s["requests"] >= w.B - 2
+
+
 def test_history_filters_and_onehot(sv, oracle_lib):
     """Candidate lists, radix select, no filter and greedy rows with a history; then the same
     batch through the one-hot entry point."""

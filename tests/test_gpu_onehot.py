@@ -69,6 +69,17 @@ def test_onehot_random_batches(sv, oracle_lib, case):
         assert (o["accept_len"] > 0).any()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_onehot_per_row_selection(sv, oracle_lib, dtype):
+    """One-hot drafts in a batch of more rows than the select kernel holds at once (per-row
+    selection; no residual job can arise, so every worker but the first leaves at once)."""
+    w = W.random_batch(47, B=700, k_max=3, V=2048, dtype=dtype, varlen=True, greedy_frac=0.3)
+    assert w.total_rows > 1368
+    argmax_drafts(w, 0.8, 47)
+    s, g, o = full_compare(oracle_lib, w)
+    assert (o["accept_len"] > 0).any()
+
+
 def test_onehot_filters_and_fallbacks(sv, oracle_lib):
     """Every kept-set path draws on every row: candidate lists (top-k), radix select (large
     top-k, top-p only), no filter (segment sums), and an all-equal row that overflows the
