@@ -85,8 +85,7 @@ enum : int32_t {
     KIND_GREEDY = 1,   // greedy request: argmax only
     KIND_FULL = 2,     // sampled, no filter: every token kept
     KIND_LIST = 3,     // sampled, kept set small: stored as a list (token, weight) in token order
-    KIND_THRESH = 4,   // sampled, kept set = {z >= tau}, too large for a list
-    KIND_FAIL = 5      // the row's stream did not complete (bounded wait expired)
+    KIND_THRESH = 4    // sampled, kept set = {z >= tau}, too large for a list
 };
 
 // Per-row statistics written by the row's selection and read by the request's finaliser.

@@ -893,24 +893,6 @@ __device__ void select_row(const G &g, const Args &A, RowCtx &S, const Scratch &
     if (g.t == 0) A.stats[row_idx] = st;
 }
 
-// Marks a row whose statistics cannot be trusted (a stream CTA gave up on a bounded wait):
-// its request's finaliser then writes -1 outputs and records SV_DEV_TIMEOUT.  One thread.
-__device__ __forceinline__ void fail_row(const Args &A, const RowCtx &S) {
-    RowStat st;
-    st.m = 0.f; st.s = 0.f; st.tau = -INFINITY; st.Z = 1.f; st.invZ = 1.f; st.taukey = 0;
-    st.argmax = -1; st.bonus = -1; st.kind = KIND_FAIL; st.nlist = 0; st.resid = -1; st.pad1 = 0;
-    A.stats[S.r] = st;
-    if (S.i < S.k) {
-        const size_t d = (size_t)(S.d0 + S.i);
-        A.pq[d * 2] = NAN;
-        A.pq[d * 2 + 1] = NAN;
-        if (A.out_pq) {
-            A.out_pq[d * 2] = NAN;
-            A.out_pq[d * 2 + 1] = NAN;
-        }
-    }
-}
-
 // A RowStat written by another CTA, read through L2.
 __device__ __forceinline__ RowStat load_stat(const RowStat *p) {
     const int4 *q = reinterpret_cast<const int4 *>(p);
@@ -962,7 +944,7 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X,
         int a = -1, tok = -1, need = 0;
         if (status == 0) {
             const bool greedy = S.greedy;
-            bool badtok = false, baduni = false, badrow = false, found = false;
+            bool badtok = false, baduni = false, found = false;
             a = k;
             for (int i0 = 0; i0 <= k; i0 += 32) {
                 const int i = i0 + lane;
@@ -974,7 +956,6 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X,
                     argm = __ldcg(&st->argmax);
                     bonus = __ldcg(&st->bonus);
                     resid = __ldcg(&st->resid);
-                    if (kind == KIND_FAIL) badrow = true;
                 }
                 if (i < k) {
                     const int x = __ldg(A.tokens + d0 + i);
@@ -1016,10 +997,8 @@ __device__ void finalize(const G &g, const Args &A, RowCtx &S, const Scratch &X,
             }
             badtok = __any_sync(0xffffffffu, badtok);
             baduni = __any_sync(0xffffffffu, baduni);
-            badrow = __any_sync(0xffffffffu, badrow);
             if (badtok) status = 2;
             else if (baduni) status = 5;
-            else if (badrow) status = 7;
             if (status != 0) {
                 a = -1;
                 tok = -1;
