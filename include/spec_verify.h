@@ -293,6 +293,30 @@ sv_status sv_set_phase_events(void *stream_kernel_start, void *stream_kernel_end
  * SV_OK.  Never set it in production. */
 sv_status sv_set_test_withhold(int32_t on);
 
+/*
+ * sv_prefer_lazy -- host-side choice between spec_verify and spec_verify_lazy for a batch.
+ *
+ * "Speculative Decoding in Custom LLM Servicing: Implementing Draft Models in Rust", section
+ * "The Verification Algorithm": the loop returns at the first rejection, so spec_verify_lazy
+ * skips the rows after row 0 of every request whose draft 0 is rejected, and pays a second
+ * round of streaming and row selection for the requests that kept it.  Which call is faster
+ * depends on how many requests reject draft 0, which only the caller can estimate (for example
+ * the share of the previous step's requests that returned accept_len 0).  The function weighs
+ * the two with a cost model fitted to both calls timed on a GB300: the skipped rows save their
+ * bytes at 6.8 TB/s; the second round costs 10.3 us + 0.146 ns per vocabulary entry; with every
+ * request rejecting draft 0 there is no second round.  Near the crossover the model leans to
+ * spec_verify: it does not count the whole-row residual draws of rejected rows, which the
+ * one-pass call pays more for.
+ *
+ *   B, total_rows, V, logits_dtype: the batch's sizes and logits type, as for spec_verify.
+ *   row0_reject_share: the expected share, in [0, 1], of the B requests whose draft 0 is
+ *                  rejected.
+ * Returns 1 when spec_verify_lazy is expected to be the faster call, 0 when spec_verify is, and
+ * -1 for invalid arguments (sizes as sv_workspace_bytes rejects them, an unknown dtype, a share
+ * outside [0, 1] or NaN).  Host computation only: no device access, thread-safe.
+ */
+int32_t sv_prefer_lazy(int32_t B, int32_t total_rows, int32_t V, sv_dtype logits_dtype, float row0_reject_share);
+
 /* Human-readable name of a status code. */
 const char *sv_status_string(sv_status s);
 

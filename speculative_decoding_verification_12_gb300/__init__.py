@@ -67,6 +67,8 @@ def lib():
         l.sv_set_test_withhold.argtypes = [C.c_int32]
         l.sv_set_phase_events.restype = C.c_int
         l.sv_set_phase_events.argtypes = [C.c_void_p, C.c_void_p]
+        l.sv_prefer_lazy.restype = C.c_int32
+        l.sv_prefer_lazy.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int, C.c_float]
         l.sv_status_string.restype = C.c_char_p
         l.sv_status_string.argtypes = [C.c_int]
         _lib = l
@@ -100,6 +102,18 @@ def _check(t, name, dtype=None, numel=None):
 
 def sv_workspace_bytes(B: int, total_rows: int, V: int) -> int:
     return int(lib().sv_workspace_bytes(B, total_rows, V))
+
+
+def sv_prefer_lazy(B: int, total_rows: int, V: int, dtype, row0_reject_share: float) -> bool:
+    """Whether spec_verify_lazy is expected to beat spec_verify on this batch, given the expected
+    share of requests whose draft 0 is rejected.  dtype: SV_BF16 / SV_F32 or a torch dtype."""
+    if not isinstance(dtype, int):
+        import torch
+        dtype = SV_BF16 if dtype == torch.bfloat16 else SV_F32 if dtype == torch.float32 else -1
+    r = int(lib().sv_prefer_lazy(B, total_rows, V, dtype, row0_reject_share))
+    if r < 0:
+        raise SvError(SV_ERR_INVALID_ARG, "sv_prefer_lazy")
+    return r == 1
 
 
 def _checked_args(target_logits, draft_probs, draft_tokens, num_drafts, row_offsets, k_max, temperature, top_k,

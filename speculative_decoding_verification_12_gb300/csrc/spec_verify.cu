@@ -146,6 +146,28 @@ extern "C" size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V) {
     return ws_layout(B, total_rows, V).total;
 }
 
+// Cost model of sv_prefer_lazy, fitted to one-pass and lazy calls timed on a GB300 over batches
+// whose share of requests rejecting draft 0 was set from 0 to 1: the lazy call saves the bytes
+// of the rows it skips at about the copy rate, and its second phase (a second stream launch and
+// a second round of row selection) costs a fixed time that grows with the vocabulary.
+constexpr double LAZY_SKIP_BYTES_PER_US = 6.8e6;   // 6.8 TB/s
+constexpr double LAZY_PHASE2_US = 10.3;
+constexpr double LAZY_PHASE2_US_PER_TOKEN = 1.46e-4;
+
+extern "C" int32_t sv_prefer_lazy(int32_t B, int32_t total_rows, int32_t V, sv_dtype logits_dtype,
+                                  float row0_reject_share) {
+    if (B < 1 || total_rows < B || V < 1 || (logits_dtype != SV_F32 && logits_dtype != SV_BF16) ||
+        !(row0_reject_share >= 0.f && row0_reject_share <= 1.f))
+        return -1;
+    // every request decided at row 0: the lazy call has no second phase
+    if (row0_reject_share >= 1.f) return 1;
+    const double esz = logits_dtype == SV_BF16 ? 2.0 : 4.0;
+    const double skipped = (double)row0_reject_share * (double)(total_rows - B) * (double)V * esz;
+    const double saved_us = skipped / LAZY_SKIP_BYTES_PER_US;
+    const double phase2_us = LAZY_PHASE2_US + LAZY_PHASE2_US_PER_TOKEN * (double)V;
+    return saved_us > phase2_us ? 1 : 0;
+}
+
 extern "C" const char *sv_status_string(sv_status s) {
     switch (s) {
         case SV_OK: return "ok";

@@ -101,6 +101,39 @@ def test_host_checks_reject_bad_calls(libsv):
     assert l.sv_set_phase_events(None, None) == libsv.SV_OK
 
 
+def test_prefer_lazy_choice(libsv):
+    """sv_prefer_lazy on the measured batch shapes (bf16 unless noted).  Both calls were timed
+    on a GB300 with the share of requests rejecting draft 0 set to 0, 1/4, 1/2, 3/4 and 1: the
+    lazy call won on the 64-request V=32000 batch only at share 1; on the 256-request V=128256
+    batch from about 3/4 on; on the ragged 512-request V=151936 batch from about 1/4 on (by 25 us
+    at 0.44); and on the 1024-request fp32 batch at its natural share (about 0.26)."""
+    pick = libsv.sv_prefer_lazy
+    for share in (0.0, 0.5, 0.75, 0.95):
+        assert not pick(64, 384, 32000, libsv.SV_BF16, share)
+    assert pick(64, 384, 32000, libsv.SV_BF16, 1.0)
+    assert not pick(256, 1280, 128256, libsv.SV_BF16, 0.5)
+    assert pick(256, 1280, 128256, libsv.SV_BF16, 0.9)
+    assert not pick(512, 2510, 151936, libsv.SV_BF16, 0.1)
+    assert pick(512, 2510, 151936, libsv.SV_BF16, 0.44)
+    assert pick(1024, 8192, 128256, libsv.SV_F32, 0.26)
+    assert not pick(1024, 8192, 128256, libsv.SV_F32, 0.01)
+    # one switch from the one-pass call to the lazy call as the share grows
+    for shape in ((64, 384, 32000), (256, 1280, 128256), (512, 2510, 151936), (1024, 8192, 128256)):
+        got = [pick(*shape, libsv.SV_BF16, s / 100) for s in range(101)]
+        assert got == sorted(got), shape
+    # fp32 rows skip twice the bytes of bf16 rows
+    assert pick(256, 1280, 128256, libsv.SV_F32, 0.5) and not pick(256, 1280, 128256, libsv.SV_BF16, 0.5)
+    l = libsv.lib()
+    assert l.sv_prefer_lazy(0, 10, 100, libsv.SV_BF16, 0.5) == -1
+    assert l.sv_prefer_lazy(4, 3, 100, libsv.SV_BF16, 0.5) == -1
+    assert l.sv_prefer_lazy(4, 20, 0, libsv.SV_BF16, 0.5) == -1
+    assert l.sv_prefer_lazy(4, 20, 100, 7, 0.5) == -1
+    assert l.sv_prefer_lazy(4, 20, 100, libsv.SV_BF16, 1.5) == -1
+    assert l.sv_prefer_lazy(4, 20, 100, libsv.SV_BF16, float("nan")) == -1
+    with pytest.raises(libsv.SvError):
+        pick(4, 20, 100, libsv.SV_BF16, -0.1)
+
+
 def test_package_has_no_cpu_fallback():
     """The binding never imports the oracle or a CPU implementation."""
     pkg = os.path.join(ROOT, "speculative_decoding_verification_12_gb300")
