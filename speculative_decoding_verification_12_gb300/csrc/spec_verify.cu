@@ -88,14 +88,20 @@ static cudaError_t current_device(int &dev) {
 }
 // Clears n16 16-byte words at p (the workspace header, counters and argmax keys) and the
 // residual job records; with `order` (per-row selection) block 0 also zeroes the rows' ready
-// words and builds the streaming order (build_order).  Lets its programmatic dependent (the stream kernel) start at
-// once; that kernel waits before use.
+// words and builds the streaming order (build_order).  Lets its programmatic dependent (the
+// stream kernel) be scheduled early; that kernel waits for this grid before it reads or writes
+// anything.
 __global__ void __launch_bounds__(256) clear_kernel(uint4 *p, size_t n16, const Args A, int order) {
     // Launched as a programmatic dependent of whatever ran before it on the stream, so that its
-    // CTAs can be resident before that work ends: that work is complete past this wait, and
-    // only then may the stream kernel's CTAs be scheduled.
+    // CTAs can be resident before that work ends.  Every CTA of that work has started by then
+    // (a dependent launches only once each CTA of its primary has triggered or exited), so the
+    // stream kernel's CTAs, once scheduled, can keep none of it from running; they wait for
+    // this grid, and so for that work, before their first access.  With per-row selection they
+    // are let in at once, to take SMs as the work before frees them; otherwise only once that
+    // work is done (measured the faster order for each scheme).
+    if (order) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!order) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #ifdef SV_TIMING
     if (threadIdx.x == 0) atomicMin(A.timing + (size_t)5 * A.R * NTIME + 4, global_ns());
 #endif
