@@ -218,6 +218,39 @@ def test_deterministic_repeat(sv):
         assert np.array_equal(g1[key], g2[key], equal_nan=True), key
 
 
+@pytest.mark.parametrize("rows", ["one_wave", "many_rows"])
+def test_back_to_back_calls_share_a_workspace(sv, rows):
+    """Calls queued back to back on one stream, sharing one workspace, with no synchronisation
+    between them: one-pass, lazy, one-pass, one-pass again.  Each gives what it gives alone: a
+    call's clearing kernel waits for the call before it, and its stream kernel for the clearing
+    kernel, whether that kernel lets it in before or after its own wait (per-row selection
+    above 9 rows per SM, whole-grid selection below; the lazy call's clear always after)."""
+    from speculative_decoding_verification_12_gb300.batch import DeviceBatch
+    B = 60 if rows == "one_wave" else 400
+    ws = [W.random_batch(90 + i, B=B, k_max=4, V=4096, dtype="bf16", varlen=False, greedy_frac=0.3)
+          for i in range(3)]
+    assert (ws[0].total_rows > 9 * 152) == (rows == "many_rows")
+    dbs = [DeviceBatch.from_host(w, "cuda") for w in ws]
+    solo = []
+    for j, db in enumerate(dbs):
+        db.run(lazy=(j == 1))
+        solo.append(db.results())
+    shared = dbs[0].workspace
+    for db in dbs:
+        db.workspace = shared
+        db.out_tokens.fill_(-7)
+        db.accept_len.fill_(-7)
+        db.out_pq.fill_(-7.0)
+    dbs[0].run()
+    dbs[1].run(lazy=True)
+    dbs[2].run()
+    dbs[0].run()
+    for j, db in enumerate(dbs):
+        got = db.results()
+        for key in solo[j]:
+            assert np.array_equal(got[key], solo[j][key], equal_nan=True), (j, key)
+
+
 def test_unaligned_pointers(sv, oracle_lib):
     """Logit and draft rows that start off a 16-byte boundary take the scalar-load path."""
     from speculative_decoding_verification_12_gb300.batch import DeviceBatch
