@@ -154,6 +154,9 @@ size_t sv_workspace_bytes(int32_t B, int32_t total_rows, int32_t V);
  * request's prior history (params.prior_*, optional).  A draft is accepted iff
  * p > 0 and (q == 0 or u < min(1, p/q)).  Draws use the inverse CDF in token-id order.
  * Arithmetic is fp32 (exp via ex2); a greedy row's argmax breaks ties toward the lowest id.
+ * A logit of -inf masks its token: weight 0 under every filter, so it is never accepted
+ * (p = 0) or drawn.  A row whose logits are all -inf has no distribution, and the results of
+ * its request are unspecified.
  */
 sv_status spec_verify(const void *target_logits, sv_dtype logits_dtype, const float *draft_probs,
                       const int32_t *draft_tokens, const int32_t *num_drafts, const int32_t *row_offsets,

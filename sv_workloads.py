@@ -363,6 +363,34 @@ def with_argmax_drafts(w: Workload) -> Workload:
     return w
 
 
+def with_masked_vocab(w: Workload, seed: int, frac: float, keep: int = 3) -> np.ndarray:
+    """Masks tokens out of the target rows, as a constrained-decoding mask does: each logit is
+    set to -inf with probability frac, and each 256-token segment wholly with probability
+    frac / 2; `keep` random tokens of every row stay finite.  A third of the drafts are moved
+    onto masked tokens of their row, and half of the rest onto finite ones.  Modifies w in
+    place; returns the mask [R, V] (True: masked)."""
+    r = np.random.default_rng(np.random.Philox(key=np.array([8_000_000 + seed, 0], dtype=np.uint64)))
+    R, V = w.total_rows, w.V
+    m = r.random((R, V)) < frac
+    nseg = (V + 255) // 256
+    for row in range(R):
+        for sg in np.nonzero(r.random(nseg) < frac / 2)[0]:
+            m[row, sg * 256:(sg + 1) * 256] = True
+        m[row, r.choice(V, size=min(keep, V), replace=False)] = False
+    if w.dtype == "bf16":
+        w.target_logits[m] = np.uint16(0xFF80)
+    else:
+        w.target_logits[m] = -np.inf
+    for b in range(w.B):
+        r0, d0 = w.row_start(b), w.draft_start(b)
+        for i in range(int(w.num_drafts[b])):
+            x = r.random()
+            pool = np.nonzero(m[r0 + i])[0] if x < 1 / 3 else (np.nonzero(~m[r0 + i])[0] if x < 2 / 3 else None)
+            if pool is not None and len(pool):
+                w.draft_tokens[d0 + i] = int(r.choice(pool))
+    return m
+
+
 def layout(name: str):
     """(num_drafts, row_offsets or None, total_rows, total_drafts) of a full workload, cheaply."""
     sp = spec(name)
