@@ -150,6 +150,23 @@ def test_streaming_order_mixes(sv, oracle_lib, pattern):
         full_compare(oracle_lib, w)
 
 
+@pytest.mark.parametrize("mode", ["u_zero", "u_top", "t_small", "t_large"])
+def test_extreme_uniforms_and_temperatures(sv, oracle_lib, mode):
+    """Uniforms at both ends of [0, 1) (u = 0 keeps every draft with p > 0 and draws the first
+    token of positive weight; u just below 1 draws from the top of the CDF) and temperatures of
+    1e-3 (nearly one-hot rows) and 50 (nearly flat rows)."""
+    w = W.random_batch(31, B=24, k_max=4, V=5000, dtype="bf16", varlen=True, greedy_frac=0.2)
+    if mode == "u_zero":
+        w.uniforms[:] = 0.0
+    elif mode == "u_top":
+        w.uniforms[:] = np.nextafter(np.float32(1), np.float32(0))
+    elif mode == "t_small":
+        w.temperature[:] = np.float32(1e-3)
+    else:
+        w.temperature[:] = np.float32(50.0)
+    full_compare(oracle_lib, w)
+
+
 def test_q_equals_p_and_disjoint_supports(sv, oracle_lib):
     V, k, B = 64, 4, 40
     g = np.random.default_rng(5)
