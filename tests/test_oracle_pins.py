@@ -456,6 +456,48 @@ def test_inverse_cdf_never_picks_zero_weight(oracle_lib):
     assert r["accept_len"][0] == 1 and list(r["out_tokens"][0]) == [3, 2]
 
 
+def test_masked_tokens_have_no_mass(oracle_lib):
+    """Logits of -inf (a constrained-decoding mask): weight exp(-inf) = 0 under every filter, so
+    a draft on a masked token has p = 0 and is rejected, the residual max(0, p - q) puts no mass
+    on masked tokens, and a top-k whose k-th largest value is -inf keeps the whole row.  Pinned
+    against the filters' brute-force definitions and the residual's inverse CDF written out."""
+    V = 8
+    z = np.array([1.0, -np.inf, 2.0, -np.inf, 0.5, -np.inf, -np.inf, 3.0], np.float32)
+    q = np.array([0.05, 0.3, 0.1, 0.2, 0.05, 0.1, 0.1, 0.1], np.float32)
+    T = 0.7
+    grid = (np.arange(64, dtype=np.float32) + np.float32(0.37)) / np.float32(64)
+    checked = 0
+    for K, P in [(0, 1.0), (2, 1.0), (6, 1.0), (0, 0.8), (6, 0.9)]:
+        # (temperature and top_p reach the oracle as fp32 values)
+        p = _brute_filter(z.astype(np.float64), float(np.float32(T)), K, float(np.float32(P)))
+        assert p[~np.isfinite(z)].sum() == 0
+        for x in (0, 2, 7):
+            w = W.from_rows(V, np.tile(z, (2, 1)), q[None], np.array([[x]]),
+                            np.array([[[0.999, 0.5], [0.5, 0.5]]], np.float32), temperature=T, top_k=K, top_p=P)
+            r = oracle_lib.verify(w)
+            assert abs(r["pq"][0, 0] - p[x]) < 1e-12, (K, P, x)
+        res = np.maximum(p - q.astype(np.float64), 0.0)
+        c = np.cumsum(res)
+        for u in grid:
+            t = np.float64(u) * c[-1]
+            if np.min(np.abs(c - t)) < 1e-9:
+                continue                          # a near-tie of the draw: either token is right
+            w = W.from_rows(V, np.tile(z, (2, 1)), q[None], np.array([[1]]),
+                            np.array([[[0.0, u], [0.5, 0.5]]], np.float32), temperature=T, top_k=K, top_p=P)
+            r = oracle_lib.verify(w)
+            assert r["accept_len"][0] == 0 and r["pq"][0, 0] == 0.0
+            want = int(np.argmax(c > t))
+            assert r["out_tokens"][0, 0] == want and np.isfinite(z[want]), (K, P, float(u))
+            checked += 1
+    assert checked > 250
+    # greedy: the argmax among the finite logits
+    for x, a, last in ((7, 1, 7), (2, 0, 7), (3, 0, 7)):
+        w = W.from_rows(V, np.tile(z, (2, 1)), q[None], np.array([[x]]),
+                        np.array([[[0.5, 0.5], [0.5, 0.5]]], np.float32), greedy=1)
+        r = oracle_lib.verify(w)
+        assert r["accept_len"][0] == a and r["out_tokens"][0, a] == last
+
+
 # ------------------------------------------------------------------------------------------
 # P9: the one-hot-draft scheme (FreeToken PR #836, Design: drafts are argmax proposals, so
 # every verify row is sampled as decode would sample it and the matching prefix is kept)
