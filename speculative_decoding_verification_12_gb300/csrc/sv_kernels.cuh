@@ -314,9 +314,13 @@ __global__ void __launch_bounds__(stream_threads<E>(), stream_ctas<E>()) stream_
             // writes to this warp): publish it as one share of its row.  The scheduler, not each
             // streamer warp, pays the fence, and it waits on exactly this unit anyway.
             if (PERROW && j >= NRB && lane == 0) row_share_done(A, R.r, R.nparts);
+            // With whole-grid selection each CTA's first unit is unit blockIdx.x and the counter
+            // hands out the rest (one contended atomic fewer before the first copies); the lazy
+            // scheme's second phase claims from a counter of its own.
+            constexpr bool FIXED_FIRST = SCH == SCH_GRID;
             int u = 0;
-            // (the lazy scheme's second phase claims from a counter of its own)
-            if (lane == 0) u = atomicAdd(A.hdr + (LAZY && A.phase == 2 ? 6 : 2), 1);
+            if (FIXED_FIRST && j == 0) u = (int)blockIdx.x;
+            else if (lane == 0) u = (FIXED_FIRST ? (int)gridDim.x : 0) + atomicAdd(A.hdr + (LAZY && A.phase == 2 ? 6 : 2), 1);
             u = __shfl_sync(0xffffffffu, u, 0);
             if (u >= units) {
                 if (lane == 0) {
