@@ -34,7 +34,7 @@ METRIC = "verify rows/s and achieved HBM GB/s (% of GB300 roofline) vs CPU oracl
 # DRAM bytes (read + write) of one stream-kernel launch on the full batch, from the ncu capture
 # summarised under profiles/ (a 160-request cut, scaled by rows).  Valid only for the kernel as
 # captured; absent (null) otherwise.
-TRAFFIC_STREAM_KERNEL = {"b256_k4_v128256_bf16_zipf": 335.8e6}
+TRAFFIC_STREAM_KERNEL = {"b256_k4_v128256_bf16_zipf": 335.3e6}
 DEFAULT_WORKLOAD = "b256_k4_v128256_bf16_zipf"
 
 
