@@ -70,3 +70,25 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch, capsys):
         workload, steps, warmup, gpus, scheme = "tiny", 1, 3, 2, "accept"
     assert bench.run_reference(Args()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm prints one JSON line: the oracle timed on the host cores, on
+    the same metric and workload as the CUDA arm, with its sample and a zero-copy e2e."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "0")
+
+    class Args:
+        workload, steps, warmup, gpus, scheme = "tiny", 2, 3, 1, "accept"
+    bench.run_reference(Args(), budget_s=2.0)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "rows/s"
+    assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cores"] >= 1 and "requests" in d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("tiny")
